@@ -1,0 +1,66 @@
+"""Regression fixture of the oracle, and properties of the seeded generator."""
+import hashlib
+import json
+import os
+
+import numpy as np
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "oracle_m128_seed0_rows0-7.json")
+
+
+def _digest(a):
+    return hashlib.sha256(np.ascontiguousarray(a).tobytes()).hexdigest()
+
+
+def test_oracle_matches_stored_regression_fixture(oracle_mod):
+    with open(GOLDEN) as f:
+        g = json.load(f)
+    rows = g["inputs"]["rows"]
+    R = synth.residual(0, rows)
+    y = synth.sublayer_out(0, rows)
+    assert _digest(R) == g["inputs"]["R_sha256"]       # generator is stable across machines
+    assert _digest(y) == g["inputs"]["y_sha256"]
+    W = synth.weights(0)
+    o = oracle_mod.pre(R, W.fn, W.scale, W.base, W.norm_w)
+    np.testing.assert_allclose(o["mix"], g["mix"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(o["pre"], g["pre"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(o["post"], g["post"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(o["comb"], g["comb"], rtol=1e-12, atol=1e-13)
+    assert _digest(o["x_norm"]) == g["x_norm_sha256"]
+    r_out = oracle_mod.post(R, y, o["post"].astype(np.float32), o["comb"].astype(np.float32))
+    assert _digest(r_out) == g["r_out_sha256"]
+
+
+def test_generator_is_counter_based_and_sliceable():
+    # rows drawn alone equal the same rows drawn inside a larger call
+    full = synth.residual(3, 40)
+    part = synth.residual(3, 7, row0=21)
+    np.testing.assert_array_equal(full[21:28], part)
+    yf = synth.sublayer_out(3, 30)
+    np.testing.assert_array_equal(yf[10:13], synth.sublayer_out(3, 3, row0=10))
+
+
+def test_generator_distributions():
+    R = synth.bf16_bits_to_f32(synth.residual(1, 64)).astype(np.float64)
+    assert abs(R[:, :, 64:].std() - 0.5) < 0.01
+    assert abs(R[:, :, :64].std() - 20.0) < 0.5
+    assert abs(R.mean()) < 0.05
+    W = synth.weights(1)
+    assert abs(W.fn.std() - 0.0225) < 2e-4
+    assert W.scale.min() >= 0.01 and W.scale.max() <= 0.06
+    w = synth.bf16_bits_to_f32(W.norm_w)
+    assert abs(w.mean() - 1.0) < 0.01 and abs(w.std() - 0.1) < 0.01
+    u = synth.uniform(9, 1, 200000)
+    assert 0 < u.min() and u.max() < 1 and abs(u.mean() - 0.5) < 0.005
+    n = synth.normal(9, 2, 200000)
+    assert abs(n.mean()) < 0.01 and abs(n.std() - 1) < 0.01
+
+
+def test_bf16_bit_helpers_round_trip():
+    x = np.array([1.0, -2.5, 3.14159, 1e-30, 65504.0], np.float32)
+    b = synth.f32_to_bf16_bits(x)
+    np.testing.assert_allclose(synth.bf16_bits_to_f32(b), x, rtol=2 ** -8)
+    np.testing.assert_array_equal(synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(b)), b)
