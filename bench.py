@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Throughput of the mHC hot path (mhc_pre + mhc_post) on GB300.
+
+One step = mhc_pre then mhc_post over one M=16384-row chunk of the residual
+R[M,4,5120] (the prefill-chunk workload), with synthetic seeded inputs
+already resident in HBM.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mhc|reference]
+
+Multi-GPU (torchrun): rows are independent, so every rank runs its own
+16384-row chunk (weak scaling) with no collective on the data path; a barrier
+and a max-over-ranks of the elapsed time bracket the timed region.
+--impl reference times the CPU oracle (the deliberately slow reference arm)
+on a bounded sample of rows per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "mHC pre+post rows/s and achieved HBM GB/s (% of GB300 peak) at M=16384"
+HC, H, K, MIX = 4, 5120, 20480, 24
+ROWS = 16384
+SEED = 4
+# algorithmic HBM bytes: pre reads R and writes x_norm/post/comb; post reads
+# R/y/post/comb and writes R'.  Per call, fn (fp32), scale, base, norm_w once.
+PRE_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4          # 51,280
+POST_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4 + K * 2  # 92,240
+PRE_BYTES_CALL = MIX * K * 4 + H * 2 + 3 * 4 + MIX * 4         # fn, norm_w, scale, base
+PRE_LAUNCHES, POST_LAUNCHES = 3, 1                             # kernels per call
+DOMINANT_SRC = {"mhc_pre": ["pre_simt.cu"], "mhc_post": ["post.cu"]}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def src_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "hyper_connection_residual_mhc_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[kernel]
+    except Exception:
+        return None
+    if t.get("src_sha256_16") != src_hash(DOMINANT_SRC[kernel]):
+        return None
+    return t.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.path = index, None, None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.path or not os.path.exists(self.path):
+            return out
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sms.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if sms:
+            out.update(sm_mhz=statistics.median(sms), sm_max_mhz=mx, reasons=sorted(reasons),
+                       samples=len(sms))
+        return out
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def oracle_rows_per_s(R, y, W, rows, threads):
+    """Oracle pre+post on the first `rows` rows, row blocks spread over threads."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    oracle.build()
+    blk = 8
+    spans = [(lo, min(rows, lo + blk)) for lo in range(0, rows, blk)]
+
+    def one(span):
+        lo, hi = span
+        o = oracle.pre(R[lo:hi], W.fn, W.scale, W.base, W.norm_w)
+        oracle.post(R[lo:hi], y[lo:hi], o["post"].astype(np.float32), o["comb"].astype(np.float32))
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, spans))
+    return rows / (time.perf_counter() - t0)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    R = synth.residual(SEED, 512)
+    y = synth.sublayer_out(SEED, 512)
+    W = synth.weights(SEED)
+    # ~25 ms of CPU per row for pre+post: size the per-step sample so the whole
+    # run stays around two minutes of wall time.
+    per_step = int(max(threads, min(512, 120.0 * threads / 0.025 / max(1, args.steps + args.warmup))))
+    per_step = max(1, per_step // threads * threads)
+    for _ in range(args.warmup):
+        oracle_rows_per_s(R, y, W, per_step, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_rows_per_s(R, y, W, per_step, threads)
+    dt = time.perf_counter() - t0
+    v = per_step * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"M={ROWS} rows of R[M,4,5120] bf16 (seed {SEED}); "
+                               f"each step the CPU oracle on the first {per_step} rows"},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} rows per step, {args.steps} steps"},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_mhc(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import hyper_connection_residual_mhc_gb300 as m
+    from hyper_connection_residual_mhc_gb300 import build as b
+    b.build()
+    m.lib()
+
+    M = ROWS
+    row0 = rank * M                      # each rank: its own chunk of rows
+    Rh = synth.residual(SEED, M, row0=row0)
+    yh = synth.sublayer_out(SEED, M, row0=row0)
+    W = synth.weights(SEED)
+
+    dev = torch.device("cuda", local)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    R = bf(Rh).to(dev)
+    y = bf(yh).to(dev)
+    fn = torch.from_numpy(W.fn).to(dev)
+    scale = torch.from_numpy(W.scale).to(dev)
+    base = torch.from_numpy(W.base).to(dev)
+    w = bf(W.norm_w).to(dev)
+    xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    post = torch.empty((M, HC), dtype=torch.float32, device=dev)
+    comb = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
+    R2 = torch.empty_like(R)
+    ws = torch.empty((max(1, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        m.mhc_pre(R, fn, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn, post=post,
+                  comb=comb, stream=stream)
+        m.mhc_post(R, y, post, comb, logical_rows=M, out=R2, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    K_ = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(K_):
+            ev[i][0].record(stream)
+            m.mhc_pre(R, fn, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn, post=post,
+                      comb=comb, stream=stream)
+            ev[i][1].record(stream)
+            m.mhc_post(R, y, post, comb, logical_rows=M, out=R2, stream=stream)
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+    clocks = clk.summary()
+    ms = start.elapsed_time(end)
+    pre_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    post_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: host buffers, copies inside the timed region ----------
+    e2e_steps = max(3, min(K_, 20))
+    Rp = bf(Rh).pin_memory()
+    yp = bf(yh).pin_memory()
+    xn_h = torch.empty((M, H), dtype=torch.bfloat16).pin_memory()
+    R2_h = torch.empty((M, HC, H), dtype=torch.bfloat16).pin_memory()
+    post_h = torch.empty((M, HC), dtype=torch.float32).pin_memory()
+    comb_h = torch.empty((M, HC, HC), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        R.copy_(Rp, non_blocking=True)
+        y.copy_(yp, non_blocking=True)
+        step()
+        xn_h.copy_(xn, non_blocking=True)
+        R2_h.copy_(R2, non_blocking=True)
+        post_h.copy_(post, non_blocking=True)
+        comb_h.copy_(comb, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = s2.elapsed_time(e2)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (Rp.numel() + yp.numel()) * 2
+    d2h = (xn_h.numel() + R2_h.numel()) * 2 + (post_h.numel() + comb_h.numel()) * 4
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) --------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        sample = max(threads, min(1024, threads * 48))
+        v = oracle_rows_per_s(Rh, yh, W, sample, threads)
+        cpu = {"value": v, "unit": "rows/s", "cores": threads, "kind": "oracle",
+               "sample": f"oracle pre+post on rows 0..{sample - 1} of the M={M} workload"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm_peak, peak_src = peaks()
+    step_bytes = M * (PRE_BYTES_ROW + POST_BYTES_ROW) + PRE_BYTES_CALL
+    rows_per_s = world * M * K_ / (ms / 1e3)
+    gbs = step_bytes * K_ / (ms / 1e3) / 1e9
+    pre_gbs = (M * PRE_BYTES_ROW + PRE_BYTES_CALL) / (pre_ms / 1e3) / 1e9
+    post_gbs = M * POST_BYTES_ROW / (post_ms / 1e3) / 1e9
+    if post_ms >= pre_ms:
+        dom, dgbs, dbytes = "mhc_post", post_gbs, M * POST_BYTES_ROW
+    else:
+        dom, dgbs, dbytes = "mhc_pre", pre_gbs, M * PRE_BYTES_ROW + PRE_BYTES_CALL
+    line = {
+        "metric": METRIC,
+        "value": rows_per_s,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": K_,
+        "warmup": args.warmup,
+        "ms_per_step": ms / K_,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"M={M} rows per GPU: R[M,4,5120] bf16, fn[24,20480] f32, y[M,5120] bf16 "
+                        f"(seed {SEED}); one step = mhc_pre + mhc_post",
+            "rows_per_gpu": M,
+            "l2": "inputs larger than L2 (R alone is 671 MB per step); no flush",
+            "achieved_gbs": gbs,
+            "frac_of_hbm": gbs / hbm_peak,
+            "pre_ms": pre_ms,
+            "post_ms": post_ms,
+            "pre_gbs": pre_gbs,
+            "post_gbs": post_gbs,
+            "algorithmic_bytes_per_step": step_bytes,
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": dom,
+            "achieved": dgbs,
+            "peak": hbm_peak,
+            "peak_source": f"{peak_src} (hbm_gbs)",
+            "unit": "GB/s",
+            "frac": dgbs / hbm_peak,
+            "traffic": traffic_for(dom),
+            "algorithmic_bytes_per_launch": dbytes,
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * M * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": K_ * (PRE_LAUNCHES + POST_LAUNCHES),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mhc(args)
+
+
+if __name__ == "__main__":
+    main()

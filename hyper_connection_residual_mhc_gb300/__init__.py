@@ -1,0 +1,192 @@
+"""Python binding of libmhc (GB300 / sm_103a hyper-connection kernels).
+
+Argument marshalling only: every step of the hot path runs in libmhc's CUDA
+kernels.  Functions carry the C entry points' names (include/mhc.h) and take
+torch CUDA tensors; torch provides device memory and the current stream.
+Outputs the caller does not pass are allocated with torch.empty.
+
+If ``_build/libmhc.so`` is missing, every call raises: there is no fallback.
+Build it with ``python -m hyper_connection_residual_mhc_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HC, H, K, MIX = 4, 5120, 20480, 24
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libmhc.so")
+
+MHC_OK = 0
+
+
+class MhcParams(ctypes.Structure):
+    """Mirror of ``mhc_params`` (include/mhc.h)."""
+    _fields_ = [("rms_eps", ctypes.c_float), ("hc_pre_eps", ctypes.c_float),
+                ("hc_sinkhorn_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
+                ("post_mult", ctypes.c_float), ("sinkhorn_iters", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class MhcError(RuntimeError):
+    def __init__(self, fn, code, text):
+        super().__init__(f"{fn} failed with {code}: {text}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+# name -> (restype, argtypes); keep in step with include/mhc.h
+SIGNATURES = {
+    "mhc_default_params": (None, [ctypes.POINTER(MhcParams)]),
+    "mhc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "mhc_last_cuda_error": (ctypes.c_char_p, []),
+    "mhc_pre_workspace_bytes": (ctypes.c_size_t, [_i64]),
+    "mhc_pre": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.POINTER(MhcParams),
+                               _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mhc_post": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp]),
+    "mhc_combine_norm": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp]),
+}
+
+
+def lib():
+    """The loaded libmhc (ctypes.CDLL).  Raises if the library was not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libmhc is not built ({LIB_PATH} missing); run "
+                    "`python -m hyper_connection_residual_mhc_gb300.build`")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(l, name)
+                f.restype, f.argtypes = res, args
+            _lib = l
+    return _lib
+
+
+def default_params(**overrides) -> MhcParams:
+    p = MhcParams()
+    lib().mhc_default_params(ctypes.byref(p))
+    for k, v in overrides.items():
+        setattr(p, k, v)
+    return p
+
+
+def _check(fn, code):
+    if code != MHC_OK:
+        l = lib()
+        text = l.mhc_strerror(code).decode()
+        if code == -7:
+            text += f" ({l.mhc_last_cuda_error().decode()})"
+        raise MhcError(fn, code, text)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t, name, dtype, shape):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t
+
+
+def mhc_pre_workspace_bytes(rows: int) -> int:
+    return int(lib().mhc_pre_workspace_bytes(int(rows)))
+
+
+def mhc_pre(R, fn, scale, base, norm_w, *, logical_rows=None, params=None, workspace=None,
+            x_norm=None, post=None, comb=None, pre_out=None, mix_out=None, stream=None):
+    """Stats, split/Sinkhorn, combine + RMSNorm (see mhc_pre in include/mhc.h).
+
+    Returns ``(x_norm [rows,5120] bf16, post [rows,4] f32, comb [rows,4,4] f32)``.
+    """
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(fn, "fn", torch.float32, (MIX, K))
+    _need(scale, "scale", torch.float32, (3,))
+    _need(base, "base", torch.float32, (MIX,))
+    _need(norm_w, "norm_w", torch.bfloat16, (H,))
+    dev = R.device
+    x_norm = torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if x_norm is None else x_norm
+    post = torch.empty((rows, HC), dtype=torch.float32, device=dev) if post is None else post
+    comb = torch.empty((rows, HC, HC), dtype=torch.float32, device=dev) if comb is None else comb
+    _need(x_norm, "x_norm", torch.bfloat16, (rows, H))
+    _need(post, "post", torch.float32, (rows, HC))
+    _need(comb, "comb", torch.float32, (rows, HC, HC))
+    if pre_out is not None:
+        _need(pre_out, "pre_out", torch.float32, (rows, HC))
+    if mix_out is not None:
+        _need(mix_out, "mix_out", torch.float32, (rows, MIX))
+    need = mhc_pre_workspace_bytes(rows)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    p = default_params() if params is None else params
+    code = lib().mhc_pre(
+        _ptr(R), _ptr(fn), _ptr(scale), _ptr(base), _ptr(norm_w), rows,
+        rows if logical_rows is None else int(logical_rows), ctypes.byref(p),
+        _ptr(workspace), ws_bytes, _ptr(x_norm), _ptr(post), _ptr(comb), _ptr(pre_out),
+        _ptr(mix_out), _stream(stream))
+    _check("mhc_pre", code)
+    return x_norm, post, comb
+
+
+def mhc_post(R, y, post, comb, *, logical_rows=None, out=None, stream=None):
+    """New residual after a sublayer (see mhc_post in include/mhc.h)."""
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(y, "y", torch.bfloat16, (rows, H))
+    _need(post, "post", torch.float32, (rows, HC))
+    _need(comb, "comb", torch.float32, (rows, HC, HC))
+    out = torch.empty_like(R) if out is None else out
+    _need(out, "out", torch.bfloat16, (rows, HC, H))
+    code = lib().mhc_post(_ptr(R), _ptr(y), _ptr(post), _ptr(comb), rows,
+                          rows if logical_rows is None else int(logical_rows), _ptr(out),
+                          _stream(stream))
+    _check("mhc_post", code)
+    return out
+
+
+def mhc_combine_norm(R, pre, norm_w, norm_eps=1e-6, *, logical_rows=None, out=None, stream=None):
+    """Combine + RMSNorm with a given pre gate (see mhc_combine_norm in include/mhc.h)."""
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(pre, "pre", torch.float32, (rows, HC))
+    _need(norm_w, "norm_w", torch.bfloat16, (H,))
+    out = torch.empty((rows, H), dtype=torch.bfloat16, device=R.device) if out is None else out
+    _need(out, "out", torch.bfloat16, (rows, H))
+    code = lib().mhc_combine_norm(_ptr(R), _ptr(pre), _ptr(norm_w), float(norm_eps), rows,
+                                  rows if logical_rows is None else int(logical_rows),
+                                  _ptr(out), _stream(stream))
+    _check("mhc_combine_norm", code)
+    return out

@@ -1,0 +1,182 @@
+// abi.cu -- the extern "C" entry points of libmhc: host-side validation, then
+// the internal launchers.  Nothing here allocates device memory.
+#include <cmath>
+#include <cstring>
+#include <string>
+
+#include "mhc_common.cuh"
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
+  return MHC_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool finite_nonneg(float v) { return std::isfinite(v) && v >= 0.f; }
+
+struct Span {
+  uintptr_t lo, hi;
+};
+Span span(const void *p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + bytes};
+}
+bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// rows are indexed with 32-bit block counts in places: keep rows * 640 chunks
+// (the largest per-row grid) inside a signed 32-bit grid dimension times 256.
+constexpr int64_t kMaxRows = (int64_t)1 << 24;
+
+int check_rows(int64_t rows, int64_t logical_rows) {
+  if (rows < 0 || logical_rows < rows || rows > kMaxRows) return MHC_ERR_SHAPE;
+  return MHC_OK;
+}
+
+// The kernels are built for sm_103a only.  Check the current device once per
+// device (cached), after argument validation, before the first launch.
+int check_device() {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  static int ok_mask = 0;  // bit d set: device d verified
+  if (dev >= 0 && dev < 31 && (ok_mask >> dev) & 1) return MHC_OK;
+  int major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (major != 10 || minor != 3) return MHC_ERR_DEVICE;
+  if (dev >= 0 && dev < 31) ok_mask |= 1 << dev;
+  return MHC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void mhc_default_params(mhc_params *p) {
+  if (!p) return;
+  p->rms_eps = 1e-6f;
+  p->hc_pre_eps = 1e-6f;
+  p->hc_sinkhorn_eps = 1e-6f;
+  p->norm_eps = 1e-6f;
+  p->post_mult = 2.0f;
+  p->sinkhorn_iters = 20;
+}
+
+const char *mhc_strerror(int code) {
+  switch (code) {
+    case MHC_OK: return "ok";
+    case MHC_ERR_NULL: return "a required pointer is NULL";
+    case MHC_ERR_SHAPE: return "bad row count (rows < 0, logical_rows < rows, or too many rows)";
+    case MHC_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case MHC_ERR_PARAM: return "bad scalar parameter (eps < 0 or not finite, iterations < 1)";
+    case MHC_ERR_OVERLAP: return "an output buffer overlaps an input buffer";
+    case MHC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MHC_ERR_CUDA: return "a CUDA call failed";
+    case MHC_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    default: return "unknown libmhc error code";
+  }
+}
+
+const char *mhc_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+size_t mhc_pre_workspace_bytes(int64_t rows) {
+  if (rows <= 0) return 0;
+  return mhc::pre_simt_workspace_bytes(rows);
+}
+
+int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float *base,
+            const uint16_t *norm_w, int64_t rows, int64_t logical_rows, const mhc_params *p_in,
+            void *workspace, size_t workspace_bytes, uint16_t *x_norm, float *post,
+            float *comb, float *pre_out, float *mix_out, void *stream) {
+  mhc_params p;
+  if (p_in) p = *p_in; else mhc_default_params(&p);
+  if (int e = check_rows(rows, logical_rows)) return e;
+  if (!finite_nonneg(p.rms_eps) || !finite_nonneg(p.hc_pre_eps) ||
+      !finite_nonneg(p.hc_sinkhorn_eps) || !finite_nonneg(p.norm_eps) ||
+      !std::isfinite(p.post_mult) || p.sinkhorn_iters < 1 || p.sinkhorn_iters > 100000)
+    return MHC_ERR_PARAM;
+  if (rows == 0) return MHC_OK;
+  if (!R || !fn || !scale || !base || !norm_w || !x_norm || !post || !comb) return MHC_ERR_NULL;
+  const void *al[] = {R, fn, scale, base, norm_w, x_norm, post, comb};
+  for (const void *q : al)
+    if (!aligned16(q)) return MHC_ERR_ALIGN;
+  if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
+  const size_t need = mhc_pre_workspace_bytes(rows);
+  if (need > 0 && (!workspace || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return MHC_ERR_WORKSPACE;
+
+  const size_t nr = (size_t)rows;
+  const Span ins[] = {span(R, nr * MHC_K * 2), span(fn, (size_t)MHC_MIX * MHC_K * 4),
+                      span(scale, 12), span(base, MHC_MIX * 4), span(norm_w, MHC_HIDDEN * 2)};
+  Span outs[6];
+  int n_out = 0;
+  outs[n_out++] = span(x_norm, nr * MHC_HIDDEN * 2);
+  outs[n_out++] = span(post, nr * MHC_HC * 4);
+  outs[n_out++] = span(comb, nr * MHC_HC * MHC_HC * 4);
+  if (pre_out) outs[n_out++] = span(pre_out, nr * MHC_HC * 4);
+  if (mix_out) outs[n_out++] = span(mix_out, nr * MHC_MIX * 4);
+  if (need) outs[n_out++] = span(workspace, need);
+  for (int a = 0; a < n_out; ++a) {
+    for (const Span &b : ins)
+      if (overlap(outs[a], b)) return MHC_ERR_OVERLAP;
+    for (int b = a + 1; b < n_out; ++b)
+      if (overlap(outs[a], outs[b])) return MHC_ERR_OVERLAP;
+  }
+
+  if (int e = check_device()) return e;
+  cudaError_t ce = mhc::launch_pre_simt(R, fn, scale, base, norm_w, rows, logical_rows, p,
+                                        workspace, x_norm, post, comb, pre_out, mix_out,
+                                        static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+
+int mhc_post(const uint16_t *R, const uint16_t *y, const float *post, const float *comb,
+             int64_t rows, int64_t logical_rows, uint16_t *R_out, void *stream) {
+  if (int e = check_rows(rows, logical_rows)) return e;
+  if (rows == 0) return MHC_OK;
+  if (!R || !y || !post || !comb || !R_out) return MHC_ERR_NULL;
+  const void *al[] = {R, y, post, comb, R_out};
+  for (const void *q : al)
+    if (!aligned16(q)) return MHC_ERR_ALIGN;
+  const size_t nr = (size_t)rows;
+  const Span out = span(R_out, nr * MHC_K * 2);
+  const Span ins[] = {span(R, nr * MHC_K * 2), span(y, nr * MHC_HIDDEN * 2),
+                      span(post, nr * MHC_HC * 4), span(comb, nr * MHC_HC * MHC_HC * 4)};
+  for (const Span &b : ins)
+    if (overlap(out, b)) return MHC_ERR_OVERLAP;
+  if (int e = check_device()) return e;
+  cudaError_t ce = mhc::launch_post(R, y, post, comb, rows, logical_rows, R_out,
+                                    static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+
+int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
+                     float norm_eps, int64_t rows, int64_t logical_rows, uint16_t *x_norm,
+                     void *stream) {
+  if (int e = check_rows(rows, logical_rows)) return e;
+  if (!finite_nonneg(norm_eps)) return MHC_ERR_PARAM;
+  if (rows == 0) return MHC_OK;
+  if (!R || !pre || !norm_w || !x_norm) return MHC_ERR_NULL;
+  const void *al[] = {R, pre, norm_w, x_norm};
+  for (const void *q : al)
+    if (!aligned16(q)) return MHC_ERR_ALIGN;
+  const size_t nr = (size_t)rows;
+  const Span out = span(x_norm, nr * MHC_HIDDEN * 2);
+  const Span ins[] = {span(R, nr * MHC_K * 2), span(pre, nr * MHC_HC * 4),
+                      span(norm_w, MHC_HIDDEN * 2)};
+  for (const Span &b : ins)
+    if (overlap(out, b)) return MHC_ERR_OVERLAP;
+  if (int e = check_device()) return e;
+  cudaError_t ce = mhc::launch_combine_norm(R, pre, norm_w, norm_eps, rows, logical_rows,
+                                            x_norm, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+
+}  // extern "C"

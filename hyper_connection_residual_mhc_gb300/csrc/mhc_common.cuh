@@ -1,0 +1,68 @@
+// mhc_common.cuh -- device helpers and internal launcher declarations shared
+// by the libmhc translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mhc.h"
+
+namespace mhc {
+
+constexpr int kHC = MHC_HC;        // residual streams
+constexpr int kH = MHC_HIDDEN;     // hidden width
+constexpr int kK = MHC_K;          // flattened row width
+constexpr int kMix = MHC_MIX;      // mixes per row
+constexpr int kChunk = 8;          // bf16 per 16-byte vector
+constexpr int kChunksPerStream = kH / kChunk;   // 640
+
+// ---- bf16 <-> fp32 on 16-byte vectors -------------------------------------
+// bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(w[q] << 16);
+    f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+  }
+}
+
+// fp32 -> bf16, round to nearest even, two at a time (low half = first).
+__device__ __forceinline__ uint32_t pack2_rn(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ uint4 pack8_rn(const float (&f)[8]) {
+  uint4 v;
+  v.x = pack2_rn(f[0], f[1]);
+  v.y = pack2_rn(f[2], f[3]);
+  v.z = pack2_rn(f[4], f[5]);
+  v.w = pack2_rn(f[6], f[7]);
+  return v;
+}
+
+// Streaming (evict-first) 16-byte global accesses for data touched once.
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
+
+// ---- internal launchers (host side) ----------------------------------------
+// Each returns cudaSuccess or the launch error; arguments are validated by the
+// C entry points before these are called.
+cudaError_t launch_post(const uint16_t *R, const uint16_t *y, const float *post,
+                        const float *comb, int64_t rows, int64_t logical_rows, uint16_t *R_out,
+                        cudaStream_t s);
+
+cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
+                                float norm_eps, int64_t rows, int64_t logical_rows,
+                                uint16_t *x_norm, cudaStream_t s);
+
+size_t pre_simt_workspace_bytes(int64_t rows);
+cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *scale,
+                            const float *base, const uint16_t *norm_w, int64_t rows,
+                            int64_t logical_rows, const mhc_params &p, void *workspace,
+                            uint16_t *x_norm, float *post, float *comb, float *pre_out,
+                            float *mix_out, cudaStream_t s);
+
+}  // namespace mhc

@@ -1,0 +1,164 @@
+/*
+ * mhc.h -- C ABI of libmhc: the row-local manifold-constrained hyper-connection
+ * (mHC) work around one sublayer of a DeepSeek-V4 decoder layer, on GB300
+ * (sm_103a).
+ *
+ * The residual R of a chunk of M tokens carries HC = 4 streams of width
+ * H = 5120 (R[M, 4, 5120], bf16).  Around every sublayer the model runs
+ *   pre : stats -> split/Sinkhorn -> combine + RMSNorm  (feeds the sublayer)
+ *   post: new residual from the sublayer output          (after the sublayer)
+ * as defined in deepseek_v4.py (sglang), DeepseekV4DecoderLayer.hc_pre and
+ * DeepseekV4DecoderLayer.hc_post.
+ *
+ * Conventions for every entry point below
+ *  - All tensor arguments are DEVICE pointers, owned by the caller, row-major
+ *    and densely packed in the layout stated; bf16 tensors are passed as
+ *    uint16_t bit patterns.  Every tensor pointer must be 16-byte aligned.
+ *  - Calls are asynchronous: they enqueue kernels on `stream` (a
+ *    cudaStream_t; NULL means the legacy default stream) and never
+ *    synchronise.  Device-side faults surface at the caller's next
+ *    synchronisation, as with any CUDA launch.
+ *  - `rows` is the number of rows this call processes (a row-range shard
+ *    passes pointers already offset to its first row).  `logical_rows` is
+ *    the row count of the whole chunk the rows belong to; launch heuristics
+ *    may read only `logical_rows`, never `rows`, so any row range
+ *    [lo, hi) of a chunk gives exactly the bits the whole-chunk call gives
+ *    on those rows (prefill_sp.py, sp_logical_rows: kernel gates key on the
+ *    full chunk row count).  logical_rows >= rows is required.
+ *  - rows == 0 returns MHC_OK without launching anything.
+ *  - Arguments are validated on the host before any launch; on an error the
+ *    call returns a negative code, launches nothing and writes nothing.
+ *  - Output buffers must not overlap any input buffer.
+ *  - The library allocates no device memory.  Scratch space, where an
+ *    entry point needs it, is passed in by the caller (`workspace`).
+ */
+#ifndef MHC_H
+#define MHC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MHC_HC 4                       /* hc_mult: residual streams */
+#define MHC_HIDDEN 5120                /* hidden size H */
+#define MHC_K (MHC_HC * MHC_HIDDEN)    /* flattened row width 20480 */
+#define MHC_MIX 24                     /* (2 + hc_mult) * hc_mult mixes */
+
+/* return codes */
+#define MHC_OK 0
+#define MHC_ERR_NULL (-1)        /* a required pointer is NULL */
+#define MHC_ERR_SHAPE (-2)       /* rows < 0, logical_rows < rows, or rows too large */
+#define MHC_ERR_ALIGN (-3)       /* a tensor pointer is not 16-byte aligned */
+#define MHC_ERR_PARAM (-4)       /* eps < 0 or not finite, iters < 1, ... */
+#define MHC_ERR_OVERLAP (-5)     /* an output buffer overlaps an input buffer */
+#define MHC_ERR_WORKSPACE (-6)   /* workspace NULL or smaller than required */
+#define MHC_ERR_CUDA (-7)        /* a CUDA call failed (see mhc_last_cuda_error) */
+#define MHC_ERR_DEVICE (-8)      /* current device is not an sm_103 GPU */
+
+/* Scalars of the split/Sinkhorn and the two RMS normalisations.
+ * deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre passes rms_eps =
+ * rms_norm_eps, hc_pre_eps = hc_sinkhorn_eps = hc_eps, post_mult =
+ * _MHC_POST_MULT_VALUE (2.0) and sinkhorn_repeat = hc_sinkhorn_iters;
+ * norm_eps is the RMSNorm's variance epsilon. */
+typedef struct mhc_params {
+    float rms_eps;          /* added to mean(x^2) of the flattened row (stats) */
+    float hc_pre_eps;       /* pre = sigmoid(logit) + hc_pre_eps */
+    float hc_sinkhorn_eps;  /* added to every Sinkhorn row and column sum */
+    float norm_eps;         /* RMSNorm: added to mean(y^2) */
+    float post_mult;        /* post = post_mult * sigmoid(logit) */
+    int32_t sinkhorn_iters; /* full row+column normalisation rounds, >= 1 */
+} mhc_params;
+
+/* Fill *p with rms_eps = hc_pre_eps = hc_sinkhorn_eps = norm_eps = 1e-6,
+ * post_mult = 2, sinkhorn_iters = 20 (the values test_prefill_sp_gpu.py's
+ * Layer stand-in uses). */
+void mhc_default_params(mhc_params *p);
+
+/* Static description of a return code; never NULL. */
+const char *mhc_strerror(int code);
+
+/* Text of the last CUDA error seen by this thread inside libmhc ("" if none). */
+const char *mhc_last_cuda_error(void);
+
+/* Bytes of device scratch mhc_pre needs for a call on `rows` rows. */
+size_t mhc_pre_workspace_bytes(int64_t rows);
+
+/*
+ * mhc_pre -- stats, split/Sinkhorn, combine + RMSNorm for `rows` rows.
+ *
+ * deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre: with x = R[m] flattened
+ * stream-major (k = i*5120 + h) in fp32,
+ *   rsqrt     = 1 / sqrt(mean_k x_k^2 + rms_eps)
+ *   mix[c]    = rsqrt * sum_k x_k * fn[c, k]                     (c < 24)
+ *   logit[c]  = mix[c] * scale[g(c)] + base[c],  g = 0 | 1 | 2 for
+ *               c in [0,4) | [4,8) | [8,24)
+ *   pre[i]    = sigmoid(logit[i]) + hc_pre_eps
+ *   post[i]   = post_mult * sigmoid(logit[4+i])
+ *   comb      = exp(logit[8 + 4j + i]) as comb[j][i], then sinkhorn_iters
+ *               rounds of: divide row j by (sum_i comb[j][i] + eps), then
+ *               column i by (sum_j comb[j][i] + eps)  (hc_split_sinkhorn)
+ *   y[h]      = sum_i pre[i] * R[m, i, h]                        (fp32)
+ *   x_norm[h] = bf16( y[h] / sqrt(mean_h y^2 + norm_eps) * w[h] )
+ * (RMSNorm fused without rounding y first, as the fused combine+norm gate of
+ * prefill_sp.py, _combine_norm_fused, requires.)
+ *
+ * Arguments
+ *   R        [rows, 4, 5120] bf16      residual rows
+ *   fn       [24, 20480] fp32          hc_fn mixing projection
+ *   scale    [3] fp32                  hc_scale (pre, post, comb)
+ *   base     [24] fp32                 hc_base
+ *   norm_w   [5120] bf16               RMSNorm weight
+ *   p        host pointer; NULL means mhc_default_params
+ *   workspace, workspace_bytes  device scratch of at least
+ *            mhc_pre_workspace_bytes(rows) bytes, 256-byte aligned; its
+ *            contents on entry do not matter; the call owns it until the
+ *            stream reaches the end of the call.
+ * Outputs (fp32 unless stated)
+ *   x_norm   [rows, 5120] bf16         normalised combine (sublayer input)
+ *   post     [rows, 4]                 post gate
+ *   comb     [rows, 4, 4]              Sinkhorn mix, comb[m][j][i]
+ *   pre_out  [rows, 4] or NULL         pre gate
+ *   mix_out  [rows, 24] or NULL        mix (after rsqrt scaling)
+ */
+int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float *base,
+            const uint16_t *norm_w, int64_t rows, int64_t logical_rows, const mhc_params *p,
+            void *workspace, size_t workspace_bytes, uint16_t *x_norm, float *post,
+            float *comb, float *pre_out, float *mix_out, void *stream);
+
+/*
+ * mhc_post -- the new residual after a sublayer.
+ *
+ * deepseek_v4.py, DeepseekV4DecoderLayer.hc_post (hc_post_torch_impl):
+ *   R_out[m, i, h] = bf16( post[m, i] * y[m, h] + sum_j comb[m, j, i] * R[m, j, h] )
+ * computed in fp32 and rounded once.
+ *   R      [rows, 4, 5120] bf16   residual that entered the sublayer
+ *   y      [rows, 5120] bf16      sublayer output
+ *   post   [rows, 4] fp32, comb [rows, 4, 4] fp32 (as mhc_pre wrote them)
+ *   R_out  [rows, 4, 5120] bf16   output; must not overlap any input
+ */
+int mhc_post(const uint16_t *R, const uint16_t *y, const float *post, const float *comb,
+             int64_t rows, int64_t logical_rows, uint16_t *R_out, void *stream);
+
+/*
+ * mhc_combine_norm -- the combine + RMSNorm step alone, with a given pre.
+ *
+ * deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre (combine after
+ * hc_split_sinkhorn) fused with RMSNorm as in prefill_sp.py,
+ * hc_combine_norm_rows:
+ *   x_norm[m, h] = bf16( y[h] / sqrt(mean_h y^2 + norm_eps) * w[h] ),
+ *   y[h] = sum_i pre[m, i] * R[m, i, h].
+ *   R [rows, 4, 5120] bf16, pre [rows, 4] fp32, norm_w [5120] bf16,
+ *   x_norm [rows, 5120] bf16.  norm_eps >= 0 and finite.
+ */
+int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
+                     float norm_eps, int64_t rows, int64_t logical_rows, uint16_t *x_norm,
+                     void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHC_H */

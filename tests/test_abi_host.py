@@ -1,0 +1,130 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every function include/*.h declares, and argument validation rejects
+bad calls before any CUDA call.
+
+Every call below carries at least one defect that the host checks catch, so no
+call ever reaches a kernel launch (the pointers are fake addresses and are
+never dereferenced).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_PARAM, ERR_OVERLAP, ERR_WORKSPACE = -1, -2, -3, -4, -5, -6
+K, H = 20480, 5120
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from hyper_connection_residual_mhc_gb300 import build
+    build.build()
+    import hyper_connection_residual_mhc_gb300 as m
+    return m.lib()
+
+
+def declared_functions():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(hdr).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(mhc_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("mhc_pre", "mhc_post", "mhc_combine_norm", "mhc_pre_workspace_bytes",
+              "mhc_default_params", "mhc_strerror", "mhc_last_cuda_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_the_header():
+    import hyper_connection_residual_mhc_gb300 as m
+    assert set(declared_functions()) <= set(m.SIGNATURES)
+
+
+def test_strerror_and_defaults(lib):
+    import hyper_connection_residual_mhc_gb300 as m
+    for code in range(0, -9, -1):
+        assert lib.mhc_strerror(code)
+    p = m.default_params()
+    assert p.sinkhorn_iters == 20 and p.post_mult == 2.0
+    assert abs(p.rms_eps - 1e-6) < 1e-12 and abs(p.norm_eps - 1e-6) < 1e-12
+    assert lib.mhc_pre_workspace_bytes(0) == 0
+    assert lib.mhc_pre_workspace_bytes(1000) >= 1000 * 4 * 4
+
+
+A = 1 << 32          # fake, 256-byte aligned device addresses, far apart
+BIG = 1 << 34
+
+
+def fake(i):
+    return A + i * BIG
+
+
+def call_post(lib, R=fake(0), y=fake(1), post=fake(2), comb=fake(3), rows=4, logical=4,
+              out=fake(4)):
+    return lib.mhc_post(R, y, post, comb, rows, logical, out, None)
+
+
+def call_pre(lib, rows=4, logical=4, params=None, ws=fake(9), ws_bytes=None, **over):
+    import hyper_connection_residual_mhc_gb300 as m
+    a = dict(R=fake(0), fn=fake(1), scale=fake(2), base=fake(3), w=fake(4), xn=fake(5),
+             post=fake(6), comb=fake(7), pre=None, mix=None)
+    a.update(over)
+    p = m.default_params() if params is None else params
+    wsb = lib.mhc_pre_workspace_bytes(rows) if ws_bytes is None else ws_bytes
+    return lib.mhc_pre(a["R"], a["fn"], a["scale"], a["base"], a["w"], rows, logical,
+                       ctypes.byref(p), ws, wsb, a["xn"], a["post"], a["comb"], a["pre"],
+                       a["mix"], None)
+
+
+def test_post_validation(lib):
+    assert call_post(lib, rows=-1) == ERR_SHAPE
+    assert call_post(lib, rows=8, logical=4) == ERR_SHAPE
+    assert call_post(lib, R=None) == ERR_NULL
+    assert call_post(lib, out=None) == ERR_NULL
+    assert call_post(lib, y=fake(1) + 8) == ERR_ALIGN
+    assert call_post(lib, out=fake(0) + 4 * K * 2 - 16) == ERR_OVERLAP     # tail overlaps R
+    assert call_post(lib, out=fake(1)) == ERR_OVERLAP
+
+
+def test_post_zero_rows_is_a_no_op(lib):
+    assert call_post(lib, rows=0, logical=0, R=None, out=None) == 0
+
+
+def test_pre_validation(lib):
+    import hyper_connection_residual_mhc_gb300 as m
+    assert call_pre(lib, rows=-3) == ERR_SHAPE
+    assert call_pre(lib, rows=5, logical=4) == ERR_SHAPE
+    assert call_pre(lib, params=m.default_params(sinkhorn_iters=0)) == ERR_PARAM
+    assert call_pre(lib, params=m.default_params(norm_eps=-1.0)) == ERR_PARAM
+    assert call_pre(lib, params=m.default_params(rms_eps=float("nan"))) == ERR_PARAM
+    assert call_pre(lib, fn=None) == ERR_NULL
+    assert call_pre(lib, comb=fake(7) + 4) == ERR_ALIGN
+    assert call_pre(lib, mix=fake(8) + 4) == ERR_ALIGN
+    assert call_pre(lib, ws=None) == ERR_WORKSPACE
+    assert call_pre(lib, ws_bytes=16) == ERR_WORKSPACE
+    assert call_pre(lib, ws=fake(9) + 16) == ERR_WORKSPACE                # not 256-byte aligned
+    assert call_pre(lib, xn=fake(0)) == ERR_OVERLAP                         # x_norm on R
+    assert call_pre(lib, post=fake(7)) == ERR_OVERLAP                       # post on comb
+    assert call_pre(lib, ws=fake(5)) == ERR_OVERLAP                         # workspace on x_norm
+
+
+def test_combine_norm_validation(lib):
+    f = lib.mhc_combine_norm
+    assert f(fake(0), fake(1), fake(2), ctypes.c_float(-1.0), 4, 4, fake(3), None) == ERR_PARAM
+    assert f(fake(0), None, fake(2), ctypes.c_float(1e-6), 4, 4, fake(3), None) == ERR_NULL
+    assert f(fake(0), fake(1), fake(2), ctypes.c_float(1e-6), 4, 2, fake(3), None) == ERR_SHAPE
+    assert f(fake(0), fake(1), fake(2), ctypes.c_float(1e-6), 4, 4, fake(0), None) == ERR_OVERLAP

@@ -64,3 +64,28 @@ def test_bf16_bit_helpers_round_trip():
     b = synth.f32_to_bf16_bits(x)
     np.testing.assert_allclose(synth.bf16_bits_to_f32(b), x, rtol=2 ** -8)
     np.testing.assert_array_equal(synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(b)), b)
+
+
+def test_parity_checker_flags_injected_errors(oracle_mod):
+    # the element-wise checker must accept the reference itself and flag a
+    # 3-ulp perturbation of one element (fault injection on the host).
+    import pytest
+    from tests import parity as P
+    R = synth.residual(0, 2)
+    W = synth.weights(0)
+    o = oracle_mod.pre(R, W.fn, W.scale, W.base, W.norm_w)
+    tm = P.combine_term_magnitude(R, o["pre"], W.norm_w, 1e-6)
+    P.check_bf16(o["x_norm"], o["x_norm"], "x_norm", term_mag=tm)
+    bad = o["x_norm"].copy()
+    h = 1000 + int(np.argmax(np.abs(P.unbf(bad[1, 1000:2000]))))   # a large, unscaled element
+    bad[1, h] = bad[1, h] + np.uint16(3)
+    with pytest.raises(AssertionError):
+        P.check_bf16(bad, o["x_norm"], "x_norm", term_mag=tm)
+    mix = o["mix"].copy()
+    mix[0, 5] *= 1 + 3e-4
+    with pytest.raises(AssertionError):
+        P.check_mix(mix, o["mix"])
+    comb = o["comb"].copy()
+    comb[1, 2, 3] += 3e-6
+    with pytest.raises(AssertionError):
+        P.check_abs(comb, o["comb"], 1e-6, "comb")
