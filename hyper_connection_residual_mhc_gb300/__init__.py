@@ -53,6 +53,9 @@ SIGNATURES = {
     "mhc_pre_workspace_bytes": (ctypes.c_size_t, [_i64]),
     "mhc_pre": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.POINTER(MhcParams),
                                _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mhc_pre_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                       ctypes.POINTER(MhcParams), _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mhc_pre_noalloc_max_rows": (ctypes.c_int64, []),
     "mhc_post": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp]),
     "mhc_combine_norm": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp]),
 }
@@ -156,6 +159,39 @@ def mhc_pre(R, fn, scale, base, norm_w, *, logical_rows=None, params=None, works
         _ptr(workspace), ws_bytes, _ptr(x_norm), _ptr(post), _ptr(comb), _ptr(pre_out),
         _ptr(mix_out), _stream(stream))
     _check("mhc_pre", code)
+    return x_norm, post, comb
+
+
+def mhc_pre_noalloc_max_rows() -> int:
+    return int(lib().mhc_pre_noalloc_max_rows())
+
+
+def mhc_pre_noalloc(R, fn, scale, base, norm_w, x_norm, post, comb, *, logical_rows=None,
+                    params=None, pre_out=None, mix_out=None, stream=None):
+    """mhc_pre for callers that cannot provide device scratch (see mhc_pre_noalloc
+    in include/mhc.h).  Allocates nothing: every output is passed in.  The first
+    call on a device sets up the scratch address there; make it before any
+    stream capture.  Calls overlapping on the GPU race on the shared scratch."""
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(fn, "fn", torch.float32, (MIX, K))
+    _need(scale, "scale", torch.float32, (3,))
+    _need(base, "base", torch.float32, (MIX,))
+    _need(norm_w, "norm_w", torch.bfloat16, (H,))
+    _need(x_norm, "x_norm", torch.bfloat16, (rows, H))
+    _need(post, "post", torch.float32, (rows, HC))
+    _need(comb, "comb", torch.float32, (rows, HC, HC))
+    if pre_out is not None:
+        _need(pre_out, "pre_out", torch.float32, (rows, HC))
+    if mix_out is not None:
+        _need(mix_out, "mix_out", torch.float32, (rows, MIX))
+    p = default_params() if params is None else params
+    code = lib().mhc_pre_noalloc(
+        _ptr(R), _ptr(fn), _ptr(scale), _ptr(base), _ptr(norm_w), rows,
+        rows if logical_rows is None else int(logical_rows), ctypes.byref(p), _ptr(x_norm),
+        _ptr(post), _ptr(comb), _ptr(pre_out), _ptr(mix_out), _stream(stream))
+    _check("mhc_pre_noalloc", code)
     return x_norm, post, comb
 
 

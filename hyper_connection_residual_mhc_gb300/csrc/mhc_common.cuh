@@ -65,4 +65,13 @@ cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *sca
                             uint16_t *x_norm, float *post, float *comb, float *pre_out,
                             float *mix_out, cudaStream_t s);
 
+// allocation-free variant of the CUDA-core pre path (scratch in a static
+// device array of noalloc_max_rows() rows)
+int64_t noalloc_max_rows();
+cudaError_t launch_pre_noalloc(const uint16_t *R, const float *fn, const float *scale,
+                               const float *base, const uint16_t *norm_w, int64_t rows,
+                               int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
+                               float *post, float *comb, float *pre_out, float *mix_out,
+                               cudaStream_t s);
+
 }  // namespace mhc

@@ -29,8 +29,9 @@
  *  - Arguments are validated on the host before any launch; on an error the
  *    call returns a negative code, launches nothing and writes nothing.
  *  - Output buffers must not overlap any input buffer.
- *  - The library allocates no device memory.  Scratch space, where an
- *    entry point needs it, is passed in by the caller (`workspace`).
+ *  - No call allocates device memory.  Scratch space, where an entry point
+ *    needs it, is passed in by the caller (`workspace`), except for
+ *    mhc_pre_noalloc, which uses a fixed array inside the library.
  */
 #ifndef MHC_H
 #define MHC_H
@@ -57,6 +58,7 @@ extern "C" {
 #define MHC_ERR_WORKSPACE (-6)   /* workspace NULL or smaller than required */
 #define MHC_ERR_CUDA (-7)        /* a CUDA call failed (see mhc_last_cuda_error) */
 #define MHC_ERR_DEVICE (-8)      /* current device is not an sm_103 GPU */
+#define MHC_ERR_SCRATCH_LIMIT (-9) /* rows above mhc_pre_noalloc's fixed scratch size */
 
 /* Scalars of the split/Sinkhorn and the two RMS normalisations.
  * deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre passes rms_eps =
@@ -127,6 +129,40 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
             const uint16_t *norm_w, int64_t rows, int64_t logical_rows, const mhc_params *p,
             void *workspace, size_t workspace_bytes, uint16_t *x_norm, float *post,
             float *comb, float *pre_out, float *mix_out, void *stream);
+
+/*
+ * mhc_pre_noalloc -- mhc_pre for callers that cannot provide device scratch.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory on this library's behalf: a framework
+ * whose caching allocator owns the device memory, a plugin/operator enqueue
+ * that must not allocate, a latency-critical serving loop that cannot afford
+ * cudaMalloc/cudaFree (they may synchronise the device), or a C/FFI caller
+ * with no device allocator.
+ *
+ * Same arguments, outputs and validation as mhc_pre, minus the workspace;
+ * results agree with mhc_pre's within the parity tolerances.  It runs
+ * libmhc's CUDA-core pre kernels with their scratch in a fixed
+ * 256-byte-aligned device array inside libmhc, sized for
+ * mhc_pre_noalloc_max_rows() = 16384 rows (about 25.3 MiB, held on every GPU
+ * that loads the library until the process exits).  rows above that limit
+ * return MHC_ERR_SCRATCH_LIMIT.  It allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library call).
+ *
+ * The first call on a device looks up the array's device address there (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  All calls share the one array, which keeps the last call's
+ * contents (nothing in it needs to start at zero): calls whose execution
+ * overlaps on the GPU (other streams, other host threads) race on it, so
+ * order them, e.g. on one stream.
+ */
+int mhc_pre_noalloc(const uint16_t *R, const float *fn, const float *scale, const float *base,
+                    const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+                    const mhc_params *p, uint16_t *x_norm, float *post, float *comb,
+                    float *pre_out, float *mix_out, void *stream);
+
+/* Largest `rows` mhc_pre_noalloc accepts (16384). */
+int64_t mhc_pre_noalloc_max_rows(void);
 
 /*
  * mhc_post -- the new residual after a sublayer.
