@@ -51,6 +51,8 @@ SIGNATURES = {
     "mhc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "mhc_last_cuda_error": (ctypes.c_char_p, []),
     "mhc_pre_workspace_bytes": (ctypes.c_size_t, [_i64]),
+    "mhc_kernel_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "mhc_kernel_status_detail": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "mhc_pre": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.POINTER(MhcParams),
                                _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mhc_pre_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64,
@@ -118,6 +120,24 @@ def _need(t, name, dtype, shape):
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
     return t
+
+
+def mhc_kernel_status(reset: bool = False) -> int:
+    """Device status word (0 = no kernel gave up a bounded wait); synchronous."""
+    w = ctypes.c_uint32(0)
+    _check("mhc_kernel_status", lib().mhc_kernel_status(ctypes.byref(w), int(bool(reset))))
+    return int(w.value)
+
+
+def mhc_kernel_status_detail() -> dict:
+    """{"expired": {site: (tile, rank)}, "gave_up": {site: (tile, rank)}} of the
+    fused pre kernel's bounded waits (diagnosis)."""
+    arr = (ctypes.c_uint32 * 64)()
+    _check("mhc_kernel_status_detail", lib().mhc_kernel_status_detail(arr))
+    st = mhc_kernel_status()
+    return {"expired": {s: (arr[s] >> 8, arr[s] & 0xFF) for s in range(16) if (st >> s) & 1},
+            "gave_up": {s: (arr[32 + s] >> 8, arr[32 + s] & 0xFF) for s in range(16)
+                        if (st >> (16 + s)) & 1}}
 
 
 def mhc_pre_workspace_bytes(rows: int) -> int:

@@ -88,8 +88,23 @@ const char *mhc_strerror(int code) {
 const char *mhc_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
 size_t mhc_pre_workspace_bytes(int64_t rows) {
-  if (rows <= 0) return 0;
-  return mhc::pre_simt_workspace_bytes(rows);
+  (void)rows;
+  return 0;  // the fused pre kernel keeps all of its intermediates on chip
+}
+
+int mhc_kernel_status_detail(uint32_t *where64) {
+  if (!where64) return MHC_ERR_NULL;
+  cudaError_t e = mhc::fused_error_where(where64);
+  return e == cudaSuccess ? MHC_OK : cuda_fail(e);
+}
+
+int mhc_kernel_status(uint32_t *status, int reset) {
+  if (!status) return MHC_ERR_NULL;
+  unsigned int w = 0;
+  cudaError_t e = mhc::fused_error_word(&w, reset != 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *status = w;
+  return MHC_OK;
 }
 
 int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float *base,
@@ -133,9 +148,9 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
   }
 
   if (int e = check_device()) return e;
-  cudaError_t ce = mhc::launch_pre_simt(R, fn, scale, base, norm_w, rows, logical_rows, p,
-                                        workspace, x_norm, post, comb, pre_out, mix_out,
-                                        static_cast<cudaStream_t>(stream));
+  cudaError_t ce = mhc::launch_pre_fused(R, fn, scale, base, norm_w, rows, logical_rows, p,
+                                         x_norm, post, comb, pre_out, mix_out,
+                                         static_cast<cudaStream_t>(stream));
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 

@@ -65,6 +65,16 @@ cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *sca
                             uint16_t *x_norm, float *post, float *comb, float *pre_out,
                             float *mix_out, cudaStream_t s);
 
+// fused single-launch pre path (tensor-core stats, cluster of 16 CTAs)
+cudaError_t launch_pre_fused(const uint16_t *R, const float *fn, const float *scale,
+                             const float *base, const uint16_t *norm_w, int64_t rows,
+                             int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
+                             float *post, float *comb, float *pre_out, float *mix_out,
+                             cudaStream_t s);
+// the fused kernel's error word (nonzero once a bounded wait expired)
+cudaError_t fused_error_word(unsigned int *out, bool reset);
+cudaError_t fused_error_where(unsigned int *out32);
+
 // allocation-free variant of the CUDA-core pre path (scratch in a static
 // device array of noalloc_max_rows() rows)
 int64_t noalloc_max_rows();

@@ -85,8 +85,23 @@ const char *mhc_strerror(int code);
 /* Text of the last CUDA error seen by this thread inside libmhc ("" if none). */
 const char *mhc_last_cuda_error(void);
 
-/* Bytes of device scratch mhc_pre needs for a call on `rows` rows. */
+/* Bytes of device scratch mhc_pre needs for a call on `rows` rows (0: the
+ * fused kernel keeps its intermediates on chip; a NULL workspace is fine). */
 size_t mhc_pre_workspace_bytes(int64_t rows);
+
+/* Read libmhc's device status word on the current device into *status: 0,
+ * or nonzero once a kernel gave up a bounded wait (it then returned early and
+ * its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
+ * the device's pending work.  Returns MHC_OK or MHC_ERR_NULL/MHC_ERR_CUDA. */
+int mhc_kernel_status(uint32_t *status, int reset);
+
+/* Where the waits recorded in the status word ended, for diagnosis: bit s
+ * (s < 16) of the status word means a bounded wait at site s of the fused pre
+ * kernel expired, bit 16 + s that a wait at site s gave up because its CTA had
+ * already aborted.  where64[s] (expired) and where64[32 + s] (gave up) hold
+ * (tile << 8) | CTA rank in its cluster of the last such event.  where64 has
+ * 64 entries.  Synchronous. */
+int mhc_kernel_status_detail(uint32_t *where64);
 
 /*
  * mhc_pre -- stats, split/Sinkhorn, combine + RMSNorm for `rows` rows.
@@ -106,6 +121,11 @@ size_t mhc_pre_workspace_bytes(int64_t rows);
  *   x_norm[h] = bf16( y[h] / sqrt(mean_h y^2 + norm_eps) * w[h] )
  * (RMSNorm fused without rounding y first, as the fused combine+norm gate of
  * prefill_sp.py, _combine_norm_fused, requires.)
+ *
+ * One launch (pre_fused.cu): a cluster of 16 CTAs splits each 128-row tile
+ * by hidden columns; R is read from HBM once, the 24 projections run on the
+ * tensor cores against fn split into bf16 hi + lo, and sum_h y_h^2 comes from
+ * the per-row stream Gram matrix (pre^T G pre).
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual rows

@@ -301,3 +301,9 @@ def test_host_validation_rejects_before_launch(torch, mhc):
         mhc.mhc_pre(c.dR, c.dfn, c.dscale, c.dbase, c.dw,
                     params=mhc.default_params(sinkhorn_iters=0))
     assert e.value.code == -4
+
+
+def test_no_kernel_gave_up_a_wait(torch, mhc):
+    # every bounded wait of the fused kernel completed during this session
+    torch.cuda.synchronize()
+    assert mhc.mhc_kernel_status() == 0, mhc.mhc_kernel_status_detail()
