@@ -198,7 +198,7 @@ def run_mhc(args):
     b.build()
     m.lib()
 
-    M = ROWS
+    M = args.rows
     row0 = rank * M                      # each rank: its own chunk of rows
     Rh = synth.residual(SEED, M, row0=row0)
     yh = synth.sublayer_out(SEED, M, row0=row0)
@@ -261,6 +261,23 @@ def run_mhc(args):
         ms = float(t.item())
 
     # ---- end to end: host buffers, copies inside the timed region ----------
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(m, torch, dist, world, dev, stream, step, Rh, yh, R, y, xn, R2, post, comb,
+                      bf, M, K_)
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) --------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        sample = max(threads, min(1024, threads * 48))
+        v = oracle_rows_per_s(Rh, yh, W, sample, threads)
+        cpu = {"value": v, "unit": "rows/s", "cores": threads, "kind": "oracle",
+               "sample": f"oracle pre+post on rows 0..{sample - 1} of the M={M} workload"}
+    return finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, dist)
+
+
+def run_e2e(m, torch, dist, world, dev, stream, step, Rh, yh, R, y, xn, R2, post, comb, bf, M, K_):
     e2e_steps = max(3, min(K_, 20))
     Rp = bf(Rh).pin_memory()
     yp = bf(yh).pin_memory()
@@ -296,16 +313,11 @@ def run_mhc(args):
         e2e_ms = float(t.item())
     h2d = (Rp.numel() + yp.numel()) * 2
     d2h = (xn_h.numel() + R2_h.numel()) * 2 + (post_h.numel() + comb_h.numel()) * 4
+    return {"value": world * M * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) --------
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        threads = os.cpu_count() or 1
-        sample = max(threads, min(1024, threads * 48))
-        v = oracle_rows_per_s(Rh, yh, W, sample, threads)
-        cpu = {"value": v, "unit": "rows/s", "cores": threads, "kind": "oracle",
-               "sample": f"oracle pre+post on rows 0..{sample - 1} of the M={M} workload"}
 
+def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, dist):
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -338,7 +350,7 @@ def run_mhc(args):
             "workload": f"M={M} rows per GPU: R[M,4,5120] bf16, fn[24,20480] f32, y[M,5120] bf16 "
                         f"(seed {SEED}); one step = mhc_pre + mhc_post",
             "rows_per_gpu": M,
-            "l2": "inputs larger than L2 (R alone is 671 MB per step); no flush",
+            "l2": f"inputs larger than L2 (R alone is {M * K * 2 / 1e6:.0f} MB per step); no flush",
             "achieved_gbs": gbs,
             "frac_of_hbm": gbs / hbm_peak,
             "pre_ms": pre_ms,
@@ -359,8 +371,7 @@ def run_mhc(args):
             "algorithmic_bytes_per_launch": dbytes,
         },
         "cpu_baseline": cpu,
-        "e2e": {"value": world * M * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "e2e": e2e,
         "gpu_launches": K_ * (PRE_LAUNCHES + POST_LAUNCHES),
         "clocks": clocks,
     }
@@ -376,6 +387,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rows", type=int, default=ROWS,
+                    help="rows per GPU (default: the 16384-row chunk); other sizes are "
+                         "for profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -7,33 +7,35 @@
 //
 // Decomposition.  A cluster of 16 CTAs owns a 128-row tile at a time; CTA s
 // owns hidden columns [320 s, 320 s + 320) of all four streams, i.e. 1280 of a
-// row's 20480 k.  Per tile and CTA:
-//   * TMA streams R[128 rows, 64 k] boxes (128B swizzle) through a 5-stage ring;
-//   * one thread issues tcgen05.mma (M=128 rows, N=48, K=16, bf16 -> fp32 in
-//     TMEM) against fn split into bf16 hi (rows 0..23) and lo (rows 24..47)
-//     halves, resident in shared memory for the whole kernel (120 KB), so the
-//     24 dot products carry ~2^-17 relative error per term;
-//   * 16 "Gram" warps read the same stages and accumulate, per row, the ten
-//     products G_ij = sum_h R_i[h] R_j[h] of the CTA's columns.  sum_k x_k^2 is
-//     the trace of G, and the RMSNorm of y = sum_i pre_i R_i needs only
-//     sum_h y_h^2 = pre^T G pre, so the norm is known before y is formed;
-//   * the 34 partial sums per row go to the CTA that finalises the row (CTA s
-//     owns tile rows 8s..8s+7), which pulls all 16 partials over DSMEM,
-//     reduces them in CTA order, computes rsqrt, mix, gates and the 4x4
-//     Sinkhorn (16 lanes per row), writes post/comb, and broadcasts
-//     (pre, 1/rms(y)) back to the 16 CTAs' tables;
-//   * 8 combine warps re-read the tile's own columns of R (still L2-resident:
-//     the cluster's live tile is ~5 MB) and write x_norm.
-// Roles run concurrently on consecutive tiles (two TMEM accumulators, two
-// (pre, rnorm) tables), so HBM keeps streaming while a tile is finalised.
-//
+// row's 20480 k.  fn's 24 x 1280 slice of the CTA, split into bf16 hi (B rows
+// 0..23) and lo (rows 24..47) halves, stays in shared memory (120 KB) for the
+// whole kernel, so each of the 24 dot products carries ~2^-17 relative error
+// per term.  One TMA ring (5 x 16 KB stages of R[128 rows, 64 k], 128-byte
+// swizzle) carries, per CTA, the sequence
+//     stats(0), stats(1), combine(0), stats(2), combine(1), ...
+// where stats(t) reads tile t from HBM and combine(t) reads it again one tile
+// later, while it is still resident in L2.
+//   * stats blocks: one thread issues tcgen05.mma (M=128 rows, N=48, K=16,
+//     bf16 -> fp32 in TMEM, two accumulators); 16 row warps (4 lanes per row,
+//     16 columns each) accumulate the ten per-row stream products
+//     G_ij = sum_h R_i[h] R_j[h].  sum_k x_k^2 is the trace of G and the
+//     RMSNorm of y = sum_i pre_i R_i needs only sum_h y_h^2 = pre^T G pre,
+//     so the norm is known before y is formed;
+//   * end of stats(t): the row warps read the accumulator and push each row's
+//     34 partial sums into the receive buffer of the CTA that finalises it
+//     (CTA s owns tile rows 8s..8s+7).  The owner reduces the 16 partials in
+//     CTA order, computes rsqrt, mix and the gates, pushes (pre, 1/rms(y)) to
+//     all 16 CTAs, and only then runs the 4x4 Sinkhorn (16 lanes per row) and
+//     writes post/comb;
+//   * combine blocks: the row warps form y from the four stream blocks of a
+//     64-column block and write x_norm.
 // Every row is reduced in one fixed order that depends only on its own data
-// (same MMA sequence, same Gram lanes, CTA-ordered cross-CTA sums), so any
-// row range gives the whole-chunk bits.
+// (same MMA sequence, same lanes, CTA-ordered cross-CTA sums), so any row
+// range gives the whole-chunk bits.
 //
 // Every wait is bounded (~2 s of wall time); on expiry a CTA raises an abort
-// flag, records an error word, drains its in-flight MMAs and copies, frees
-// its TMEM and returns.
+// flag, records which wait expired, drains its in-flight MMAs and copies,
+// frees its TMEM and returns.
 #include <cuda.h>
 
 #include <mutex>
@@ -48,6 +50,21 @@ __device__ unsigned int g_fused_error;
 __device__ unsigned int g_fused_where[32];
 // Bit 16 + s: a wait at site s gave up because its CTA had already aborted.
 __device__ unsigned int g_fused_where_aborted[32];
+
+#ifdef MHC_TRACE
+// Diagnostic builds only: per-CTA timestamps of pipeline events.
+constexpr int kTraceTiles = 32, kTraceEv = 16, kTraceSlots = kTraceTiles * kTraceEv;
+__device__ unsigned long long *g_trace;
+#define MHC_TRACE_AT(tile, ev)                                                         \
+  do {                                                                                 \
+    if (g_trace && (tile) < kTraceTiles)                                               \
+      g_trace[(size_t)blockIdx.x * kTraceSlots + (tile) * kTraceEv + (ev)] = now_ns(); \
+  } while (0)
+#else
+#define MHC_TRACE_AT(tile, ev) \
+  do {                         \
+  } while (0)
+#endif
 
 namespace {
 
@@ -72,34 +89,33 @@ static_assert(kHs % kBk == 0 && kTile % kCl == 0, "");
 
 // ---- warp roles -------------------------------------------------------------
 constexpr int kProducerWarp = 0, kMmaWarp = 1;
-constexpr int kGram0 = 2, kGramN = 16;
-constexpr int kOwner0 = kGram0 + kGramN, kOwnerN = 4;
-constexpr int kComb0 = kOwner0 + kOwnerN, kCombN = 8;
-constexpr int kWarps = kComb0 + kCombN;       // 30
-constexpr int kThreads = kWarps * 32;         // 960
+constexpr int kRow0 = 2, kRowN = 16;          // row warps: Gram, readout, combine
+constexpr int kOwner0 = kRow0 + kRowN, kOwnerN = 4;
+constexpr int kWarps = kOwner0 + kOwnerN;     // 22
+constexpr int kThreads = kWarps * 32;         // 704
 
 // ---- shared memory (offsets from a 1024-byte aligned base) -----------------
 constexpr int kOffFn = 0;
 constexpr int kOffStage = kOffFn + kKb * kFnBlkBytes;
-constexpr int kOffPart = kOffStage + kStages * kStageBytes;
-constexpr int kOffTab = kOffPart + kTile * kPw * 4;
-constexpr int kOffRed = kOffTab + 2 * kTile * kPreW * 4;
+constexpr int kOffRecv = kOffStage + kStages * kStageBytes;   // [16 src][8 rows][34]
+constexpr int kOffTab = kOffRecv + kCl * kOwn * kPw * 4;      // [2][128 rows][5]
+constexpr int kOffRed = kOffTab + 2 * kTile * kPreW * 4;      // [8 rows][34]
 constexpr int kOffW = kOffRed + kOwn * kPw * 4;
 constexpr int kOffBar = kOffW + kHs * 2;
 // mbarrier slots (arrays are given explicit, non-overlapping ranges)
 enum Bar : int {
   B_FULL = 0,                    // [kStages] TMA landed
-  B_EMPTY = B_FULL + kStages,    // [kStages] MMA commit + 16 Gram warps done
+  B_EMPTY = B_FULL + kStages,    // [kStages] MMA role + 16 row warps done with the stage
   B_TFULL = B_EMPTY + kStages,   // [2] accumulator complete
-  B_TEMPTY = B_TFULL + 2,        // [2] accumulator read by the 16 Gram warps
-  B_PREADY = B_TEMPTY + 2,       // partials of all 16 CTAs published (remote)
-  B_PFREE = B_PREADY + 1,        // our partials pulled by all 16 owners (remote)
+  B_TEMPTY = B_TFULL + 2,        // [2] accumulator read by the 16 row warps
+  B_PREADY = B_TEMPTY + 2,       // all 16 CTAs pushed partials to us (remote)
+  B_PFREE = B_PREADY + 1,        // all 16 owners consumed our previous push (remote)
   B_QREADY = B_PFREE + 1,        // [2] (pre, rnorm) table filled by 16 owners (remote)
   B_QFREE = B_QREADY + 2,        // [2] table consumed by all 16 CTAs (remote)
-  B_GALL = B_QFREE + 2,          // 16 Gram warps wrote their partials
-  B_OPULL = B_GALL + 1,          // 4 owner warps pulled
-  B_OTAB = B_OPULL + 1,          // 4 owner warps wrote the tables
-  B_CDONE = B_OTAB + 1,          // 8 combine warps done with a table
+  B_GALL = B_QFREE + 2,          // 16 row warps pushed their partials
+  B_OPULL = B_GALL + 1,          // 4 owner warps read the receive buffer
+  B_OTAB = B_OPULL + 1,          // 4 owner warps pushed the tables
+  B_CDONE = B_OTAB + 1,          // 16 row warps done with a combine
   B_DRAIN = B_CDONE + 1,         // final MMA drain
   B_COUNT = B_DRAIN + 1
 };
@@ -155,10 +171,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t b, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
 }
-// arrive on the barrier at the same offset in CTA `cta` of this cluster
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t b, uint32_t cta) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa(b, cta))
-               : "memory");
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Arrive on the barrier at the same offset in every CTA of the cluster: one
+// cluster-scope fence orders this thread's earlier writes (and those it has
+// observed) before the arrivals, which are then relaxed.  (A release arrive
+// per CTA would fence 16 times.)
+__device__ __forceinline__ void arrive_all_ctas(uint32_t b, uint32_t n_cta) {
+  fence_cluster();
+  for (uint32_t dst = 0; dst < n_cta; ++dst)
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa(b, dst))
+                 : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint32_t b, uint32_t parity) {
   uint32_t ok;
@@ -177,8 +199,6 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t b, uint32_t parity) {
       : "=r"(ok) : "r"(b), "r"(parity) : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
@@ -260,17 +280,6 @@ struct Abort {
   }
 };
 
-// one thread
-__device__ __forceinline__ bool wait1(uint32_t b, uint32_t parity, bool cl, const Abort &ab,
-                                      int site, int it) {
-  if (cl ? mbar_test_cluster(b, parity) : mbar_test(b, parity)) return true;
-  const uint64_t t0 = now_ns();
-  for (;;) {
-    if (cl ? mbar_test_cluster(b, parity) : mbar_test(b, parity)) return true;
-    if (*ab.flag) return ab.follow(site, it);
-    if (now_ns() - t0 > kTimeoutNs) return ab.raise(site, it);
-  }
-}
 // whole warp; the outcome is warp-uniform
 __device__ __forceinline__ bool waitw(uint32_t b, uint32_t parity, bool cl, const Abort &ab,
                                       int site, int it) {
@@ -336,20 +345,20 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
     *ab.flag = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_EMPTY + s), 1 + kGramN);
+      mbar_init(bar(B_EMPTY + s), 1 + kRowN);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_TFULL + b), 1);
-      mbar_init(bar(B_TEMPTY + b), kGramN);
+      mbar_init(bar(B_TEMPTY + b), kRowN);
       mbar_init(bar(B_QREADY + b), kCl);
       mbar_init(bar(B_QFREE + b), kCl);
     }
     mbar_init(bar(B_PREADY), kCl);
     mbar_init(bar(B_PFREE), kCl);
-    mbar_init(bar(B_GALL), kGramN);
+    mbar_init(bar(B_GALL), kRowN);
     mbar_init(bar(B_OPULL), kOwnerN);
     mbar_init(bar(B_OTAB), kOwnerN);
-    mbar_init(bar(B_CDONE), kCombN);
+    mbar_init(bar(B_CDONE), kRowN);
     mbar_init(bar(B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -389,26 +398,41 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
   const uint32_t tmem = *tmem_slot;
 
   // ---- roles -------------------------------------------------------------------
+  // Per CTA the block sequence is stats(0); then for t >= 1: stats(t),
+  // combine(t-1); and combine(T-1) last.  Every ring role walks it in order.
+  const int T = my_tiles;
   if (warp == kProducerWarp) {
-    // the whole warp walks the loop (waits are warp-collective); lane 0 issues
+    // the whole warp walks the sequence (waits are warp-collective); lane 0 issues
     int stage = 0;
     uint32_t phase = 0;
     int last[kStages];
 #pragma unroll
     for (int s = 0; s < kStages; ++s) last[s] = -1;
     bool ok = true;
-    for (int it = 0; it < my_tiles && ok; ++it) {
-      const int y = (cid + it * ncl) * kTile;
-      for (int j = 0; j < kKb; ++j) {
-        if (!waitw(bar(B_EMPTY + stage), phase ^ 1, false, ab, 1, it)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_expect_tx(bar(B_FULL + stage), kStageBytes);
-          const int x = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk;
-          tma_load_2d(sb + kOffStage + stage * kStageBytes, &tmap, x, y, bar(B_FULL + stage));
+    for (int it = 0; it <= T && ok; ++it) {
+      for (int kind = 0; kind < 2 && ok; ++kind) {
+        const int t = kind == 0 ? it : it - 1;       // stats(it), then combine(it-1)
+        if (t < 0 || t >= T) continue;
+        if (kind == 1 && lane == 0) MHC_TRACE_AT(t, 2);
+        if (kind == 1 &&
+            !waitw(bar(B_QREADY + (t & 1)), (uint32_t)(t >> 1) & 1, true, ab, 12, t)) {
+          ok = false;
+          break;
         }
-        __syncwarp();
-        last[stage] = (int)phase;
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        const int y = (cid + t * ncl) * kTile;
+        if (lane == 0) MHC_TRACE_AT(t, kind == 0 ? 0 : 3);
+        for (int j = 0; j < kKb; ++j) {
+          if (!waitw(bar(B_EMPTY + stage), phase ^ 1, false, ab, 1, t)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_expect_tx(bar(B_FULL + stage), kStageBytes);
+            const int x = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk;
+            tma_load_2d(sb + kOffStage + stage * kStageBytes, &tmap, x, y, bar(B_FULL + stage));
+          }
+          __syncwarp();
+          last[stage] = (int)phase;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (lane == 0) MHC_TRACE_AT(t, kind == 0 ? 1 : 4);
       }
     }
     // every copy issued must have landed before the CTA may exit
@@ -419,28 +443,41 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int it = 0; it < my_tiles && ok; ++it) {
-      const int buf = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
-      if (!waitw(bar(B_TEMPTY + buf), (use & 1) ^ 1, false, ab, 2, it)) break;
-      tc_fence_after();
-      const uint32_t d = tmem + (uint32_t)(buf * 64);
-      for (int j = 0; j < kKb; ++j) {
-        if (!waitw(bar(B_FULL + stage), phase, false, ab, 3, it)) { ok = false; break; }
+    for (int it = 0; it <= T && ok; ++it) {
+      if (it < T) {                                   // stats(it): 20 k-blocks into TMEM
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!waitw(bar(B_TEMPTY + buf), (use & 1) ^ 1, false, ab, 2, it)) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint64_t ad = sw128_desc(sb + kOffStage + stage * kStageBytes);
-          const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes);
+        if (lane == 0) MHC_TRACE_AT(it, 5);
+        const uint32_t d = tmem + (uint32_t)(buf * 64);
+        for (int j = 0; j < kKb; ++j) {
+          if (!waitw(bar(B_FULL + stage), phase, false, ab, 3, it)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint64_t ad = sw128_desc(sb + kOffStage + stage * kStageBytes);
+            const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBk / 16; ++kk)
-            tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (j | kk) != 0);
-          tc_commit(bar(B_EMPTY + stage));
+            for (int kk = 0; kk < kBk / 16; ++kk)
+              tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (j | kk) != 0);
+            tc_commit(bar(B_EMPTY + stage));
+          }
+          __syncwarp();
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
+        if (!ok) break;
+        if (lane == 0) tc_commit(bar(B_TFULL + buf));
+        if (lane == 0) MHC_TRACE_AT(it, 6);
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
-      if (ok && lane == 0) tc_commit(bar(B_TFULL + buf));
-      __syncwarp();
+      if (it >= 1) {                                  // combine(it-1): not ours, release
+        for (int j = 0; j < kKb; ++j) {
+          if (!waitw(bar(B_FULL + stage), phase, false, ab, 3, it - 1)) { ok = false; break; }
+          if (lane == 0) mbar_arrive(bar(B_EMPTY + stage));
+          __syncwarp();
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
     }
     // all issued MMAs complete before TMEM is freed
     if (lane == 0) tc_commit(bar(B_DRAIN));
@@ -448,164 +485,217 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
     drain1(bar(B_DRAIN), 0);
     __syncwarp();
   } else if (warp < kOwner0) {
-    // ---- Gram warps: per-row stream Gram matrix + TMEM readout ---------------
-    const int gw = warp - kGram0;
+    // ---- row warps: Gram + accumulator readout (stats), x_norm (combine) -----
+    const int rw = warp - kRow0;
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-    const int part = gw >> 2;                   // 0..3
-    const int grow = 32 * quarter + 8 * part + (lane >> 2);
+    const int part = rw >> 2;                   // 0..3
+    const int grow = 32 * quarter + 8 * part + (lane >> 2);   // row of the stage work
     const int hq = lane & 3;                    // 16 columns of a 64-column block
     const int trow = 32 * quarter + lane;       // row of this lane in TMEM
     const int sw = grow & 7;
-    float *P = reinterpret_cast<float *>(sm + kOffPart);
+    const float *tabs = reinterpret_cast<const float *>(sm + kOffTab);
+    const uint4 *wsm = reinterpret_cast<const uint4 *>(sm + kOffW);
     int stage = 0;
     uint32_t phase = 0;
-    for (int it = 0; it < my_tiles; ++it) {
-      const int buf = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
-      float g00 = 0.f, g01 = 0.f, g02 = 0.f, g03 = 0.f, g11 = 0.f, g12 = 0.f, g13 = 0.f,
-            g22 = 0.f, g23 = 0.f, g33 = 0.f;
-      uint32_t v0[8], v1[8], v2[8];
-      bool ok = true;
-      for (int j = 0; j < kKb; ++j) {
-        if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, it)) { ok = false; break; }
-        const uint8_t *st = sm + kOffStage + stage * kStageBytes + grow * 128;
-        const uint4 c0 = *reinterpret_cast<const uint4 *>(st + (((2 * hq) ^ sw) << 4));
-        const uint4 c1 = *reinterpret_cast<const uint4 *>(st + (((2 * hq + 1) ^ sw) << 4));
+    bool ok = true;
+    // 16 bf16 of this lane's row in the current stage -> fp32
+    auto load16 = [&](float (&x)[16]) {
+      const uint8_t *st = sm + kOffStage + stage * kStageBytes + grow * 128;
+      const uint4 c0 = *reinterpret_cast<const uint4 *>(st + (((2 * hq) ^ sw) << 4));
+      const uint4 c1 = *reinterpret_cast<const uint4 *>(st + (((2 * hq + 1) ^ sw) << 4));
+      const uint32_t w8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[2 * e] = lo_bf(w8[e]);
+        x[2 * e + 1] = hi_bf(w8[e]);
+      }
+    };
+    // every lane's reads of the stage are complete (their values were used)
+    // before the warp's arrival lets the producer refill it
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_EMPTY + stage));
+      if (++stage == kStages) { stage = 0; phase ^= 1; }
+    };
+    for (int it = 0; it <= T && ok; ++it) {
+      if (it < T) {
+        // ---- stats(it)
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        float g00 = 0.f, g01 = 0.f, g02 = 0.f, g03 = 0.f, g11 = 0.f, g12 = 0.f, g13 = 0.f,
+              g22 = 0.f, g23 = 0.f, g33 = 0.f;
+        float s0[16], s1[16], s2[16];
+        for (int hb = 0; hb < kHb && ok; ++hb) {
+#pragma unroll
+          for (int i = 0; i < kHC; ++i) {
+            if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, it)) { ok = false; break; }
+            if (hb == 0 && i == 0 && warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 7);
+            float x[16];
+            load16(x);
+            if (i == 0) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) { g00 = fmaf(x[e], x[e], g00); s0[e] = x[e]; }
+            } else if (i == 1) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                g11 = fmaf(x[e], x[e], g11); g01 = fmaf(s0[e], x[e], g01); s1[e] = x[e];
+              }
+            } else if (i == 2) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                g22 = fmaf(x[e], x[e], g22); g02 = fmaf(s0[e], x[e], g02);
+                g12 = fmaf(s1[e], x[e], g12); s2[e] = x[e];
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                g33 = fmaf(x[e], x[e], g33); g03 = fmaf(s0[e], x[e], g03);
+                g13 = fmaf(s1[e], x[e], g13); g23 = fmaf(s2[e], x[e], g23);
+              }
+            }
+            // the stage is released only after every lane has used its data
+            release();
+          }
+        }
+        if (!ok) break;
+        if (warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 8);
+        // accumulator: hi and lo halves of mixes 6*part .. 6*part+5 of row trow
+        if (!waitw(bar(B_TFULL + buf), use & 1, false, ab, 5, it)) break;
+        if (warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 9);
+        tc_fence_after();
+        const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * 64 + 6 * part);
+        float hv[6], lv[6];
+        tc_ld2(ta + 0, hv[0], hv[1]);
+        tc_ld2(ta + 2, hv[2], hv[3]);
+        tc_ld2(ta + 4, hv[4], hv[5]);
+        tc_ld2(ta + kMix + 0, lv[0], lv[1]);
+        tc_ld2(ta + kMix + 2, lv[2], lv[3]);
+        tc_ld2(ta + kMix + 4, lv[4], lv[5]);
+        tc_wait_ld();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_EMPTY + stage));
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
-        const uint32_t cur[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        switch (j & 3) {
-          case 0:
+        if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
+        // Gram of the row: lanes 4r'..4r'+3 hold its four column quarters
+        float gg[10] = {g00, g01, g02, g03, g11, g12, g13, g22, g23, g33};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float a0 = lo_bf(cur[e]), a1 = hi_bf(cur[e]);
-              g00 = fmaf(a0, a0, g00); g00 = fmaf(a1, a1, g00);
-              v0[e] = cur[e];
-            }
-            break;
-          case 1:
+        for (int q = 0; q < 10; ++q) {
+          gg[q] += __shfl_xor_sync(0xffffffffu, gg[q], 1);
+          gg[q] += __shfl_xor_sync(0xffffffffu, gg[q], 2);
+        }
+        // push the partials into the owners' receive buffers
+        if (!waitw(bar(B_PFREE), (uint32_t)(it & 1) ^ 1, true, ab, 6, it)) break;
+        {
+          const uint32_t dst = mapa(sb + kOffRecv +
+                                        (uint32_t)(((crank * kOwn + (trow & 7)) * kPw + 6 * part) * 4),
+                                    (uint32_t)(trow >> 3));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float a0 = lo_bf(cur[e]), a1 = hi_bf(cur[e]);
-              const float p0 = lo_bf(v0[e]), p1 = hi_bf(v0[e]);
-              g11 = fmaf(a0, a0, g11); g11 = fmaf(a1, a1, g11);
-              g01 = fmaf(p0, a0, g01); g01 = fmaf(p1, a1, g01);
-              v1[e] = cur[e];
-            }
-            break;
-          case 2:
+          for (int q = 0; q < 6; ++q)
+            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4 * q), "f"(hv[q] + lv[q])
+                         : "memory");
+          if (hq == 0) {
+            const uint32_t dg = mapa(sb + kOffRecv +
+                                         (uint32_t)(((crank * kOwn + (grow & 7)) * kPw + kMix) * 4),
+                                     (uint32_t)(grow >> 3));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float a0 = lo_bf(cur[e]), a1 = hi_bf(cur[e]);
-              const float p0 = lo_bf(v0[e]), p1 = hi_bf(v0[e]);
-              const float q0 = lo_bf(v1[e]), q1 = hi_bf(v1[e]);
-              g22 = fmaf(a0, a0, g22); g22 = fmaf(a1, a1, g22);
-              g02 = fmaf(p0, a0, g02); g02 = fmaf(p1, a1, g02);
-              g12 = fmaf(q0, a0, g12); g12 = fmaf(q1, a1, g12);
-              v2[e] = cur[e];
-            }
-            break;
-          default:
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float a0 = lo_bf(cur[e]), a1 = hi_bf(cur[e]);
-              const float p0 = lo_bf(v0[e]), p1 = hi_bf(v0[e]);
-              const float q0 = lo_bf(v1[e]), q1 = hi_bf(v1[e]);
-              const float r0 = lo_bf(v2[e]), r1 = hi_bf(v2[e]);
-              g33 = fmaf(a0, a0, g33); g33 = fmaf(a1, a1, g33);
-              g03 = fmaf(p0, a0, g03); g03 = fmaf(p1, a1, g03);
-              g13 = fmaf(q0, a0, g13); g13 = fmaf(q1, a1, g13);
-              g23 = fmaf(r0, a0, g23); g23 = fmaf(r1, a1, g23);
-            }
-            break;
+            for (int q = 0; q < 10; ++q)
+              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dg + 4 * q), "f"(gg[q])
+                           : "memory");
+          }
+        }
+        fence_cluster();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_GALL));
+        if (warp == kRow0) {
+          if (!waitw(bar(B_GALL), (uint32_t)(it & 1), false, ab, 7, it)) break;
+          if (lane == 0)
+            arrive_all_ctas(bar(B_PREADY), kCl);
+          if (lane == 0) MHC_TRACE_AT(it, 10);
+          __syncwarp();
         }
       }
-      if (!ok) break;
-      // this tile's accumulator: hi and lo halves of 6 of the 24 mixes
-      if (!waitw(bar(B_TFULL + buf), use & 1, false, ab, 5, it)) break;
-      tc_fence_after();
-      const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * 64 + 6 * part);
-      float hv[6], lv[6];   // columns 6p..6p+5 (hi) and 24+6p.. (lo), even-aligned pairs
-      tc_ld2(ta + 0, hv[0], hv[1]);
-      tc_ld2(ta + 2, hv[2], hv[3]);
-      tc_ld2(ta + 4, hv[4], hv[5]);
-      tc_ld2(ta + kMix + 0, lv[0], lv[1]);
-      tc_ld2(ta + kMix + 2, lv[2], lv[3]);
-      tc_ld2(ta + kMix + 4, lv[4], lv[5]);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
-      // Gram partials of the row: lanes 4r'..4r'+3 hold its four column quarters
-      float gg[10] = {g00, g01, g02, g03, g11, g12, g13, g22, g23, g33};
+      if (it >= 1) {
+        // ---- combine(t): y = sum_i pre_i R_i, x_norm = bf16(y * rnorm * w)
+        const int t = it - 1;
+        if (!waitw(bar(B_QREADY + (t & 1)), (uint32_t)(t >> 1) & 1, true, ab, 12, t)) break;
+        if (warp == kRow0 && lane == 0) MHC_TRACE_AT(t, 11);
+        const float *tr = tabs + ((t & 1) * kTile + grow) * kPreW;
+        const float p0 = tr[0], p1 = tr[1], p2 = tr[2], p3 = tr[3], rn = tr[4];
+        const int64_t grow_g = (int64_t)(cid + t * ncl) * kTile + grow;
+        const bool live = grow_g < a.rows;
+        for (int hb = 0; hb < kHb && ok; ++hb) {
+          float yv[16];
 #pragma unroll
-      for (int t = 0; t < 10; ++t) {
-        gg[t] += __shfl_xor_sync(0xffffffffu, gg[t], 1);
-        gg[t] += __shfl_xor_sync(0xffffffffu, gg[t], 2);
-      }
-      if (!waitw(bar(B_PFREE), (uint32_t)(it & 1) ^ 1, true, ab, 6, it)) break;
-      float *pr = P + trow * kPw + 6 * part;
+          for (int i = 0; i < kHC; ++i) {
+            if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, t)) { ok = false; break; }
+            float x[16];
+            load16(x);
+            const float pi = i == 0 ? p0 : (i == 1 ? p1 : (i == 2 ? p2 : p3));
 #pragma unroll
-      for (int t = 0; t < 6; ++t) pr[t] = hv[t] + lv[t];
-      if (hq == 0) {
+            for (int e = 0; e < 16; ++e) yv[e] = i == 0 ? pi * x[e] : fmaf(pi, x[e], yv[e]);
+            release();
+          }
+          if (!ok) break;
+          if (live) {
+            const uint4 wa = wsm[(kBk * hb + 16 * hq) / 8], wb = wsm[(kBk * hb + 16 * hq) / 8 + 1];
+            const uint32_t ww[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+            uint32_t ow[8];
 #pragma unroll
-        for (int t = 0; t < 10; ++t) P[grow * kPw + kMix + t] = gg[t];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_GALL));
-      if (warp == kGram0) {
-        if (!waitw(bar(B_GALL), (uint32_t)(it & 1), false, ab, 7, it)) break;
-        if (lane == 0) {
-          fence_cluster();
-          for (uint32_t dst = 0; dst < kCl; ++dst) mbar_arrive_remote(bar(B_PREADY), dst);
+            for (int e = 0; e < 8; ++e)
+              ow[e] = pack2_rn((yv[2 * e] * rn) * lo_bf(ww[e]), (yv[2 * e + 1] * rn) * hi_bf(ww[e]));
+            uint4 *dst = reinterpret_cast<uint4 *>(a.x_norm + grow_g * kH + (int64_t)crank * kHs +
+                                                   kBk * hb + 16 * hq);
+            st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+            st_stream(dst + 1, make_uint4(ow[4], ow[5], ow[6], ow[7]));
+          }
         }
+        if (!ok) break;
         __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_CDONE));
+        if (warp == kRow0) {
+          if (!waitw(bar(B_CDONE), (uint32_t)(t & 1), false, ab, 13, t)) break;
+          if (lane == 0)
+            arrive_all_ctas(bar(B_QFREE + (t & 1)), kCl);
+          if (lane == 0) MHC_TRACE_AT(t, 12);
+          __syncwarp();
+        }
       }
     }
-  } else if (warp < kComb0) {
+  } else {
     // ---- owner warps: finalise 8 rows of each tile --------------------------
     const int o = threadIdx.x - kOwner0 * 32;   // 0..127
     const int q = o >> 4, e = o & 15;           // row of 8, lane of 16
     const int row_t = (int)crank * kOwn + q;
+    const float *recv = reinterpret_cast<const float *>(sm + kOffRecv);
     float *red = reinterpret_cast<float *>(sm + kOffRed);
     const float sc0 = __ldg(a.scale), sc1 = __ldg(a.scale + 1), sc2 = __ldg(a.scale + 2);
     const float bcomb = __ldg(a.base + 8 + e);
     const float bgate = e < 8 ? __ldg(a.base + e) : 0.f;
-    // a row's 16 lanes are one half of the warp; xor 1/2/4/8 stay inside it
-    const unsigned gmask = 0xffffffffu;
-    for (int it = 0; it < my_tiles; ++it) {
+    const unsigned full = 0xffffffffu;          // a row's 16 lanes are half the warp
+    const int gb = lane & 16;
+    for (int it = 0; it < T; ++it) {
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       const int64_t grow = (int64_t)(cid + it * ncl) * kTile + row_t;
       if (!waitw(bar(B_PREADY), (uint32_t)(it & 1), true, ab, 8, it)) break;
-      // pull this row's 34 partials from the 16 CTAs, summed in CTA order
-      const uint32_t pa = sb + kOffPart + (uint32_t)(row_t * kPw) * 4u;
+      if (warp == kOwner0 && lane == 0) MHC_TRACE_AT(it, 13);
+      // this row's 34 partials from the 16 CTAs, summed in CTA order
       float acc[3] = {0.f, 0.f, 0.f};
 #pragma unroll
       for (int w3 = 0; w3 < 3; ++w3) {
         const int v = e + 16 * w3;
         if (v < kPw) {
-          float tv[kCl];
+          float sacc = 0.f;
 #pragma unroll
-          for (int src = 0; src < kCl; ++src) {
-            asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                         : "=f"(tv[src]) : "r"(mapa(pa + 4u * (uint32_t)v, (uint32_t)src)));
-          }
-          float s = 0.f;
-#pragma unroll
-          for (int src = 0; src < kCl; ++src) s += tv[src];
-          acc[w3] = s;
+          for (int src = 0; src < kCl; ++src) sacc += recv[(src * kOwn + q) * kPw + v];
+          acc[w3] = sacc;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_OPULL));
       if (warp == kOwner0) {
         if (!waitw(bar(B_OPULL), (uint32_t)(it & 1), false, ab, 9, it)) break;
-        if (lane == 0) {
-          fence_cluster();
-          for (uint32_t dst = 0; dst < kCl; ++dst) mbar_arrive_remote(bar(B_PFREE), dst);
-        }
+        if (lane == 0)
+          arrive_all_ctas(bar(B_PFREE), kCl);
         __syncwarp();
       }
       float *rq = red + q * kPw;
@@ -617,16 +707,6 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
       const float G12 = rq[29], G13 = rq[30], G22 = rq[31], G23 = rq[32], G33 = rq[33];
       const float ss = ((G00 + G11) + G22) + G33;
       const float rsq = 1.0f / sqrtf(ss / (float)kK + a.rms_eps);
-      // Sinkhorn on exp(logits): lane e holds comb[e/4][e%4]
-      float C = expf(fmaf(rq[8 + e] * rsq, sc2, bcomb));
-      for (int t = 0; t < a.iters; ++t) {
-        float rs = C + __shfl_xor_sync(gmask, C, 1);
-        rs = rs + __shfl_xor_sync(gmask, rs, 2);
-        C = C / (rs + a.sink_eps);
-        float cs = C + __shfl_xor_sync(gmask, C, 4);
-        cs = cs + __shfl_xor_sync(gmask, cs, 8);
-        C = C / (cs + a.sink_eps);
-      }
       // gates: lanes 0..3 pre, 4..7 post
       float gate = 0.f;
       if (e < 8) {
@@ -634,25 +714,15 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
         const float sg = 1.0f / (1.0f + expf(-l));
         gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
       }
-      const int gb = lane & 16;
-      const float p0 = __shfl_sync(gmask, gate, gb + 0), p1 = __shfl_sync(gmask, gate, gb + 1);
-      const float p2 = __shfl_sync(gmask, gate, gb + 2), p3 = __shfl_sync(gmask, gate, gb + 3);
+      const float p0 = __shfl_sync(full, gate, gb + 0), p1 = __shfl_sync(full, gate, gb + 1);
+      const float p2 = __shfl_sync(full, gate, gb + 2), p3 = __shfl_sync(full, gate, gb + 3);
       // sum_h y_h^2 = pre^T G pre
       float yy = p0 * p0 * G00 + p1 * p1 * G11 + p2 * p2 * G22 + p3 * p3 * G33;
       yy += 2.0f * (p0 * p1 * G01 + p0 * p2 * G02 + p0 * p3 * G03 + p1 * p2 * G12 +
                     p1 * p3 * G13 + p2 * p3 * G23);
       yy = fmaxf(yy, 0.f);
       const float rn = 1.0f / sqrtf(yy / (float)kH + a.norm_eps);
-      if (grow < a.rows) {
-        a.comb[grow * 16 + e] = C;
-        if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
-        if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
-        if (a.mix_out) {
-          a.mix_out[grow * kMix + e] = rq[e] * rsq;
-          if (e < 8) a.mix_out[grow * kMix + 16 + e] = rq[16 + e] * rsq;
-        }
-      }
-      // (pre, rnorm) of this row into table `buf` of CTA e
+      // (pre, rnorm) of this row into table `buf` of CTA e: the combines wait on it
       if (!waitw(bar(B_QFREE + buf), (use & 1) ^ 1, true, ab, 10, it)) break;
       const uint32_t ta = mapa(sb + kOffTab + (uint32_t)((buf * kTile + row_t) * kPreW) * 4u, (uint32_t)e);
       asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ta), "f"(p0) : "memory");
@@ -665,83 +735,32 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
       if (lane == 0) mbar_arrive(bar(B_OTAB));
       if (warp == kOwner0) {
         if (!waitw(bar(B_OTAB), (uint32_t)(it & 1), false, ab, 11, it)) break;
-        if (lane == 0) {
-          fence_cluster();
-          for (uint32_t dst = 0; dst < kCl; ++dst) mbar_arrive_remote(bar(B_QREADY + buf), dst);
-        }
+        if (lane == 0)
+          arrive_all_ctas(bar(B_QREADY + buf), kCl);
+        if (lane == 0) MHC_TRACE_AT(it, 14);
         __syncwarp();
       }
-    }
-  } else {
-    // ---- combine warps: x_norm of this CTA's 320 columns ---------------------
-    const int ct = threadIdx.x - kComb0 * 32;    // 0..255
-    const float *tabs = reinterpret_cast<const float *>(sm + kOffTab);
-    const uint4 *wv = reinterpret_cast<const uint4 *>(sm + kOffW);
-    for (int it = 0; it < my_tiles; ++it) {
-      const int buf = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
-      const int64_t row0 = (int64_t)(cid + it * ncl) * kTile;
-      if (!waitw(bar(B_QREADY + buf), use & 1, true, ab, 12, it)) break;
-      const float *tab = tabs + buf * kTile * kPreW;
-      constexpr int kItems = kTile * kChunks;          // 5120
-      constexpr int kPer = kItems / (kCombN * 32);     // 20
-#pragma unroll 1
-      for (int n = 0; n < kPer; n += 2) {
-        uint4 rv[2][kHC];
-        int rt[2], cc[2];
-        bool live[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int item = ct + (kCombN * 32) * (n + u);
-          rt[u] = item / kChunks;
-          cc[u] = item - rt[u] * kChunks;
-          live[u] = row0 + rt[u] < a.rows;
-          if (live[u]) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                a.R + (row0 + rt[u]) * kK + (int64_t)crank * kHs + 8 * cc[u]);
-#pragma unroll
-            for (int i = 0; i < kHC; ++i) rv[u][i] = ld_stream(src + i * (kH / 8));
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (!live[u]) continue;
-          const float *tr = tab + rt[u] * kPreW;
-          const float q0 = tr[0], q1 = tr[1], q2 = tr[2], q3 = tr[3], rn = tr[4];
-          const uint4 wq = wv[cc[u]];
-          const uint32_t ww[4] = {wq.x, wq.y, wq.z, wq.w};
-          const uint32_t s0[4] = {rv[u][0].x, rv[u][0].y, rv[u][0].z, rv[u][0].w};
-          const uint32_t s1[4] = {rv[u][1].x, rv[u][1].y, rv[u][1].z, rv[u][1].w};
-          const uint32_t s2[4] = {rv[u][2].x, rv[u][2].y, rv[u][2].z, rv[u][2].w};
-          const uint32_t s3[4] = {rv[u][3].x, rv[u][3].y, rv[u][3].z, rv[u][3].w};
-          uint32_t ow[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            float ya = q0 * lo_bf(s0[x]);
-            ya = fmaf(q1, lo_bf(s1[x]), ya);
-            ya = fmaf(q2, lo_bf(s2[x]), ya);
-            ya = fmaf(q3, lo_bf(s3[x]), ya);
-            float yb = q0 * hi_bf(s0[x]);
-            yb = fmaf(q1, hi_bf(s1[x]), yb);
-            yb = fmaf(q2, hi_bf(s2[x]), yb);
-            yb = fmaf(q3, hi_bf(s3[x]), yb);
-            ow[x] = pack2_rn((ya * rn) * lo_bf(ww[x]), (yb * rn) * hi_bf(ww[x]));
-          }
-          st_stream(reinterpret_cast<uint4 *>(a.x_norm + (row0 + rt[u]) * kH +
-                                              (int64_t)crank * kHs + 8 * cc[u]),
-                    make_uint4(ow[0], ow[1], ow[2], ow[3]));
+      // Sinkhorn on exp(logits), off the combine's critical path: lane e holds comb[e/4][e%4]
+      float C = expf(fmaf(rq[8 + e] * rsq, sc2, bcomb));
+      for (int k = 0; k < a.iters; ++k) {
+        float rs = C + __shfl_xor_sync(full, C, 1);
+        rs = rs + __shfl_xor_sync(full, rs, 2);
+        C = C / (rs + a.sink_eps);
+        float cs = C + __shfl_xor_sync(full, C, 4);
+        cs = cs + __shfl_xor_sync(full, cs, 8);
+        C = C / (cs + a.sink_eps);
+      }
+      if (warp == kOwner0 && lane == 0) MHC_TRACE_AT(it, 15);
+      if (grow < a.rows) {
+        a.comb[grow * 16 + e] = C;
+        if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
+        if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
+        if (a.mix_out) {
+          a.mix_out[grow * kMix + e] = rq[e] * rsq;
+          if (e < 8) a.mix_out[grow * kMix + 16 + e] = rq[16 + e] * rsq;
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_CDONE));
-      if (warp == kComb0) {
-        if (!waitw(bar(B_CDONE), (uint32_t)(it & 1), false, ab, 13, it)) break;
-        if (lane == 0) {
-          fence_cluster();
-          for (uint32_t dst = 0; dst < kCl; ++dst) mbar_arrive_remote(bar(B_QFREE + buf), dst);
-        }
-        __syncwarp();
-      }
     }
   }
 
@@ -867,6 +886,12 @@ cudaError_t launch_pre_fused(const uint16_t *R, const float *fn, const float *sc
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, pre_fused_kernel, map, a);
 }
+
+#ifdef MHC_TRACE
+extern "C" int mhc_trace_set(void *buf) {
+  return (int)cudaMemcpyToSymbol(g_trace, &buf, sizeof buf);
+}
+#endif
 
 cudaError_t fused_error_word(unsigned int *out, bool reset) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_fused_error, sizeof(unsigned int));
