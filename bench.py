@@ -41,8 +41,8 @@ SEED = 4
 PRE_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4          # 51,280
 POST_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4 + K * 2  # 92,240
 PRE_BYTES_CALL = MIX * K * 4 + H * 2 + 3 * 4 + MIX * 4         # fn, norm_w, scale, base
-PRE_LAUNCHES, POST_LAUNCHES = 1, 1                             # kernels per call
-DOMINANT_SRC = {"mhc_pre": ["pre_fused.cu"], "mhc_post": ["post.cu"]}
+PRE_LAUNCHES, POST_LAUNCHES = 2, 1                             # kernels per call
+DOMINANT_SRC = {"mhc_pre": ["pre_stats.cu", "pre_simt.cu"], "mhc_post": ["post.cu"]}
 
 
 def peaks():

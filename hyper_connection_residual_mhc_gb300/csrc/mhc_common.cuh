@@ -65,13 +65,13 @@ cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *sca
                             uint16_t *x_norm, float *post, float *comb, float *pre_out,
                             float *mix_out, cudaStream_t s);
 
-// fused single-launch pre path (tensor-core stats, cluster of 16 CTAs)
-cudaError_t launch_pre_fused(const uint16_t *R, const float *fn, const float *scale,
-                             const float *base, const uint16_t *norm_w, int64_t rows,
-                             int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
-                             float *post, float *comb, float *pre_out, float *mix_out,
-                             cudaStream_t s);
-// the fused kernel's error word (nonzero once a bounded wait expired)
+// tensor-core stats half of mhc_pre (cluster of 16 CTAs): writes the pre gates
+// to pre_ws [rows, 4] for the combine launch, and post, comb (+ pre_out, mix_out)
+cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
+                             const float *base, int64_t rows, int64_t logical_rows,
+                             const mhc_params &p, float *pre_ws, float *post, float *comb,
+                             float *pre_out, float *mix_out, cudaStream_t s);
+// the stats kernel's error word (nonzero once a bounded wait expired)
 cudaError_t fused_error_word(unsigned int *out, bool reset);
 cudaError_t fused_error_where(unsigned int *out32);
 

@@ -147,7 +147,9 @@ static_assert(kChunksPerStream % kCnThreads == 0, "");
 __global__ void __launch_bounds__(kCnThreads)
 combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
                     const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out) {
-  const int64_t row = blockIdx.x;
+  // last rows first: after mhc_pre's stats launch the most recently read rows
+  // are the ones still in L2
+  const int64_t row = (int64_t)gridDim.x - 1 - blockIdx.x;
   const int tid = threadIdx.x;
   const float4 pq = __ldg(pre + row);
   const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};

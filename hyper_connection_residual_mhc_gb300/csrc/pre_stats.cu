@@ -1,34 +1,32 @@
-// pre_fused.cu -- mhc_pre in one launch on GB300: stats on the 5th-generation
-// tensor cores, split/Sinkhorn, combine + RMSNorm, reading R from HBM once.
+// pre_stats.cu -- the stats half of mhc_pre on GB300: per row, the 24
+// projections of the flattened residual on the 5th-generation tensor cores,
+// the row's sum of squares, and the split into gates and the Sinkhorn mix.
 //
-// Definitions: deepseek_v4.py (sglang), DeepseekV4DecoderLayer.hc_pre
-// (hc_pre_torch_impl, hc_split_sinkhorn, the combine) with RMSNorm fused as in
-// prefill_sp.py, hc_combine_norm_rows.
+// Definitions: deepseek_v4.py (sglang), DeepseekV4DecoderLayer.hc_pre:
+// hc_pre_torch_impl (rsqrt of mean(x^2) + rms_eps; mixes = (x @ fn^T) * rsqrt)
+// and hc_split_sinkhorn (gates and the 4x4 Sinkhorn).
 //
 // Decomposition.  A cluster of 16 CTAs owns a 128-row tile at a time; CTA s
 // owns hidden columns [320 s, 320 s + 320) of all four streams, i.e. 1280 of a
 // row's 20480 k.  fn's 24 x 1280 slice of the CTA, split into bf16 hi (B rows
 // 0..23) and lo (rows 24..47) halves, stays in shared memory (120 KB) for the
-// whole kernel, so each of the 24 dot products carries ~2^-17 relative error
-// per term.  One TMA ring (5 x 16 KB stages of R[128 rows, 64 k], 128-byte
-// swizzle) carries, per CTA, the sequence
-//     stats(0), stats(1), combine(0), stats(2), combine(1), ...
-// where stats(t) reads tile t from HBM and combine(t) reads it again one tile
-// later, while it is still resident in L2.
-//   * stats blocks: one thread issues tcgen05.mma (M=128 rows, N=48, K=16,
-//     bf16 -> fp32 in TMEM, two accumulators); 16 row warps (4 lanes per row,
-//     16 columns each) accumulate the ten per-row stream products
-//     G_ij = sum_h R_i[h] R_j[h].  sum_k x_k^2 is the trace of G and the
-//     RMSNorm of y = sum_i pre_i R_i needs only sum_h y_h^2 = pre^T G pre,
-//     so the norm is known before y is formed;
-//   * end of stats(t): the row warps read the accumulator and push each row's
-//     34 partial sums into the receive buffer of the CTA that finalises it
-//     (CTA s owns tile rows 8s..8s+7).  The owner reduces the 16 partials in
-//     CTA order, computes rsqrt, mix and the gates, pushes (pre, 1/rms(y)) to
-//     all 16 CTAs, and only then runs the 4x4 Sinkhorn (16 lanes per row) and
-//     writes post/comb;
-//   * combine blocks: the row warps form y from the four stream blocks of a
-//     64-column block and write x_norm.
+// whole kernel, so each product is exact and the dot products carry ~2^-17
+// relative error per term.  Per tile and CTA:
+//   * TMA streams R[128 rows, 64 k] boxes (128-byte swizzle) through a
+//     5-stage ring -- R is read from HBM exactly once;
+//   * one thread issues tcgen05.mma (M=128 rows, N=48, K=16, bf16 -> fp32,
+//     two accumulators in tensor memory);
+//   * 16 row warps (4 lanes per row, 16 columns each) accumulate sum x^2 from
+//     the same stages, then read the accumulator and push each row's 24 mix
+//     partials and its sum of squares into the receive buffer of the CTA
+//     that finalises the row (CTA s owns tile rows 8s..8s+7);
+//   * 4 owner warps reduce the 16 partials of a row in CTA order, compute
+//     rsqrt, mix, the gates and the 4x4 Sinkhorn (16 lanes per row) and write
+//     pre, post and comb.
+// The combine + RMSNorm (x_norm) runs as a second, streaming launch
+// (pre_simt.cu, combine_norm_kernel) that reads the pre gates this kernel
+// writes.
+//
 // Every row is reduced in one fixed order that depends only on its own data
 // (same MMA sequence, same lanes, CTA-ordered cross-CTA sums), so any row
 // range gives the whole-chunk bits.
@@ -44,11 +42,11 @@
 
 namespace mhc {
 
-// Bit s set: a bounded wait at site s expired (sites are numbered in the
-// kernel); g_fused_where[s] holds (tile << 8) | cluster rank of the last one.
+// Bit s set: a bounded wait at site s expired; g_fused_where[s] holds
+// (tile << 8) | cluster rank of the last one.  Bit 16 + s: a wait at site s
+// gave up because its CTA had already aborted (g_fused_where_aborted[s]).
 __device__ unsigned int g_fused_error;
 __device__ unsigned int g_fused_where[32];
-// Bit 16 + s: a wait at site s gave up because its CTA had already aborted.
 __device__ unsigned int g_fused_where_aborted[32];
 
 #ifdef MHC_TRACE
@@ -79,52 +77,55 @@ constexpr int kStages = 5;
 constexpr int kN = 2 * kMix;                  // 48 = fn hi (24) + fn lo (24)
 constexpr int kStageBytes = kTile * kBk * 2;  // 16384
 constexpr int kFnBlkBytes = kN * kBk * 2;     // 6144
-constexpr int kPw = 34;                       // partial words per row: 24 dots + 10 Gram
+constexpr int kRw = 28;                       // receive words per row: 24 dots, sum x^2, pad
 constexpr int kOwn = kTile / kCl;             // 8 rows finalised per CTA
-constexpr int kPreW = 5;                      // table words per row: pre0..3, rnorm
-constexpr int kChunks = kHs / 8;              // 40 16-byte chunks per stream and row
 constexpr int kTmemCols = 128;                // two 48-column accumulators at 0 and 64
 
 static_assert(kHs % kBk == 0 && kTile % kCl == 0, "");
 
 // ---- warp roles -------------------------------------------------------------
+// warp 0 producer, 1 MMA; 4..7 row warps and 8..11 readout warps (warp & 3 =
+// the TMEM lane quarter, one thread per tile row); 2, 3, 12, 13 owners
 constexpr int kProducerWarp = 0, kMmaWarp = 1;
-constexpr int kRow0 = 2, kRowN = 16;          // row warps: Gram, readout, combine
-constexpr int kOwner0 = kRow0 + kRowN, kOwnerN = 4;
-constexpr int kWarps = kOwner0 + kOwnerN;     // 22
-constexpr int kThreads = kWarps * 32;         // 704
+constexpr int kRow0 = 4, kRowN = 4;           // sum x^2 from the stages
+constexpr int kRead0 = 8, kReadN = 4;         // accumulator readout + push
+constexpr int kOwnerN = 4;
+constexpr int kOwnerLead = 2;                 // owner warp that broadcasts PFREE
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;         // 448
+__device__ __forceinline__ int owner_index(int warp) {   // -1: not an owner warp
+  return warp == 2 || warp == 3 ? warp - 2 : (warp == 12 || warp == 13 ? warp - 10 : -1);
+}
 
 // ---- shared memory (offsets from a 1024-byte aligned base) -----------------
 constexpr int kOffFn = 0;
 constexpr int kOffStage = kOffFn + kKb * kFnBlkBytes;
-constexpr int kOffRecv = kOffStage + kStages * kStageBytes;   // [16 src][8 rows][34]
-constexpr int kOffTab = kOffRecv + kCl * kOwn * kPw * 4;      // [2][128 rows][5]
-constexpr int kOffRed = kOffTab + 2 * kTile * kPreW * 4;      // [8 rows][34]
-constexpr int kOffW = kOffRed + kOwn * kPw * 4;
-constexpr int kOffBar = kOffW + kHs * 2;
+constexpr int kOffRecv = kOffStage + kStages * kStageBytes;   // [16 src][8 rows][kRw]
+constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;      // [8 rows][kRw]
+constexpr int kOffSs = kOffRed + kOwn * kRw * 4;              // [2][128 rows] sum x^2
+constexpr int kOffBar = kOffSs + 2 * kTile * 4;
 // mbarrier slots (arrays are given explicit, non-overlapping ranges)
 enum Bar : int {
   B_FULL = 0,                    // [kStages] TMA landed
-  B_EMPTY = B_FULL + kStages,    // [kStages] MMA role + 16 row warps done with the stage
+  B_EMPTY = B_FULL + kStages,    // [kStages] MMA commit + 4 row warps done with the stage
   B_TFULL = B_EMPTY + kStages,   // [2] accumulator complete
-  B_TEMPTY = B_TFULL + 2,        // [2] accumulator read by the 16 row warps
+  B_TEMPTY = B_TFULL + 2,        // [2] accumulator and sum x^2 read by the readout warps
   B_PREADY = B_TEMPTY + 2,       // all 16 CTAs pushed partials to us (remote)
   B_PFREE = B_PREADY + 1,        // all 16 owners consumed our previous push (remote)
-  B_QREADY = B_PFREE + 1,        // [2] (pre, rnorm) table filled by 16 owners (remote)
-  B_QFREE = B_QREADY + 2,        // [2] table consumed by all 16 CTAs (remote)
-  B_GALL = B_QFREE + 2,          // 16 row warps pushed their partials
+  B_GALL = B_PFREE + 1,          // the readout warps pushed their partials
   B_OPULL = B_GALL + 1,          // 4 owner warps read the receive buffer
-  B_OTAB = B_OPULL + 1,          // 4 owner warps pushed the tables
-  B_CDONE = B_OTAB + 1,          // 16 row warps done with a combine
-  B_DRAIN = B_CDONE + 1,         // final MMA drain
-  B_COUNT = B_DRAIN + 1
+  B_DRAIN = B_OPULL + 1,         // final MMA drain
+  B_FNREADY = B_DRAIN + 1,       // fn hi/lo tiles written (all warps but the producer)
+  B_SSREADY = B_FNREADY + 1,     // [2] the row warps wrote a tile's sum x^2
+  B_COUNT = B_SSREADY + 2
 };
-static_assert(B_COUNT == 2 * kStages + 2 + 2 + 1 + 1 + 2 + 2 + 5, "barrier slots overlap");
+static_assert(B_COUNT == 2 * kStages + 2 + 2 + 6 + 2, "barrier slots overlap");
 constexpr int kOffMisc = kOffBar + B_COUNT * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
 static_assert(kOffStage % 1024 == 0 && kFnBlkBytes % 1024 == 0, "SW128 tiles need 1024-B alignment");
+static_assert(kOffRecv % 16 == 0 && (kRw * 4) % 16 == 0, "receive rows must take 16-byte stores");
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
@@ -245,6 +246,18 @@ __device__ __forceinline__ void tc_ld2(uint32_t taddr, float &v0, float &v1) {
   v0 = __uint_as_float(r0);
   v1 = __uint_as_float(r1);
 }
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -309,25 +322,32 @@ __device__ __forceinline__ void drain1(uint32_t b, uint32_t parity) {
 __device__ __forceinline__ float lo_bf(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-struct FusedArgs {
+struct StatsArgs {
   const float *fn;
   const float *scale;
   const float *base;
-  const uint16_t *norm_w;
-  const uint16_t *R;
-  uint16_t *x_norm;
+  float *pre_ws;     // [rows, 4] pre gates for the combine launch
   float *post;
   float *comb;
   float *pre_out;
   float *mix_out;
   int64_t rows;
   int num_tiles;
-  float rms_eps, pre_eps, sink_eps, norm_eps, post_mult;
+  float rms_eps, pre_eps, sink_eps, post_mult;
   int iters;
 };
 
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
+pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -335,7 +355,7 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_rank();
   const int cid = (int)cluster_id(), ncl = (int)cluster_count();
-  const int my_tiles = cid < a.num_tiles ? (a.num_tiles - 1 - cid) / ncl + 1 : 0;
+  const int T = cid < a.num_tiles ? (a.num_tiles - 1 - cid) / ncl + 1 : 0;   // our tiles
   auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8u * (uint32_t)i; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
   Abort ab{reinterpret_cast<volatile int *>(sm + kOffMisc + 4), crank};
@@ -349,24 +369,29 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_TFULL + b), 1);
-      mbar_init(bar(B_TEMPTY + b), kRowN);
-      mbar_init(bar(B_QREADY + b), kCl);
-      mbar_init(bar(B_QFREE + b), kCl);
+      mbar_init(bar(B_TEMPTY + b), kReadN);
+      mbar_init(bar(B_SSREADY + b), kRowN);
     }
     mbar_init(bar(B_PREADY), kCl);
     mbar_init(bar(B_PFREE), kCl);
-    mbar_init(bar(B_GALL), kRowN);
+    mbar_init(bar(B_GALL), kReadN);
     mbar_init(bar(B_OPULL), kOwnerN);
-    mbar_init(bar(B_OTAB), kOwnerN);
-    mbar_init(bar(B_CDONE), kRowN);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_FNREADY), kWarps - 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync_all();
+  const uint32_t tmem = *tmem_slot;
 
-  // fn columns of this CTA -> bf16 hi/lo B tiles (K-major, 128-byte swizzle):
+  // fn columns of this CTA -> bf16 hi/lo B tiles (K-major, 128-byte swizzle),
+  // written by every warp but the producer, which meanwhile starts streaming R:
   // k-block j covers k = (j%4)*5120 + 320*crank + 64*(j/4) + [0, 64)
-  for (int item = threadIdx.x; item < kMix * kKb * 8; item += kThreads) {
+  if (warp != kProducerWarp) {
+  for (int item = threadIdx.x - 32; item < kMix * kKb * 8; item += kThreads - 32) {
     const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
     const int k0 = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk + 8 * q;
     const float4 f0 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0));
@@ -387,53 +412,36 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
     *reinterpret_cast<uint4 *>(tile + (nl >> 3) * 1024 + (nl & 7) * 128 + ((q ^ (nl & 7)) << 4)) =
         make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
-  if (threadIdx.x < kChunks)
-    reinterpret_cast<uint4 *>(sm + kOffW)[threadIdx.x] =
-        __ldg(reinterpret_cast<const uint4 *>(a.norm_w + crank * kHs) + threadIdx.x);
+  // generic-proxy writes -> visible to the tensor core (async proxy)
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  cluster_sync_all();
-  const uint32_t tmem = *tmem_slot;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar(B_FNREADY));
+  }
 
   // ---- roles -------------------------------------------------------------------
-  // Per CTA the block sequence is stats(0); then for t >= 1: stats(t),
-  // combine(t-1); and combine(T-1) last.  Every ring role walks it in order.
-  const int T = my_tiles;
   if (warp == kProducerWarp) {
-    // the whole warp walks the sequence (waits are warp-collective); lane 0 issues
+    // the whole warp walks the loop (waits are warp-collective); lane 0 issues
     int stage = 0;
     uint32_t phase = 0;
     int last[kStages];
 #pragma unroll
     for (int s = 0; s < kStages; ++s) last[s] = -1;
     bool ok = true;
-    for (int it = 0; it <= T && ok; ++it) {
-      for (int kind = 0; kind < 2 && ok; ++kind) {
-        const int t = kind == 0 ? it : it - 1;       // stats(it), then combine(it-1)
-        if (t < 0 || t >= T) continue;
-        if (kind == 1 && lane == 0) MHC_TRACE_AT(t, 2);
-        if (kind == 1 &&
-            !waitw(bar(B_QREADY + (t & 1)), (uint32_t)(t >> 1) & 1, true, ab, 12, t)) {
-          ok = false;
-          break;
+    for (int it = 0; it < T && ok; ++it) {
+      const int y = (cid + it * ncl) * kTile;
+      if (lane == 0) MHC_TRACE_AT(it, 0);
+      for (int j = 0; j < kKb; ++j) {
+        if (!waitw(bar(B_EMPTY + stage), phase ^ 1, false, ab, 1, it)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_expect_tx(bar(B_FULL + stage), kStageBytes);
+          const int x = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk;
+          tma_load_2d(sb + kOffStage + stage * kStageBytes, &tmap, x, y, bar(B_FULL + stage));
         }
-        const int y = (cid + t * ncl) * kTile;
-        if (lane == 0) MHC_TRACE_AT(t, kind == 0 ? 0 : 3);
-        for (int j = 0; j < kKb; ++j) {
-          if (!waitw(bar(B_EMPTY + stage), phase ^ 1, false, ab, 1, t)) { ok = false; break; }
-          if (lane == 0) {
-            mbar_expect_tx(bar(B_FULL + stage), kStageBytes);
-            const int x = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk;
-            tma_load_2d(sb + kOffStage + stage * kStageBytes, &tmap, x, y, bar(B_FULL + stage));
-          }
-          __syncwarp();
-          last[stage] = (int)phase;
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
-        if (lane == 0) MHC_TRACE_AT(t, kind == 0 ? 1 : 4);
+        __syncwarp();
+        last[stage] = (int)phase;
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
+      if (lane == 0) MHC_TRACE_AT(it, 1);
     }
     // every copy issued must have landed before the CTA may exit
     for (int s = 0; s < kStages; ++s)
@@ -442,227 +450,128 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
   } else if (warp == kMmaWarp) {
     int stage = 0;
     uint32_t phase = 0;
-    bool ok = true;
-    for (int it = 0; it <= T && ok; ++it) {
-      if (it < T) {                                   // stats(it): 20 k-blocks into TMEM
-        const int buf = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
-        if (!waitw(bar(B_TEMPTY + buf), (use & 1) ^ 1, false, ab, 2, it)) break;
+    bool ok = waitw(bar(B_FNREADY), 0, false, ab, 0, 0);
+    for (int it = 0; it < T && ok; ++it) {
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!waitw(bar(B_TEMPTY + buf), (use & 1) ^ 1, false, ab, 2, it)) break;
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(buf * 64);
+      for (int j = 0; j < kKb; ++j) {
+        if (!waitw(bar(B_FULL + stage), phase, false, ab, 3, it)) { ok = false; break; }
         tc_fence_after();
-        if (lane == 0) MHC_TRACE_AT(it, 5);
-        const uint32_t d = tmem + (uint32_t)(buf * 64);
-        for (int j = 0; j < kKb; ++j) {
-          if (!waitw(bar(B_FULL + stage), phase, false, ab, 3, it)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint64_t ad = sw128_desc(sb + kOffStage + stage * kStageBytes);
-            const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes);
+        if (lane == 0) {
+          const uint64_t ad = sw128_desc(sb + kOffStage + stage * kStageBytes);
+          const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBk / 16; ++kk)
-              tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (j | kk) != 0);
-            tc_commit(bar(B_EMPTY + stage));
-          }
-          __syncwarp();
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          for (int kk = 0; kk < kBk / 16; ++kk)
+            tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (j | kk) != 0);
+          tc_commit(bar(B_EMPTY + stage));
         }
-        if (!ok) break;
-        if (lane == 0) tc_commit(bar(B_TFULL + buf));
-        if (lane == 0) MHC_TRACE_AT(it, 6);
         __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
-      if (it >= 1) {                                  // combine(it-1): not ours, release
-        for (int j = 0; j < kKb; ++j) {
-          if (!waitw(bar(B_FULL + stage), phase, false, ab, 3, it - 1)) { ok = false; break; }
-          if (lane == 0) mbar_arrive(bar(B_EMPTY + stage));
-          __syncwarp();
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
-      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(bar(B_TFULL + buf));
+      __syncwarp();
     }
     // all issued MMAs complete before TMEM is freed
     if (lane == 0) tc_commit(bar(B_DRAIN));
     __syncwarp();
     drain1(bar(B_DRAIN), 0);
     __syncwarp();
-  } else if (warp < kOwner0) {
-    // ---- row warps: Gram + accumulator readout (stats), x_norm (combine) -----
-    const int rw = warp - kRow0;
-    const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-    const int part = rw >> 2;                   // 0..3
-    const int grow = 32 * quarter + 8 * part + (lane >> 2);   // row of the stage work
-    const int hq = lane & 3;                    // 16 columns of a 64-column block
-    const int trow = 32 * quarter + lane;       // row of this lane in TMEM
-    const int sw = grow & 7;
-    const float *tabs = reinterpret_cast<const float *>(sm + kOffTab);
-    const uint4 *wsm = reinterpret_cast<const uint4 *>(sm + kOffW);
+  } else if (warp >= kRow0 && warp < kRow0 + kRowN) {
+    // ---- row warps: one thread per tile row; sum x^2 from every stage -------
+    const int row = 32 * (warp & 3) + lane;     // tile row
+    const int sw = row & 7;
+    float *ssbuf = reinterpret_cast<float *>(sm + kOffSs);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    // 16 bf16 of this lane's row in the current stage -> fp32
-    auto load16 = [&](float (&x)[16]) {
-      const uint8_t *st = sm + kOffStage + stage * kStageBytes + grow * 128;
-      const uint4 c0 = *reinterpret_cast<const uint4 *>(st + (((2 * hq) ^ sw) << 4));
-      const uint4 c1 = *reinterpret_cast<const uint4 *>(st + (((2 * hq + 1) ^ sw) << 4));
-      const uint32_t w8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    for (int it = 0; it < T && ok; ++it) {
+      float ss = 0.f;
+      for (int j = 0; j < kKb; ++j) {
+        if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, it)) { ok = false; break; }
+        if (j == 0 && warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 2);
+        const uint8_t *st = sm + kOffStage + stage * kStageBytes + row * 128;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        x[2 * e] = lo_bf(w8[e]);
-        x[2 * e + 1] = hi_bf(w8[e]);
+        for (int q = 0; q < 8; ++q) {
+          const uint4 c = *reinterpret_cast<const uint4 *>(st + ((q ^ sw) << 4));
+          const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = lo_bf(w4[e]), x1 = hi_bf(w4[e]);
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
+          }
+        }
+        // the stage is released only after every lane has used its data
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_EMPTY + stage));
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
-    };
-    // every lane's reads of the stage are complete (their values were used)
-    // before the warp's arrival lets the producer refill it
-    auto release = [&]() {
+      if (!ok) break;
+      if (warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 3);
+      // hand the row's sum x^2 to the readout warps (slot free once tile it-2
+      // was read out)
+      const int buf = it & 1;
+      if (!waitw(bar(B_TEMPTY + buf), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 10, it)) break;
+      ssbuf[buf * kTile + row] = ss;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_EMPTY + stage));
-      if (++stage == kStages) { stage = 0; phase ^= 1; }
-    };
-    for (int it = 0; it <= T && ok; ++it) {
-      if (it < T) {
-        // ---- stats(it)
-        const int buf = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
-        float g00 = 0.f, g01 = 0.f, g02 = 0.f, g03 = 0.f, g11 = 0.f, g12 = 0.f, g13 = 0.f,
-              g22 = 0.f, g23 = 0.f, g33 = 0.f;
-        float s0[16], s1[16], s2[16];
-        for (int hb = 0; hb < kHb && ok; ++hb) {
+      if (lane == 0) mbar_arrive(bar(B_SSREADY + buf));
+    }
+  } else if (warp >= kRead0 && warp < kRead0 + kReadN) {
+    // ---- readout warps: one thread per tile row (= TMEM lane) ---------------
+    // accumulator + sum x^2 of tile t -> the owner CTA's receive buffer
+    const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+    const int row = 32 * quarter + lane;
+    const float *ssbuf = reinterpret_cast<const float *>(sm + kOffSs);
+    for (int t = 0; t < T; ++t) {
+      const int buf = t & 1;
+      const uint32_t use = (uint32_t)(t >> 1);
+      if (!waitw(bar(B_TFULL + buf), use & 1, false, ab, 5, t)) break;
+      if (!waitw(bar(B_SSREADY + buf), use & 1, false, ab, 11, t)) break;
+      tc_fence_after();
+      const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * 64);
+      float a0[16], a1[16], a2[16];             // columns 0..47: hi 0..23, lo 24..47
+      tc_ld16(ta + 0, a0);
+      tc_ld16(ta + 16, a1);
+      tc_ld16(ta + 32, a2);
+      tc_wait_ld();
+      const float ss = ssbuf[buf * kTile + row];
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
+      float mix[kMix];                          // hi + lo of the 24 dots
 #pragma unroll
-          for (int i = 0; i < kHC; ++i) {
-            if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, it)) { ok = false; break; }
-            if (hb == 0 && i == 0 && warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 7);
-            float x[16];
-            load16(x);
-            if (i == 0) {
+      for (int c = 0; c < 8; ++c) mix[c] = a0[c] + a1[c + 8];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) { g00 = fmaf(x[e], x[e], g00); s0[e] = x[e]; }
-            } else if (i == 1) {
+      for (int c = 8; c < 16; ++c) mix[c] = a0[c] + a2[c - 8];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                g11 = fmaf(x[e], x[e], g11); g01 = fmaf(s0[e], x[e], g01); s1[e] = x[e];
-              }
-            } else if (i == 2) {
+      for (int c = 16; c < 24; ++c) mix[c] = a1[c - 16] + a2[c - 8];
+      // slot [our rank][row % 8] of the owner CTA (row / 8)
+      if (!waitw(bar(B_PFREE), (uint32_t)(t & 1) ^ 1, true, ab, 6, t)) break;
+      const uint32_t dm = mapa(sb + kOffRecv + (uint32_t)(((crank * kOwn + (row & 7)) * kRw) * 4),
+                               (uint32_t)(row >> 3));
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                g22 = fmaf(x[e], x[e], g22); g02 = fmaf(s0[e], x[e], g02);
-                g12 = fmaf(s1[e], x[e], g12); s2[e] = x[e];
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                g33 = fmaf(x[e], x[e], g33); g03 = fmaf(s0[e], x[e], g03);
-                g13 = fmaf(s1[e], x[e], g13); g23 = fmaf(s2[e], x[e], g23);
-              }
-            }
-            // the stage is released only after every lane has used its data
-            release();
-          }
-        }
-        if (!ok) break;
-        if (warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 8);
-        // accumulator: hi and lo halves of mixes 6*part .. 6*part+5 of row trow
-        if (!waitw(bar(B_TFULL + buf), use & 1, false, ab, 5, it)) break;
-        if (warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 9);
-        tc_fence_after();
-        const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * 64 + 6 * part);
-        float hv[6], lv[6];
-        tc_ld2(ta + 0, hv[0], hv[1]);
-        tc_ld2(ta + 2, hv[2], hv[3]);
-        tc_ld2(ta + 4, hv[4], hv[5]);
-        tc_ld2(ta + kMix + 0, lv[0], lv[1]);
-        tc_ld2(ta + kMix + 2, lv[2], lv[3]);
-        tc_ld2(ta + kMix + 4, lv[4], lv[5]);
-        tc_wait_ld();
-        tc_fence_before();
+      for (int v = 0; v < 6; ++v)
+        st_cluster_v4(dm + 16 * v, mix[4 * v], mix[4 * v + 1], mix[4 * v + 2], mix[4 * v + 3]);
+      st_cluster_f32(dm + 4 * kMix, ss);
+      // make the stores visible cluster-wide, then count this warp in
+      fence_cluster();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_GALL));
+      if (warp == kRead0) {
+        // all readout warps pushed tile t: tell all 16 owners
+        if (!waitw(bar(B_GALL), (uint32_t)(t & 1), false, ab, 7, t)) break;
+        if (lane == 0) arrive_all_ctas(bar(B_PREADY), kCl);
+        if (lane == 0) MHC_TRACE_AT(t, 4);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
-        // Gram of the row: lanes 4r'..4r'+3 hold its four column quarters
-        float gg[10] = {g00, g01, g02, g03, g11, g12, g13, g22, g23, g33};
-#pragma unroll
-        for (int q = 0; q < 10; ++q) {
-          gg[q] += __shfl_xor_sync(0xffffffffu, gg[q], 1);
-          gg[q] += __shfl_xor_sync(0xffffffffu, gg[q], 2);
-        }
-        // push the partials into the owners' receive buffers
-        if (!waitw(bar(B_PFREE), (uint32_t)(it & 1) ^ 1, true, ab, 6, it)) break;
-        {
-          const uint32_t dst = mapa(sb + kOffRecv +
-                                        (uint32_t)(((crank * kOwn + (trow & 7)) * kPw + 6 * part) * 4),
-                                    (uint32_t)(trow >> 3));
-#pragma unroll
-          for (int q = 0; q < 6; ++q)
-            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4 * q), "f"(hv[q] + lv[q])
-                         : "memory");
-          if (hq == 0) {
-            const uint32_t dg = mapa(sb + kOffRecv +
-                                         (uint32_t)(((crank * kOwn + (grow & 7)) * kPw + kMix) * 4),
-                                     (uint32_t)(grow >> 3));
-#pragma unroll
-            for (int q = 0; q < 10; ++q)
-              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dg + 4 * q), "f"(gg[q])
-                           : "memory");
-          }
-        }
-        fence_cluster();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_GALL));
-        if (warp == kRow0) {
-          if (!waitw(bar(B_GALL), (uint32_t)(it & 1), false, ab, 7, it)) break;
-          if (lane == 0)
-            arrive_all_ctas(bar(B_PREADY), kCl);
-          if (lane == 0) MHC_TRACE_AT(it, 10);
-          __syncwarp();
-        }
-      }
-      if (it >= 1) {
-        // ---- combine(t): y = sum_i pre_i R_i, x_norm = bf16(y * rnorm * w)
-        const int t = it - 1;
-        if (!waitw(bar(B_QREADY + (t & 1)), (uint32_t)(t >> 1) & 1, true, ab, 12, t)) break;
-        if (warp == kRow0 && lane == 0) MHC_TRACE_AT(t, 11);
-        const float *tr = tabs + ((t & 1) * kTile + grow) * kPreW;
-        const float p0 = tr[0], p1 = tr[1], p2 = tr[2], p3 = tr[3], rn = tr[4];
-        const int64_t grow_g = (int64_t)(cid + t * ncl) * kTile + grow;
-        const bool live = grow_g < a.rows;
-        for (int hb = 0; hb < kHb && ok; ++hb) {
-          float yv[16];
-#pragma unroll
-          for (int i = 0; i < kHC; ++i) {
-            if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, t)) { ok = false; break; }
-            float x[16];
-            load16(x);
-            const float pi = i == 0 ? p0 : (i == 1 ? p1 : (i == 2 ? p2 : p3));
-#pragma unroll
-            for (int e = 0; e < 16; ++e) yv[e] = i == 0 ? pi * x[e] : fmaf(pi, x[e], yv[e]);
-            release();
-          }
-          if (!ok) break;
-          if (live) {
-            const uint4 wa = wsm[(kBk * hb + 16 * hq) / 8], wb = wsm[(kBk * hb + 16 * hq) / 8 + 1];
-            const uint32_t ww[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-            uint32_t ow[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              ow[e] = pack2_rn((yv[2 * e] * rn) * lo_bf(ww[e]), (yv[2 * e + 1] * rn) * hi_bf(ww[e]));
-            uint4 *dst = reinterpret_cast<uint4 *>(a.x_norm + grow_g * kH + (int64_t)crank * kHs +
-                                                   kBk * hb + 16 * hq);
-            st_stream(dst, make_uint4(ow[0], ow[1], ow[2], ow[3]));
-            st_stream(dst + 1, make_uint4(ow[4], ow[5], ow[6], ow[7]));
-          }
-        }
-        if (!ok) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_CDONE));
-        if (warp == kRow0) {
-          if (!waitw(bar(B_CDONE), (uint32_t)(t & 1), false, ab, 13, t)) break;
-          if (lane == 0)
-            arrive_all_ctas(bar(B_QFREE + (t & 1)), kCl);
-          if (lane == 0) MHC_TRACE_AT(t, 12);
-          __syncwarp();
-        }
       }
     }
   } else {
     // ---- owner warps: finalise 8 rows of each tile --------------------------
-    const int o = threadIdx.x - kOwner0 * 32;   // 0..127
+    const int o = owner_index(warp) * 32 + lane;   // 0..127
     const int q = o >> 4, e = o & 15;           // row of 8, lane of 16
     const int row_t = (int)crank * kOwn + q;
     const float *recv = reinterpret_cast<const float *>(sm + kOffRecv);
@@ -673,40 +582,29 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
     const unsigned full = 0xffffffffu;          // a row's 16 lanes are half the warp
     const int gb = lane & 16;
     for (int it = 0; it < T; ++it) {
-      const int buf = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
       const int64_t grow = (int64_t)(cid + it * ncl) * kTile + row_t;
       if (!waitw(bar(B_PREADY), (uint32_t)(it & 1), true, ab, 8, it)) break;
-      if (warp == kOwner0 && lane == 0) MHC_TRACE_AT(it, 13);
-      // this row's 34 partials from the 16 CTAs, summed in CTA order
-      float acc[3] = {0.f, 0.f, 0.f};
+      if (warp == kOwnerLead && lane == 0) MHC_TRACE_AT(it, 5);
+      // this row's 25 partials from the 16 CTAs, summed in CTA order
+      float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int w3 = 0; w3 < 3; ++w3) {
-        const int v = e + 16 * w3;
-        if (v < kPw) {
-          float sacc = 0.f;
+      for (int src = 0; src < kCl; ++src) acc0 += recv[(src * kOwn + q) * kRw + e];
+      if (e + 16 <= kMix) {
 #pragma unroll
-          for (int src = 0; src < kCl; ++src) sacc += recv[(src * kOwn + q) * kPw + v];
-          acc[w3] = sacc;
-        }
+        for (int src = 0; src < kCl; ++src) acc1 += recv[(src * kOwn + q) * kRw + e + 16];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_OPULL));
-      if (warp == kOwner0) {
+      if (warp == kOwnerLead) {
         if (!waitw(bar(B_OPULL), (uint32_t)(it & 1), false, ab, 9, it)) break;
-        if (lane == 0)
-          arrive_all_ctas(bar(B_PFREE), kCl);
+        if (lane == 0) arrive_all_ctas(bar(B_PFREE), kCl);
         __syncwarp();
       }
-      float *rq = red + q * kPw;
-      rq[e] = acc[0];
-      rq[e + 16] = acc[1];
-      if (e < 2) rq[e + 32] = acc[2];
+      float *rq = red + q * kRw;
+      rq[e] = acc0;
+      if (e + 16 <= kMix) rq[e + 16] = acc1;
       __syncwarp();
-      const float G00 = rq[24], G01 = rq[25], G02 = rq[26], G03 = rq[27], G11 = rq[28];
-      const float G12 = rq[29], G13 = rq[30], G22 = rq[31], G23 = rq[32], G33 = rq[33];
-      const float ss = ((G00 + G11) + G22) + G33;
-      const float rsq = 1.0f / sqrtf(ss / (float)kK + a.rms_eps);
+      const float rsq = 1.0f / sqrtf(rq[kMix] / (float)kK + a.rms_eps);
       // gates: lanes 0..3 pre, 4..7 post
       float gate = 0.f;
       if (e < 8) {
@@ -714,33 +612,7 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
         const float sg = 1.0f / (1.0f + expf(-l));
         gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
       }
-      const float p0 = __shfl_sync(full, gate, gb + 0), p1 = __shfl_sync(full, gate, gb + 1);
-      const float p2 = __shfl_sync(full, gate, gb + 2), p3 = __shfl_sync(full, gate, gb + 3);
-      // sum_h y_h^2 = pre^T G pre
-      float yy = p0 * p0 * G00 + p1 * p1 * G11 + p2 * p2 * G22 + p3 * p3 * G33;
-      yy += 2.0f * (p0 * p1 * G01 + p0 * p2 * G02 + p0 * p3 * G03 + p1 * p2 * G12 +
-                    p1 * p3 * G13 + p2 * p3 * G23);
-      yy = fmaxf(yy, 0.f);
-      const float rn = 1.0f / sqrtf(yy / (float)kH + a.norm_eps);
-      // (pre, rnorm) of this row into table `buf` of CTA e: the combines wait on it
-      if (!waitw(bar(B_QFREE + buf), (use & 1) ^ 1, true, ab, 10, it)) break;
-      const uint32_t ta = mapa(sb + kOffTab + (uint32_t)((buf * kTile + row_t) * kPreW) * 4u, (uint32_t)e);
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ta), "f"(p0) : "memory");
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ta + 4), "f"(p1) : "memory");
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ta + 8), "f"(p2) : "memory");
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ta + 12), "f"(p3) : "memory");
-      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ta + 16), "f"(rn) : "memory");
-      fence_cluster();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_OTAB));
-      if (warp == kOwner0) {
-        if (!waitw(bar(B_OTAB), (uint32_t)(it & 1), false, ab, 11, it)) break;
-        if (lane == 0)
-          arrive_all_ctas(bar(B_QREADY + buf), kCl);
-        if (lane == 0) MHC_TRACE_AT(it, 14);
-        __syncwarp();
-      }
-      // Sinkhorn on exp(logits), off the combine's critical path: lane e holds comb[e/4][e%4]
+      // Sinkhorn on exp(logits): lane e holds comb[e/4][e%4]
       float C = expf(fmaf(rq[8 + e] * rsq, sc2, bcomb));
       for (int k = 0; k < a.iters; ++k) {
         float rs = C + __shfl_xor_sync(full, C, 1);
@@ -750,9 +622,9 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
         cs = cs + __shfl_xor_sync(full, cs, 8);
         C = C / (cs + a.sink_eps);
       }
-      if (warp == kOwner0 && lane == 0) MHC_TRACE_AT(it, 15);
       if (grow < a.rows) {
         a.comb[grow * 16 + e] = C;
+        if (e < 4) a.pre_ws[grow * kHC + e] = gate;
         if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
         if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
         if (a.mix_out) {
@@ -760,6 +632,8 @@ pre_fused_kernel(const __grid_constant__ CUtensorMap tmap, const FusedArgs a) {
           if (e < 8) a.mix_out[grow * kMix + 16 + e] = rq[16 + e] * rsq;
         }
       }
+      if (warp == kOwnerLead && lane == 0) MHC_TRACE_AT(it, 6);
+      (void)gb;
       __syncwarp();
     }
   }
@@ -806,10 +680,10 @@ cudaError_t configure(int dev, int *max_clusters) {
     *max_clusters = g_max_clusters[dev];
     return cudaSuccess;
   }
-  cudaError_t e = cudaFuncSetAttribute(pre_fused_kernel,
+  cudaError_t e = cudaFuncSetAttribute(pre_stats_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pre_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(pre_stats_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
@@ -823,7 +697,7 @@ cudaError_t configure(int dev, int *max_clusters) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, pre_fused_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, pre_stats_kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
   g_max_clusters[dev] = n;
@@ -833,11 +707,10 @@ cudaError_t configure(int dev, int *max_clusters) {
 
 }  // namespace
 
-cudaError_t launch_pre_fused(const uint16_t *R, const float *fn, const float *scale,
-                             const float *base, const uint16_t *norm_w, int64_t rows,
-                             int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
-                             float *post, float *comb, float *pre_out, float *mix_out,
-                             cudaStream_t s) {
+cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
+                             const float *base, int64_t rows, int64_t logical_rows,
+                             const mhc_params &p, float *pre_ws, float *post, float *comb,
+                             float *pre_out, float *mix_out, cudaStream_t s) {
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   int dev = 0;
@@ -858,13 +731,13 @@ cudaError_t launch_pre_fused(const uint16_t *R, const float *fn, const float *sc
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  FusedArgs a;
-  a.fn = fn; a.scale = scale; a.base = base; a.norm_w = norm_w; a.R = R;
-  a.x_norm = x_norm; a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out;
+  StatsArgs a;
+  a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
+  a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out;
   a.rows = rows;
   a.num_tiles = (int)((rows + kTile - 1) / kTile);
   a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.sink_eps = p.hc_sinkhorn_eps;
-  a.norm_eps = p.norm_eps; a.post_mult = p.post_mult; a.iters = p.sinkhorn_iters;
+  a.post_mult = p.post_mult; a.iters = p.sinkhorn_iters;
 
   // grid: as many clusters as fit at once, never more than the whole chunk's
   // tiles (the count depends on logical_rows only; per-row arithmetic does not
@@ -884,7 +757,7 @@ cudaError_t launch_pre_fused(const uint16_t *R, const float *fn, const float *sc
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pre_fused_kernel, map, a);
+  return cudaLaunchKernelEx(&cfg, pre_stats_kernel, map, a);
 }
 
 #ifdef MHC_TRACE

@@ -85,13 +85,14 @@ const char *mhc_strerror(int code);
 /* Text of the last CUDA error seen by this thread inside libmhc ("" if none). */
 const char *mhc_last_cuda_error(void);
 
-/* Bytes of device scratch mhc_pre needs for a call on `rows` rows (0: the
- * fused kernel keeps its intermediates on chip; a NULL workspace is fine). */
+/* Bytes of device scratch mhc_pre needs for a call on `rows` rows: the pre
+ * gates [rows, 4] fp32 handed from its stats launch to its combine launch,
+ * rounded up to 256 bytes (0 for rows <= 0). */
 size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
- * or nonzero once a kernel gave up a bounded wait (it then returned early and
- * its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
+ * or nonzero once the stats kernel of mhc_pre gave up a bounded wait (it then
+ * returned early and its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
  * the device's pending work.  Returns MHC_OK or MHC_ERR_NULL/MHC_ERR_CUDA. */
 int mhc_kernel_status(uint32_t *status, int reset);
 
@@ -122,10 +123,11 @@ int mhc_kernel_status_detail(uint32_t *where64);
  * (RMSNorm fused without rounding y first, as the fused combine+norm gate of
  * prefill_sp.py, _combine_norm_fused, requires.)
  *
- * One launch (pre_fused.cu): a cluster of 16 CTAs splits each 128-row tile
- * by hidden columns; R is read from HBM once, the 24 projections run on the
- * tensor cores against fn split into bf16 hi + lo, and sum_h y_h^2 comes from
- * the per-row stream Gram matrix (pre^T G pre).
+ * Two launches: (1) stats (pre_stats.cu): a cluster of 16 CTAs splits each
+ * 128-row tile by hidden columns, streams R once with TMA, runs the 24
+ * projections on the tensor cores against fn split into bf16 hi + lo, and
+ * finalises the gates and the Sinkhorn per row; (2) combine + RMSNorm
+ * (pre_simt.cu, combine_norm_kernel), streaming R again with the gates.
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual rows

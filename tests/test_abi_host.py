@@ -62,7 +62,8 @@ def test_strerror_and_defaults(lib):
     assert p.sinkhorn_iters == 20 and p.post_mult == 2.0
     assert abs(p.rms_eps - 1e-6) < 1e-12 and abs(p.norm_eps - 1e-6) < 1e-12
     assert lib.mhc_pre_workspace_bytes(0) == 0
-    assert lib.mhc_pre_workspace_bytes(1000) == 0      # the fused kernel needs no scratch
+    assert lib.mhc_pre_workspace_bytes(1000) == 16128   # the pre gates, 256-byte rounded
+    assert lib.mhc_pre_workspace_bytes(1) == 256
 
 
 A = 1 << 32          # fake, 256-byte aligned device addresses, far apart
@@ -114,6 +115,10 @@ def test_pre_validation(lib):
     assert call_pre(lib, fn=None) == ERR_NULL
     assert call_pre(lib, comb=fake(7) + 4) == ERR_ALIGN
     assert call_pre(lib, mix=fake(8) + 4) == ERR_ALIGN
+    assert call_pre(lib, ws=None) == ERR_WORKSPACE
+    assert call_pre(lib, ws_bytes=16) == ERR_WORKSPACE
+    assert call_pre(lib, ws=fake(9) + 16) == ERR_WORKSPACE                # not 256-byte aligned
+    assert call_pre(lib, ws=fake(5)) == ERR_OVERLAP                         # workspace on x_norm
     assert call_pre(lib, xn=fake(0)) == ERR_OVERLAP                         # x_norm on R
     assert call_pre(lib, post=fake(7)) == ERR_OVERLAP                       # post on comb
 
