@@ -377,7 +377,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     mbar_init(bar(B_GALL), kReadN);
     mbar_init(bar(B_OPULL), kOwnerN);
     mbar_init(bar(B_DRAIN), 1);
-    mbar_init(bar(B_FNREADY), kWarps - 1);
+    mbar_init(bar(B_FNREADY), kWarps - 1 - kRowN);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -388,34 +388,52 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
   const uint32_t tmem = *tmem_slot;
 
   // fn columns of this CTA -> bf16 hi/lo B tiles (K-major, 128-byte swizzle),
-  // written by every warp but the producer, which meanwhile starts streaming R:
+  // written by the MMA, readout and owner warps while the producer starts
+  // streaming R and the row warps wait for it:
   // k-block j covers k = (j%4)*5120 + 320*crank + 64*(j/4) + [0, 64)
-  if (warp != kProducerWarp) {
-  for (int item = threadIdx.x - 32; item < kMix * kKb * 8; item += kThreads - 32) {
-    const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
-    const int k0 = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk + 8 * q;
-    const float4 f0 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0));
-    const float4 f1 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0 + 4));
-    const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-    uint32_t hw[4], lw[4];
+  if (warp != kProducerWarp && !(warp >= kRow0 && warp < kRow0 + kRowN)) {
+    // 10 loader warps; loads of 8 items are issued before any is converted
+    const int loader = warp == kMmaWarp ? 0 : (warp < kRow0 ? warp - 1 : warp - kRowN - 1);
+    const int lt = loader * 32 + lane, nl = (kWarps - 1 - kRowN) * 32;
+    constexpr int kItems = kMix * kKb * 8;     // 3840 items of 8 consecutive k
+    for (int base = lt; base < kItems; base += 8 * nl) {
+      float4 f0[8], f1[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * e]);
-      const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * e + 1]);
-      hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
-      lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
+      for (int u = 0; u < 8; ++u) {
+        const int item = base + u * nl;
+        if (item < kItems) {
+          const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
+          const int k0 = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk + 8 * q;
+          f0[u] = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0));
+          f1[u] = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0 + 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int item = base + u * nl;
+        if (item >= kItems) continue;
+        const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
+        const float f[8] = {f0[u].x, f0[u].y, f0[u].z, f0[u].w, f1[u].x, f1[u].y, f1[u].z, f1[u].w};
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * e]);
+          const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * e + 1]);
+          hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
+          lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
+        }
+        uint8_t *tile = sm + kOffFn + j * kFnBlkBytes;
+        const int nh = c, nlo = c + kMix;
+        *reinterpret_cast<uint4 *>(tile + (nh >> 3) * 1024 + (nh & 7) * 128 + ((q ^ (nh & 7)) << 4)) =
+            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(tile + (nlo >> 3) * 1024 + (nlo & 7) * 128 +
+                                   ((q ^ (nlo & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
     }
-    uint8_t *tile = sm + kOffFn + j * kFnBlkBytes;
-    const int nh = c, nl = c + kMix;
-    *reinterpret_cast<uint4 *>(tile + (nh >> 3) * 1024 + (nh & 7) * 128 + ((q ^ (nh & 7)) << 4)) =
-        make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4 *>(tile + (nl >> 3) * 1024 + (nl & 7) * 128 + ((q ^ (nl & 7)) << 4)) =
-        make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  }
-  // generic-proxy writes -> visible to the tensor core (async proxy)
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar(B_FNREADY));
+    // generic-proxy writes -> visible to the tensor core (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(B_FNREADY));
   }
 
   // ---- roles -------------------------------------------------------------------
