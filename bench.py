@@ -42,7 +42,8 @@ PRE_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4          # 51,280
 POST_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4 + K * 2  # 92,240
 PRE_BYTES_CALL = MIX * K * 4 + H * 2 + 3 * 4 + MIX * 4         # fn, norm_w, scale, base
 PRE_LAUNCHES, POST_LAUNCHES = 2, 1                             # kernels per call
-DOMINANT_SRC = {"mhc_pre": ["pre_stats.cu", "pre_simt.cu"], "mhc_post": ["post.cu"]}
+KERNEL_SRC = {"mhc_post": ["post.cu"], "mhc_pre_stats": ["pre_stats.cu"],
+              "mhc_pre_combine": ["pre_simt.cu"]}
 
 
 def peaks():
@@ -70,9 +71,13 @@ def traffic_for(kernel):
             t = json.load(f)[kernel]
     except Exception:
         return None
-    if t.get("src_sha256_16") != src_hash(DOMINANT_SRC[kernel]):
+    if t.get("src_sha256_16") != src_hash(KERNEL_SRC[kernel]):
         return None
     return t.get("dram_bytes_per_launch_full_size")
+
+
+def _sum_or_none(*xs):
+    return None if any(x is None for x in xs) else sum(xs)
 
 
 class ClockSampler:
@@ -329,10 +334,9 @@ def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, d
     gbs = step_bytes * K_ / (ms / 1e3) / 1e9
     pre_gbs = (M * PRE_BYTES_ROW + PRE_BYTES_CALL) / (pre_ms / 1e3) / 1e9
     post_gbs = M * POST_BYTES_ROW / (post_ms / 1e3) / 1e9
-    if post_ms >= pre_ms:
-        dom, dgbs, dbytes = "mhc_post", post_gbs, M * POST_BYTES_ROW
-    else:
-        dom, dgbs, dbytes = "mhc_pre", pre_gbs, M * PRE_BYTES_ROW + PRE_BYTES_CALL
+    # dominant single kernel: post_kernel (the largest share of the launch
+    # list); mhc_pre is two launches and is reported beside it as a call
+    dom, dgbs, dbytes = "mhc_post", post_gbs, M * POST_BYTES_ROW
     line = {
         "metric": METRIC,
         "value": rows_per_s,
@@ -369,6 +373,12 @@ def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, d
             "frac": dgbs / hbm_peak,
             "traffic": traffic_for(dom),
             "algorithmic_bytes_per_launch": dbytes,
+            "kernel_name": "post_kernel",
+            "pre_call": {"launches": PRE_LAUNCHES, "ms": pre_ms, "achieved": pre_gbs,
+                         "frac": pre_gbs / hbm_peak,
+                         "algorithmic_bytes": M * PRE_BYTES_ROW + PRE_BYTES_CALL,
+                         "traffic": _sum_or_none(traffic_for("mhc_pre_stats"),
+                                                 traffic_for("mhc_pre_combine"))},
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
