@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
+from hyper_connection_residual_mhc_gb300.shard import max_over_ranks  # noqa: E402
 
 METRIC = "mHC pre+post rows/s and achieved HBM GB/s (% of GB300 peak) at M=16384"
 HC, H, K, MIX = 4, 5120, 20480, 24
@@ -260,10 +261,7 @@ def run_mhc(args):
     ms = start.elapsed_time(end)
     pre_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     post_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist if world > 1 else None, dev)
 
     # ---- end to end: host buffers, copies inside the timed region ----------
     e2e = None
@@ -312,10 +310,7 @@ def run_e2e(m, torch, dist, world, dev, stream, step, Rh, yh, R, y, xn, R2, post
     e2.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = s2.elapsed_time(e2)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist if world > 1 else None, dev)
     h2d = (Rp.numel() + yp.numel()) * 2
     d2h = (xn_h.numel() + R2_h.numel()) * 2 + (post_h.numel() + comb_h.numel()) * 4
     return {"value": world * M * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
