@@ -66,8 +66,9 @@ def _load():
             lib.oracle_post.argtypes = [_U16, _U16, _F, _F, i64, _U16]
             lib.oracle_pre.argtypes = [_U16, i64, _F, _F, _F, _U16, dbl, dbl, dbl, dbl, dbl,
                                        c_int, _D, _D, _D, _D, _D, _U16]
+            lib.oracle_hc_head.argtypes = [_U16, i64, _F, _F, _F, dbl, dbl, _D, _D, _U16]
             for f in ("oracle_stats", "oracle_split_sinkhorn", "oracle_combine_norm",
-                      "oracle_post", "oracle_pre"):
+                      "oracle_post", "oracle_pre", "oracle_hc_head"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -176,3 +177,26 @@ def pre(R, fn, scale, base, w, *, rms_eps=1e-6, hc_pre_eps=1e-6, hc_sinkhorn_eps
         int(iters), _p(out["mix"], _D), _p(out["logits"], _D), _p(out["pre"], _D),
         _p(out["post"], _D), _p(out["comb"], _D), _p(out["x_norm"], _U16))
     return out
+
+
+def hc_head(R, fn, scale, base, *, norm_eps=1e-6, hc_eps=1e-6):
+    """The final stream collapse (deepseek_v4.py, hc_head_torch): dict of mix
+    [rows,4], pre [rows,4] (float64) and y [rows,5120] (bf16 bits)."""
+    R = _u16(R, (HC, H))
+    rows = R.shape[0]
+    out = {"mix": np.zeros((rows, HC), np.float64), "pre": np.zeros((rows, HC), np.float64),
+           "y": np.zeros((rows, H), np.uint16)}
+    _load().oracle_hc_head(
+        _p(R, _U16), rows, _p(_f32(fn).reshape(HC, K), _F), _p(_f32(scale).reshape(1), _F),
+        _p(_f32(base).reshape(HC), _F), float(norm_eps), float(hc_eps), _p(out["mix"], _D),
+        _p(out["pre"], _D), _p(out["y"], _U16))
+    return out
+
+
+def fused_post_pre(R, y, post_w, comb, fn, scale, base, w, **pre_kw):
+    """hc_post of one sublayer followed by hc_pre of the next on its result
+    (deepseek_v4.py, the fused post->pre path between sublayers): the
+    definition is the plain composition, R' rounded to bf16 in between.
+    Returns (R' bf16 bits, the pre dict of R')."""
+    R2 = post(R, y, post_w, comb)
+    return R2, pre(R2, fn, scale, base, w, **pre_kw)

@@ -27,6 +27,10 @@
  *     R'[:, i, :] = post_i * y + sum_j comb[:, j, i] * R[:, j, :].
  *   prefill_sp.py, _combine_norm_fused: the fused combine+RMSNorm kernel is
  *     used only when the norm does not cast x before the weight multiply.
+ *   deepseek_v4.py, make_hc_head_params and hc_head_torch: the model's final
+ *     collapse of the 4 streams, fn [4, 4H], base [4], scale [1];
+ *     rsqrt(mean(x^2) + norm_eps); pre = sigmoid(mixes*scale + base) + hc_eps;
+ *     y = sum_i pre_i * x_i, cast once to the residual's dtype.
  *
  * The body of hc_split_sinkhorn is not on the pages.  The reading used here
  * (each choice is also listed in the design notes):
@@ -241,4 +245,48 @@ void oracle_pre(const uint16_t *R, int64_t rows, const float *fn, const float *s
         oracle_combine_norm(R, rows, pre, w, norm_eps, 0, x_norm);
     if (!mix)
         free(mix_buf);
+}
+
+/* ---- hc_head: the final collapse of the streams --------------------------- */
+
+/* For each row m, with x = R[m] flattened stream-major:
+ *   rsq       = 1 / sqrt( (sum_k x_k^2) / 20480 + norm_eps )
+ *   mix[m, c] = rsq * sum_k x_k * fn[c, k]                 (c = 0..3)
+ *   pre[m, i] = sigmoid( mix[m, i] * scale[0] + base[i] ) + hc_eps
+ *   y[m, h]   = bf16( sum_i pre[m, i] * R[m, i, h] )
+ * fn is [4, 20480] fp32, base [4], scale [1].  mix and pre may be NULL. */
+void oracle_hc_head(const uint16_t *R, int64_t rows, const float *fn, const float *scale,
+                    const float *base, double norm_eps, double hc_eps, double *mix,
+                    double *pre, uint16_t *y)
+{
+    double *x = (double *)malloc(sizeof(double) * O_K);
+    for (int64_t m = 0; m < rows; ++m) {
+        const uint16_t *row = R + m * (int64_t)O_K;
+        double ss = 0.0;
+        for (int k = 0; k < O_K; ++k) {
+            x[k] = oracle_bf16_to_double(row[k]);
+            ss += x[k] * x[k];
+        }
+        double r = 1.0 / sqrt(ss / (double)O_K + norm_eps);
+        double p[O_HC];
+        for (int c = 0; c < O_HC; ++c) {
+            const float *f = fn + (int64_t)c * O_K;
+            double dot = 0.0;
+            for (int k = 0; k < O_K; ++k)
+                dot += x[k] * (double)f[k];
+            double mx = dot * r;
+            if (mix)
+                mix[m * O_HC + c] = mx;
+            p[c] = sigmoid(mx * (double)scale[0] + (double)base[c]) + hc_eps;
+            if (pre)
+                pre[m * O_HC + c] = p[c];
+        }
+        for (int h = 0; h < O_H; ++h) {
+            double acc = 0.0;
+            for (int i = 0; i < O_HC; ++i)
+                acc += p[i] * x[i * O_H + h];
+            y[m * (int64_t)O_H + h] = oracle_double_to_bf16(acc);
+        }
+    }
+    free(x);
 }
