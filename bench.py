@@ -385,6 +385,76 @@ def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, d
         dist.destroy_process_group()
 
 
+# --------------------------------------------------------------------------- other entry points
+HEAD_BYTES_ROW = K * 2 + H * 2                 # read R, write y
+HEAD_BYTES_CALL = HC * K * 4 + HC * 4 + 4      # fn, base, scale
+
+
+def run_op(args):
+    """Time one of the library's other entry points alone (1 GPU, inputs in
+    HBM): prints one JSON line in the same shape as the step's."""
+    import torch
+    import hyper_connection_residual_mhc_gb300 as m
+    from hyper_connection_residual_mhc_gb300 import build as b
+    b.build()
+    m.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M = args.rows
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    R = bf(synth.residual(SEED, M))
+    stream = torch.cuda.current_stream(dev)
+    if args.op == "hc_head":
+        hw = synth.head_weights(SEED)
+        fn = torch.from_numpy(hw.fn).to(dev)
+        scale = torch.from_numpy(hw.scale).to(dev)
+        base = torch.from_numpy(hw.base).to(dev)
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty((max(1, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+
+        def step():
+            m.mhc_hc_head(R, fn, scale, base, logical_rows=M, workspace=ws, out=y, stream=stream)
+        nbytes, launches = M * HEAD_BYTES_ROW + HEAD_BYTES_CALL, 2
+        metric = "mhc_hc_head rows/s (final stream collapse) and achieved HBM GB/s"
+        workload = f"M={M} rows: R[M,4,5120] bf16, hc_head fn[4,20480] f32 (seed {SEED})"
+    else:
+        raise SystemExit(f"unknown --op {args.op}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    clocks = clk.summary()
+    ms = start.elapsed_time(end)
+    hbm_peak, peak_src = peaks()
+    gbs = nbytes * args.steps / (ms / 1e3) / 1e9
+    line = {
+        "metric": metric, "value": M * args.steps / (ms / 1e3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload, "op": args.op, "rows": M,
+                   "l2": f"inputs larger than L2 (R is {M * K * 2 / 1e6:.0f} MB); no flush"},
+        "roofline": {"bound": "hbm", "kernel": args.op, "achieved": gbs, "peak": hbm_peak,
+                     "peak_source": f"{peak_src} (hbm_gbs)", "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,6 +463,9 @@ def main():
     ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["step", "hc_head"], default="step",
+                    help="step: mhc_pre + mhc_post (the headline); others time one entry "
+                         "point alone")
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows per GPU (default: the 16384-row chunk); other sizes are "
                          "for profiling runs")
@@ -401,6 +474,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op != "step":
+        run_op(args)
     else:
         run_mhc(args)
 

@@ -60,6 +60,8 @@ SIGNATURES = {
     "mhc_pre_noalloc_max_rows": (ctypes.c_int64, []),
     "mhc_post": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp]),
     "mhc_combine_norm": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp]),
+    "mhc_hc_head": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
+                                   ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -245,4 +247,34 @@ def mhc_combine_norm(R, pre, norm_w, norm_eps=1e-6, *, logical_rows=None, out=No
                                   rows if logical_rows is None else int(logical_rows),
                                   _ptr(out), _stream(stream))
     _check("mhc_combine_norm", code)
+    return out
+
+
+def mhc_hc_head(R, fn, scale, base, *, norm_eps=1e-6, hc_eps=1e-6, logical_rows=None,
+                workspace=None, out=None, pre_out=None, mix_out=None, stream=None):
+    """Final collapse of the 4 streams (see mhc_hc_head in include/mhc.h).
+
+    Returns ``y [rows, 5120] bf16``."""
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(fn, "fn", torch.float32, (HC, K))
+    _need(scale, "scale", torch.float32, (1,))
+    _need(base, "base", torch.float32, (HC,))
+    dev = R.device
+    out = torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if out is None else out
+    _need(out, "out", torch.bfloat16, (rows, H))
+    if pre_out is not None:
+        _need(pre_out, "pre_out", torch.float32, (rows, HC))
+    if mix_out is not None:
+        _need(mix_out, "mix_out", torch.float32, (rows, HC))
+    need = mhc_pre_workspace_bytes(rows)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().mhc_hc_head(
+        _ptr(R), _ptr(fn), _ptr(scale), _ptr(base), rows,
+        rows if logical_rows is None else int(logical_rows), float(norm_eps), float(hc_eps),
+        _ptr(workspace), ws_bytes, _ptr(out), _ptr(pre_out), _ptr(mix_out), _stream(stream))
+    _check("mhc_hc_head", code)
     return out

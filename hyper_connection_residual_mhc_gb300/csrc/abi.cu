@@ -245,4 +245,43 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 
+int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const float *base,
+                int64_t rows, int64_t logical_rows, float norm_eps, float hc_eps,
+                void *workspace, size_t workspace_bytes, uint16_t *y, float *pre_out,
+                float *mix_out, void *stream) {
+  if (int e = check_rows(rows, logical_rows)) return e;
+  if (!finite_nonneg(norm_eps) || !finite_nonneg(hc_eps)) return MHC_ERR_PARAM;
+  if (rows == 0) return MHC_OK;
+  if (!R || !fn || !scale || !base || !y) return MHC_ERR_NULL;
+  const void *al[] = {R, fn, scale, base, y};
+  for (const void *q : al)
+    if (!aligned16(q)) return MHC_ERR_ALIGN;
+  if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
+  const size_t need = mhc_pre_workspace_bytes(rows);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MHC_ERR_WORKSPACE;
+  const size_t nr = (size_t)rows;
+  const Span ins[] = {span(R, nr * MHC_K * 2), span(fn, (size_t)MHC_HC * MHC_K * 4),
+                      span(scale, 4), span(base, MHC_HC * 4)};
+  Span outs[4];
+  int n_out = 0;
+  outs[n_out++] = span(y, nr * MHC_HIDDEN * 2);
+  outs[n_out++] = span(workspace, need);
+  if (pre_out) outs[n_out++] = span(pre_out, nr * MHC_HC * 4);
+  if (mix_out) outs[n_out++] = span(mix_out, nr * MHC_HC * 4);
+  for (int a = 0; a < n_out; ++a) {
+    for (const Span &b : ins)
+      if (overlap(outs[a], b)) return MHC_ERR_OVERLAP;
+    for (int b = a + 1; b < n_out; ++b)
+      if (overlap(outs[a], outs[b])) return MHC_ERR_OVERLAP;
+  }
+  if (int e = check_device()) return e;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *pre_ws = static_cast<float *>(workspace);
+  cudaError_t ce = mhc::launch_head_stats(R, fn, scale, base, rows, logical_rows, norm_eps,
+                                          hc_eps, pre_ws, pre_out, mix_out, s);
+  if (ce == cudaSuccess) ce = mhc::launch_head_combine(R, pre_ws, rows, y, s);
+  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+
 }  // extern "C"

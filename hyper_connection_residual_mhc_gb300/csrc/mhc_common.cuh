@@ -71,6 +71,15 @@ cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *sc
                              const float *base, int64_t rows, int64_t logical_rows,
                              const mhc_params &p, float *pre_ws, float *post, float *comb,
                              float *pre_out, float *mix_out, cudaStream_t s);
+// the same stats kernel built for hc_head's 4 mixes: writes the gates to
+// pre_ws [rows, 4] (+ pre_out, mix_out [rows, 4])
+cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *scale,
+                              const float *base, int64_t rows, int64_t logical_rows,
+                              float norm_eps, float hc_eps, float *pre_ws, float *pre_out,
+                              float *mix_out, cudaStream_t s);
+// y = bf16(sum_i pre_i R_i), one block per row (hc_head's combine)
+cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows, uint16_t *y,
+                                cudaStream_t s);
 // the stats kernel's error word (nonzero once a bounded wait expired)
 cudaError_t fused_error_word(unsigned int *out, bool reset);
 cudaError_t fused_error_where(unsigned int *out32);

@@ -139,11 +139,14 @@ finalize_kernel(const float *__restrict__ partials, const float *__restrict__ sc
     *reinterpret_cast<float4 *>(comb + m * 16 + j * 4) = make_float4(C[j][0], C[j][1], C[j][2], C[j][3]);
 }
 
-// ---- combine + RMSNorm: one 128-thread block per row ------------------------
+// ---- combine (+ RMSNorm): one 128-thread block per row -----------------------
+// kNorm: x_norm = bf16(y * rsqrt(mean y^2 + eps) * w) (the pre pass);
+// otherwise y itself, cast once (hc_head: deepseek_v4.py, hc_head_torch).
 constexpr int kCnThreads = 128;
 constexpr int kCnChunks = kChunksPerStream / kCnThreads;   // 5
 static_assert(kChunksPerStream % kCnThreads == 0, "");
 
+template <bool kNorm>
 __global__ void __launch_bounds__(kCnThreads)
 combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
                     const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out) {
@@ -175,24 +178,30 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
       ss = fmaf(a, a, ss);
     }
   }
-  __shared__ float red[kCnThreads / 32];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
-  __syncthreads();
-  const float tot = ((red[0] + red[1]) + red[2]) + red[3];
-  const float rn = 1.0f / sqrtf(tot / (float)kH + norm_eps);
-
   uint4 *o = out + row * kChunksPerStream;
+  if constexpr (!kNorm) {
 #pragma unroll
-  for (int q = 0; q < kCnChunks; ++q) {
-    const int c = q * kCnThreads + tid;
-    float wf[8];
-    unpack8(__ldg(w + c), wf);
-    float v[8];
+    for (int q = 0; q < kCnChunks; ++q) st_stream(o + q * kCnThreads + tid, pack8_rn(y[q]));
+    (void)w; (void)norm_eps; (void)ss;
+  } else {
+    __shared__ float red[kCnThreads / 32];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (y[q][e] * rn) * wf[e];
-    st_stream(o + c, pack8_rn(v));
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    const float tot = ((red[0] + red[1]) + red[2]) + red[3];
+    const float rn = 1.0f / sqrtf(tot / (float)kH + norm_eps);
+
+#pragma unroll
+    for (int q = 0; q < kCnChunks; ++q) {
+      const int c = q * kCnThreads + tid;
+      float wf[8];
+      unpack8(__ldg(w + c), wf);
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = (y[q][e] * rn) * wf[e];
+      st_stream(o + c, pack8_rn(v));
+    }
   }
 }
 
@@ -208,9 +217,17 @@ size_t pre_simt_workspace_bytes(int64_t rows) {
 cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
                                 float norm_eps, int64_t rows, int64_t /*logical_rows*/,
                                 uint16_t *x_norm, cudaStream_t s) {
-  combine_norm_kernel<<<(unsigned)rows, kCnThreads, 0, s>>>(
+  combine_norm_kernel<true><<<(unsigned)rows, kCnThreads, 0, s>>>(
       reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
       reinterpret_cast<const uint4 *>(norm_w), norm_eps, reinterpret_cast<uint4 *>(x_norm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows, uint16_t *y,
+                                cudaStream_t s) {
+  combine_norm_kernel<false><<<(unsigned)rows, kCnThreads, 0, s>>>(
+      reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre), nullptr, 0.f,
+      reinterpret_cast<uint4 *>(y));
   return cudaGetLastError();
 }
 

@@ -1,29 +1,36 @@
-// pre_stats.cu -- the stats half of mhc_pre on GB300: per row, the 24
-// projections of the flattened residual on the 5th-generation tensor cores,
-// the row's sum of squares, and the split into gates and the Sinkhorn mix.
+// pre_stats.cu -- the stats half of mhc_pre and of mhc_hc_head on GB300: per
+// row, the projections of the flattened residual on the 5th-generation tensor
+// cores, the row's sum of squares, and the gates (plus, for the pre pass, the
+// Sinkhorn mix).
 //
 // Definitions: deepseek_v4.py (sglang), DeepseekV4DecoderLayer.hc_pre:
 // hc_pre_torch_impl (rsqrt of mean(x^2) + rms_eps; mixes = (x @ fn^T) * rsqrt)
-// and hc_split_sinkhorn (gates and the 4x4 Sinkhorn).
+// and hc_split_sinkhorn (gates and the 4x4 Sinkhorn); deepseek_v4.py,
+// hc_head_torch (4 mixes, pre = sigmoid(mix * scale + base) + hc_eps).
+//
+// Two builds of one kernel: NM = 24 mixes (the pre pass) and NM = 4 (hc_head).
 //
 // Decomposition.  A cluster of 16 CTAs owns a 128-row tile at a time; CTA s
 // owns hidden columns [320 s, 320 s + 320) of all four streams, i.e. 1280 of a
-// row's 20480 k.  fn's 24 x 1280 slice of the CTA, split into bf16 hi (B rows
-// 0..23) and lo (rows 24..47) halves, stays in shared memory (120 KB) for the
-// whole kernel, so each product is exact and the dot products carry ~2^-17
-// relative error per term.  Per tile and CTA:
-//   * TMA streams R[128 rows, 64 k] boxes (128-byte swizzle) through a
-//     5-stage ring -- R is read from HBM exactly once;
-//   * one thread issues tcgen05.mma (M=128 rows, N=48, K=16, bf16 -> fp32,
-//     two accumulators in tensor memory);
-//   * 16 row warps (4 lanes per row, 16 columns each) accumulate sum x^2 from
-//     the same stages, then read the accumulator and push each row's 24 mix
-//     partials and its sum of squares into the receive buffer of the CTA
-//     that finalises the row (CTA s owns tile rows 8s..8s+7);
-//   * 4 owner warps reduce the 16 partials of a row in CTA order, compute
-//     rsqrt, mix, the gates and the 4x4 Sinkhorn (16 lanes per row) and write
-//     pre, post and comb.
-// The combine + RMSNorm (x_norm) runs as a second, streaming launch
+// row's 20480 k.  fn's NM x 1280 slice of the CTA, split into bf16 hi (B rows
+// [0, NM)) and lo (rows [NM, 2 NM)) halves, zero-padded to the MMA's N, stays
+// in shared memory for the whole kernel (120 KB for 24 mixes), so each product
+// is exact and the dot products carry ~2^-17 relative error per term.  Per
+// tile and CTA:
+//   * warp 0 streams R[128 rows, 64 k] boxes (128-byte swizzle) with TMA
+//     through a 5-stage ring -- R is read from HBM exactly once;
+//   * one thread of warp 1 issues tcgen05.mma (M=128 rows, N = 48 or 16,
+//     K=16, bf16 -> fp32) into one of two accumulators in tensor memory;
+//   * row warps 4..7 (one thread per tile row) accumulate sum x^2 from the
+//     same stages;
+//   * readout warps 8..11 load the accumulator (tcgen05.ld) and push each
+//     row's NM mix partials and its sum of squares into the receive buffer of
+//     the CTA that finalises the row (CTA s owns tile rows 8s..8s+7), then
+//     signal all 16 CTAs with one cluster fence and relaxed remote arrives;
+//   * owner warps 2, 3, 12, 13 reduce the 16 partials of a row in CTA order,
+//     compute rsqrt, the mixes and the gates (and the 4x4 Sinkhorn, 16 lanes
+//     per row) and write them.
+// The combine (x_norm, or hc_head's y) runs as a second, streaming launch
 // (pre_simt.cu, combine_norm_kernel) that reads the pre gates this kernel
 // writes.
 //
@@ -74,11 +81,9 @@ constexpr int kBk = 64;                       // k per stage: 128-byte rows
 constexpr int kHb = kHs / kBk;                // 5 column blocks per stream
 constexpr int kKb = kHC * kHb;                // 20 k-blocks per tile per CTA
 constexpr int kStages = 5;
-constexpr int kN = 2 * kMix;                  // 48 = fn hi (24) + fn lo (24)
 constexpr int kStageBytes = kTile * kBk * 2;  // 16384
-constexpr int kFnBlkBytes = kN * kBk * 2;     // 6144
-constexpr int kRw = 28;                       // receive words per row: 24 dots, sum x^2, pad
 constexpr int kOwn = kTile / kCl;             // 8 rows finalised per CTA
+constexpr int kHeadMix = kHC;                 // hc_head: one mix per stream
 constexpr int kTmemCols = 128;                // two 48-column accumulators at 0 and 64
 
 static_assert(kHs % kBk == 0 && kTile % kCl == 0, "");
@@ -97,13 +102,6 @@ __device__ __forceinline__ int owner_index(int warp) {   // -1: not an owner war
   return warp == 2 || warp == 3 ? warp - 2 : (warp == 12 || warp == 13 ? warp - 10 : -1);
 }
 
-// ---- shared memory (offsets from a 1024-byte aligned base) -----------------
-constexpr int kOffFn = 0;
-constexpr int kOffStage = kOffFn + kKb * kFnBlkBytes;
-constexpr int kOffRecv = kOffStage + kStages * kStageBytes;   // [16 src][8 rows][kRw]
-constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;      // [8 rows][kRw]
-constexpr int kOffSs = kOffRed + kOwn * kRw * 4;              // [2][128 rows] sum x^2
-constexpr int kOffBar = kOffSs + 2 * kTile * 4;
 // mbarrier slots (arrays are given explicit, non-overlapping ranges)
 enum Bar : int {
   B_FULL = 0,                    // [kStages] TMA landed
@@ -120,12 +118,34 @@ enum Bar : int {
   B_COUNT = B_SSREADY + 2
 };
 static_assert(B_COUNT == 2 * kStages + 2 + 2 + 6 + 2, "barrier slots overlap");
-constexpr int kOffMisc = kOffBar + B_COUNT * 8;
-constexpr int kSmemUsed = kOffMisc + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
-static_assert(kOffStage % 1024 == 0 && kFnBlkBytes % 1024 == 0, "SW128 tiles need 1024-B alignment");
-static_assert(kOffRecv % 16 == 0 && (kRw * 4) % 16 == 0, "receive rows must take 16-byte stores");
+
+// Per-variant layout.  NM = 24: the pre pass (24 mixes); NM = 4: hc_head (4
+// mixes).  B holds fn hi in rows [0, NM), fn lo in [NM, 2 NM), zero padding
+// up to the MMA's N (a multiple of 16).  Shared memory offsets are from a
+// 1024-byte aligned base.
+template <int NM>
+struct Cfg {
+  static constexpr int kN = (2 * NM + 15) / 16 * 16;           // 48 / 16
+  static constexpr int kFnBlkBytes = kN * kBk * 2;               // 6144 / 2048
+  static constexpr int kRw = (NM + 1 + 3) / 4 * 4;               // NM dots, sum x^2, pad
+  static constexpr int kOffFn = 0;
+  static constexpr int kOffStage = kOffFn + kKb * kFnBlkBytes;
+  static constexpr int kOffRecv = kOffStage + kStages * kStageBytes;   // [16 src][8 rows][kRw]
+  static constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;      // [8 rows][kRw]
+  static constexpr int kOffSs = kOffRed + kOwn * kRw * 4;              // [2][128 rows] sum x^2
+  static constexpr int kOffBar = kOffSs + 2 * kTile * 4;
+  static constexpr int kOffMisc = kOffBar + B_COUNT * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // slack to align the base
+  // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N, M = 128
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kTile >> 4) << 24);
+  static_assert(NM == kMix || NM == kHeadMix, "two variants");
+  static_assert(kN <= 64, "an accumulator holds 64 columns");
+  static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
+  static_assert(kOffStage % 1024 == 0 && kFnBlkBytes % 1024 == 0, "SW128 tiles need 1024-B alignment");
+  static_assert(kOffRecv % 16 == 0 && (kRw * 4) % 16 == 0, "receive rows must take 16-byte stores");
+  static_assert(NM % 4 == 0 && (2 * NM) % 8 == 0, "pushes of 4 mixes; padding starts on an 8-row group");
+};
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
@@ -239,13 +259,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tc_ld2(uint32_t taddr, float &v0, float &v1) {
-  uint32_t r0, r1;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
-               : "=r"(r0), "=r"(r1) : "r"(taddr));
-  v0 = __uint_as_float(r0);
-  v1 = __uint_as_float(r1);
-}
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -270,9 +283,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
   return d;
 }
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N = 48, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) |
-                            ((uint32_t)(kTile >> 4) << 24);
 
 // ---- bounded waits ------------------------------------------------------------
 struct Abort {
@@ -327,8 +337,8 @@ struct StatsArgs {
   const float *scale;
   const float *base;
   float *pre_ws;     // [rows, 4] pre gates for the combine launch
-  float *post;
-  float *comb;
+  float *post;       // pre pass only
+  float *comb;       // pre pass only
   float *pre_out;
   float *mix_out;
   int64_t rows;
@@ -346,8 +356,10 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
 }
 
+template <int NM>
 __global__ void __launch_bounds__(kThreads, 1)
 pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
+  using C = Cfg<NM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -356,9 +368,9 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
   const uint32_t crank = cluster_rank();
   const int cid = (int)cluster_id(), ncl = (int)cluster_count();
   const int T = cid < a.num_tiles ? (a.num_tiles - 1 - cid) / ncl + 1 : 0;   // our tiles
-  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8u * (uint32_t)i; };
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
-  Abort ab{reinterpret_cast<volatile int *>(sm + kOffMisc + 4), crank};
+  auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * (uint32_t)i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kOffMisc);
+  Abort ab{reinterpret_cast<volatile int *>(sm + C::kOffMisc + 4), crank};
 
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
@@ -395,7 +407,16 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     // 10 loader warps; loads of 8 items are issued before any is converted
     const int loader = warp == kMmaWarp ? 0 : (warp < kRow0 ? warp - 1 : warp - kRowN - 1);
     const int lt = loader * 32 + lane, nl = (kWarps - 1 - kRowN) * 32;
-    constexpr int kItems = kMix * kKb * 8;     // 3840 items of 8 consecutive k
+    if constexpr (C::kN > 2 * NM) {
+      // zero the padding rows [2 NM, kN) of every k-block (whole 8-row groups)
+      constexpr int kPadRows = C::kN - 2 * NM, kPadChunks = kKb * kPadRows * 8;
+      for (int i = lt; i < kPadChunks; i += nl) {
+        const int j = i / (kPadRows * 8), r = 2 * NM + (i >> 3) % kPadRows, q = i & 7;
+        *reinterpret_cast<uint4 *>(sm + C::kOffFn + j * C::kFnBlkBytes + (r >> 3) * 1024 +
+                                   (r & 7) * 128 + (q << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    constexpr int kItems = NM * kKb * 8;       // items of 8 consecutive k (3840 for 24 mixes)
     for (int base = lt; base < kItems; base += 8 * nl) {
       float4 f0[8], f1[8];
 #pragma unroll
@@ -422,8 +443,8 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
           hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
           lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
         }
-        uint8_t *tile = sm + kOffFn + j * kFnBlkBytes;
-        const int nh = c, nlo = c + kMix;
+        uint8_t *tile = sm + C::kOffFn + j * C::kFnBlkBytes;
+        const int nh = c, nlo = c + NM;
         *reinterpret_cast<uint4 *>(tile + (nh >> 3) * 1024 + (nh & 7) * 128 + ((q ^ (nh & 7)) << 4)) =
             make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *reinterpret_cast<uint4 *>(tile + (nlo >> 3) * 1024 + (nlo & 7) * 128 +
@@ -453,7 +474,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         if (lane == 0) {
           mbar_expect_tx(bar(B_FULL + stage), kStageBytes);
           const int x = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk;
-          tma_load_2d(sb + kOffStage + stage * kStageBytes, &tmap, x, y, bar(B_FULL + stage));
+          tma_load_2d(sb + C::kOffStage + stage * kStageBytes, &tmap, x, y, bar(B_FULL + stage));
         }
         __syncwarp();
         last[stage] = (int)phase;
@@ -479,11 +500,11 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         if (!waitw(bar(B_FULL + stage), phase, false, ab, 3, it)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
-          const uint64_t ad = sw128_desc(sb + kOffStage + stage * kStageBytes);
-          const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes);
+          const uint64_t ad = sw128_desc(sb + C::kOffStage + stage * kStageBytes);
+          const uint64_t bd = sw128_desc(sb + C::kOffFn + j * C::kFnBlkBytes);
 #pragma unroll
           for (int kk = 0; kk < kBk / 16; ++kk)
-            tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (j | kk) != 0);
+            tc_mma(d, ad + 2 * kk, bd + 2 * kk, C::kIdesc, (j | kk) != 0);
           tc_commit(bar(B_EMPTY + stage));
         }
         __syncwarp();
@@ -502,7 +523,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     // ---- row warps: one thread per tile row; sum x^2 from every stage -------
     const int row = 32 * (warp & 3) + lane;     // tile row
     const int sw = row & 7;
-    float *ssbuf = reinterpret_cast<float *>(sm + kOffSs);
+    float *ssbuf = reinterpret_cast<float *>(sm + C::kOffSs);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -511,7 +532,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
       for (int j = 0; j < kKb; ++j) {
         if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, it)) { ok = false; break; }
         if (j == 0 && warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 2);
-        const uint8_t *st = sm + kOffStage + stage * kStageBytes + row * 128;
+        const uint8_t *st = sm + C::kOffStage + stage * kStageBytes + row * 128;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const uint4 c = *reinterpret_cast<const uint4 *>(st + ((q ^ sw) << 4));
@@ -543,7 +564,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     // accumulator + sum x^2 of tile t -> the owner CTA's receive buffer
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
     const int row = 32 * quarter + lane;
-    const float *ssbuf = reinterpret_cast<const float *>(sm + kOffSs);
+    const float *ssbuf = reinterpret_cast<const float *>(sm + C::kOffSs);
     for (int t = 0; t < T; ++t) {
       const int buf = t & 1;
       const uint32_t use = (uint32_t)(t >> 1);
@@ -551,30 +572,43 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
       if (!waitw(bar(B_SSREADY + buf), use & 1, false, ab, 11, t)) break;
       tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * 64);
-      float a0[16], a1[16], a2[16];             // columns 0..47: hi 0..23, lo 24..47
-      tc_ld16(ta + 0, a0);
-      tc_ld16(ta + 16, a1);
-      tc_ld16(ta + 32, a2);
-      tc_wait_ld();
-      const float ss = ssbuf[buf * kTile + row];
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
-      float mix[kMix];                          // hi + lo of the 24 dots
+      float mix[NM];                            // hi + lo of the NM dots
+      float ss;
+      if constexpr (NM == kMix) {
+        float a0[16], a1[16], a2[16];           // columns 0..47: hi 0..23, lo 24..47
+        tc_ld16(ta + 0, a0);
+        tc_ld16(ta + 16, a1);
+        tc_ld16(ta + 32, a2);
+        tc_wait_ld();
+        ss = ssbuf[buf * kTile + row];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mix[c] = a0[c] + a1[c + 8];
+        for (int c = 0; c < 8; ++c) mix[c] = a0[c] + a1[c + 8];
 #pragma unroll
-      for (int c = 8; c < 16; ++c) mix[c] = a0[c] + a2[c - 8];
+        for (int c = 8; c < 16; ++c) mix[c] = a0[c] + a2[c - 8];
 #pragma unroll
-      for (int c = 16; c < 24; ++c) mix[c] = a1[c - 16] + a2[c - 8];
+        for (int c = 16; c < 24; ++c) mix[c] = a1[c - 16] + a2[c - 8];
+      } else {
+        float a0[16];                           // columns 0..NM-1 hi, NM..2NM-1 lo
+        tc_ld16(ta + 0, a0);
+        tc_wait_ld();
+        ss = ssbuf[buf * kTile + row];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
+#pragma unroll
+        for (int c = 0; c < NM; ++c) mix[c] = a0[c] + a0[c + NM];
+      }
       // slot [our rank][row % 8] of the owner CTA (row / 8)
       if (!waitw(bar(B_PFREE), (uint32_t)(t & 1) ^ 1, true, ab, 6, t)) break;
-      const uint32_t dm = mapa(sb + kOffRecv + (uint32_t)(((crank * kOwn + (row & 7)) * kRw) * 4),
+      const uint32_t dm = mapa(sb + C::kOffRecv + (uint32_t)(((crank * kOwn + (row & 7)) * C::kRw) * 4),
                                (uint32_t)(row >> 3));
 #pragma unroll
-      for (int v = 0; v < 6; ++v)
+      for (int v = 0; v < NM / 4; ++v)
         st_cluster_v4(dm + 16 * v, mix[4 * v], mix[4 * v + 1], mix[4 * v + 2], mix[4 * v + 3]);
-      st_cluster_f32(dm + 4 * kMix, ss);
+      st_cluster_f32(dm + 4 * NM, ss);
       // make the stores visible cluster-wide, then count this warp in
       fence_cluster();
       __syncwarp();
@@ -592,11 +626,14 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     const int o = owner_index(warp) * 32 + lane;   // 0..127
     const int q = o >> 4, e = o & 15;           // row of 8, lane of 16
     const int row_t = (int)crank * kOwn + q;
-    const float *recv = reinterpret_cast<const float *>(sm + kOffRecv);
-    float *red = reinterpret_cast<float *>(sm + kOffRed);
-    const float sc0 = __ldg(a.scale), sc1 = __ldg(a.scale + 1), sc2 = __ldg(a.scale + 2);
-    const float bcomb = __ldg(a.base + 8 + e);
-    const float bgate = e < 8 ? __ldg(a.base + e) : 0.f;
+    const float *recv = reinterpret_cast<const float *>(sm + C::kOffRecv);
+    float *red = reinterpret_cast<float *>(sm + C::kOffRed);
+    // the pre pass reads scale[3] and base[24]; hc_head scale[1] and base[4]
+    const float sc0 = __ldg(a.scale);
+    const float sc1 = NM == kMix ? __ldg(a.scale + 1) : 0.f;
+    const float sc2 = NM == kMix ? __ldg(a.scale + 2) : 0.f;
+    const float bcomb = NM == kMix ? __ldg(a.base + 8 + e) : 0.f;
+    const float bgate = e < (NM == kMix ? 8 : kHC) ? __ldg(a.base + e) : 0.f;
     const unsigned full = 0xffffffffu;          // a row's 16 lanes are half the warp
     const int gb = lane & 16;
     for (int it = 0; it < T; ++it) {
@@ -605,11 +642,13 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
       if (warp == kOwnerLead && lane == 0) MHC_TRACE_AT(it, 5);
       // this row's 25 partials from the 16 CTAs, summed in CTA order
       float acc0 = 0.f, acc1 = 0.f;
+      if (e <= NM) {
 #pragma unroll
-      for (int src = 0; src < kCl; ++src) acc0 += recv[(src * kOwn + q) * kRw + e];
-      if (e + 16 <= kMix) {
+        for (int src = 0; src < kCl; ++src) acc0 += recv[(src * kOwn + q) * C::kRw + e];
+      }
+      if (e + 16 <= NM) {
 #pragma unroll
-        for (int src = 0; src < kCl; ++src) acc1 += recv[(src * kOwn + q) * kRw + e + 16];
+        for (int src = 0; src < kCl; ++src) acc1 += recv[(src * kOwn + q) * C::kRw + e + 16];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_OPULL));
@@ -618,36 +657,48 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         if (lane == 0) arrive_all_ctas(bar(B_PFREE), kCl);
         __syncwarp();
       }
-      float *rq = red + q * kRw;
-      rq[e] = acc0;
-      if (e + 16 <= kMix) rq[e + 16] = acc1;
+      float *rq = red + q * C::kRw;
+      if (e <= NM) rq[e] = acc0;
+      if (e + 16 <= NM) rq[e + 16] = acc1;
       __syncwarp();
-      const float rsq = 1.0f / sqrtf(rq[kMix] / (float)kK + a.rms_eps);
-      // gates: lanes 0..3 pre, 4..7 post
-      float gate = 0.f;
-      if (e < 8) {
-        const float l = fmaf(rq[e] * rsq, e < 4 ? sc0 : sc1, bgate);
-        const float sg = 1.0f / (1.0f + expf(-l));
-        gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
-      }
-      // Sinkhorn on exp(logits): lane e holds comb[e/4][e%4]
-      float C = expf(fmaf(rq[8 + e] * rsq, sc2, bcomb));
-      for (int k = 0; k < a.iters; ++k) {
-        float rs = C + __shfl_xor_sync(full, C, 1);
-        rs = rs + __shfl_xor_sync(full, rs, 2);
-        C = C / (rs + a.sink_eps);
-        float cs = C + __shfl_xor_sync(full, C, 4);
-        cs = cs + __shfl_xor_sync(full, cs, 8);
-        C = C / (cs + a.sink_eps);
-      }
-      if (grow < a.rows) {
-        a.comb[grow * 16 + e] = C;
-        if (e < 4) a.pre_ws[grow * kHC + e] = gate;
-        if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
-        if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
-        if (a.mix_out) {
-          a.mix_out[grow * kMix + e] = rq[e] * rsq;
-          if (e < 8) a.mix_out[grow * kMix + 16 + e] = rq[16 + e] * rsq;
+      const float rsq = 1.0f / sqrtf(rq[NM] / (float)kK + a.rms_eps);
+      if constexpr (NM == kHeadMix) {
+        // hc_head: lanes 0..3 hold pre_i = sigmoid(mix_i * scale + base_i) + hc_eps
+        if (grow < a.rows && e < kHC) {
+          const float mx = rq[e] * rsq;
+          const float sg = 1.0f / (1.0f + expf(-fmaf(mx, sc0, bgate)));
+          a.pre_ws[grow * kHC + e] = sg + a.pre_eps;
+          if (a.pre_out) a.pre_out[grow * kHC + e] = sg + a.pre_eps;
+          if (a.mix_out) a.mix_out[grow * NM + e] = mx;
+        }
+        (void)sc1; (void)sc2; (void)bcomb; (void)full;
+      } else {
+        // gates: lanes 0..3 pre, 4..7 post
+        float gate = 0.f;
+        if (e < 8) {
+          const float l = fmaf(rq[e] * rsq, e < 4 ? sc0 : sc1, bgate);
+          const float sg = 1.0f / (1.0f + expf(-l));
+          gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
+        }
+        // Sinkhorn on exp(logits): lane e holds comb[e/4][e%4]
+        float cm = expf(fmaf(rq[8 + e] * rsq, sc2, bcomb));
+        for (int k = 0; k < a.iters; ++k) {
+          float rs = cm + __shfl_xor_sync(full, cm, 1);
+          rs = rs + __shfl_xor_sync(full, rs, 2);
+          cm = cm / (rs + a.sink_eps);
+          float cs = cm + __shfl_xor_sync(full, cm, 4);
+          cs = cs + __shfl_xor_sync(full, cs, 8);
+          cm = cm / (cs + a.sink_eps);
+        }
+        if (grow < a.rows) {
+          a.comb[grow * 16 + e] = cm;
+          if (e < 4) a.pre_ws[grow * kHC + e] = gate;
+          if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
+          if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
+          if (a.mix_out) {
+            a.mix_out[grow * NM + e] = rq[e] * rsq;
+            if (e < 8) a.mix_out[grow * NM + 16 + e] = rq[16 + e] * rsq;
+          }
         }
       }
       if (warp == kOwnerLead && lane == 0) MHC_TRACE_AT(it, 6);
@@ -690,18 +741,21 @@ EncodeTiled encode_fn() {
 
 constexpr int kMaxDev = 64;
 std::mutex g_dev_mu;
+template <int NM>
 int g_max_clusters[kMaxDev];   // 0: not yet configured on that device
 
+template <int NM>
 cudaError_t configure(int dev, int *max_clusters) {
   std::lock_guard<std::mutex> lock(g_dev_mu);
-  if (g_max_clusters[dev] > 0) {
-    *max_clusters = g_max_clusters[dev];
+  if (g_max_clusters<NM>[dev] > 0) {
+    *max_clusters = g_max_clusters<NM>[dev];
     return cudaSuccess;
   }
-  cudaError_t e = cudaFuncSetAttribute(pre_stats_kernel,
+  constexpr int kSmemBytes = Cfg<NM>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(pre_stats_kernel<NM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pre_stats_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(pre_stats_kernel<NM>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
@@ -715,20 +769,17 @@ cudaError_t configure(int dev, int *max_clusters) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, pre_stats_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, pre_stats_kernel<NM>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
-  g_max_clusters[dev] = n;
+  g_max_clusters<NM>[dev] = n;
   *max_clusters = n;
   return cudaSuccess;
 }
 
-}  // namespace
-
-cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
-                             const float *base, int64_t rows, int64_t logical_rows,
-                             const mhc_params &p, float *pre_ws, float *post, float *comb,
-                             float *pre_out, float *mix_out, cudaStream_t s) {
+template <int NM>
+cudaError_t launch_stats(const uint16_t *R, const StatsArgs &a, int64_t logical_rows,
+                         cudaStream_t s) {
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   int dev = 0;
@@ -736,11 +787,11 @@ cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *sc
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   int max_clusters = 0;
-  e = configure(dev, &max_clusters);
+  e = configure<NM>(dev, &max_clusters);
   if (e != cudaSuccess) return e;
 
   CUtensorMap map;
-  const cuuint64_t gdim[2] = {(cuuint64_t)kK, (cuuint64_t)rows};
+  const cuuint64_t gdim[2] = {(cuuint64_t)kK, (cuuint64_t)a.rows};
   const cuuint64_t gstride[1] = {(cuuint64_t)kK * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kBk, (cuuint32_t)kTile};
   const cuuint32_t estride[2] = {1, 1};
@@ -748,14 +799,6 @@ cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *sc
           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-
-  StatsArgs a;
-  a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
-  a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out;
-  a.rows = rows;
-  a.num_tiles = (int)((rows + kTile - 1) / kTile);
-  a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.sink_eps = p.hc_sinkhorn_eps;
-  a.post_mult = p.post_mult; a.iters = p.sinkhorn_iters;
 
   // grid: as many clusters as fit at once, never more than the whole chunk's
   // tiles (the count depends on logical_rows only; per-row arithmetic does not
@@ -767,7 +810,7 @@ cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *sc
   cudaLaunchAttribute at[1];
   cfg.gridDim = dim3((unsigned)(clusters * kCl));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<NM>::kSmemBytes;
   cfg.stream = s;
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = kCl;
@@ -775,7 +818,36 @@ cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *sc
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pre_stats_kernel, map, a);
+  return cudaLaunchKernelEx(&cfg, pre_stats_kernel<NM>, map, a);
+}
+
+}  // namespace
+
+cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
+                             const float *base, int64_t rows, int64_t logical_rows,
+                             const mhc_params &p, float *pre_ws, float *post, float *comb,
+                             float *pre_out, float *mix_out, cudaStream_t s) {
+  StatsArgs a;
+  a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
+  a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out;
+  a.rows = rows;
+  a.num_tiles = (int)((rows + kTile - 1) / kTile);
+  a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.sink_eps = p.hc_sinkhorn_eps;
+  a.post_mult = p.post_mult; a.iters = p.sinkhorn_iters;
+  return launch_stats<kMix>(R, a, logical_rows, s);
+}
+
+cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *scale,
+                              const float *base, int64_t rows, int64_t logical_rows,
+                              float norm_eps, float hc_eps, float *pre_ws, float *pre_out,
+                              float *mix_out, cudaStream_t s) {
+  StatsArgs a;
+  a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
+  a.post = nullptr; a.comb = nullptr; a.pre_out = pre_out; a.mix_out = mix_out;
+  a.rows = rows;
+  a.num_tiles = (int)((rows + kTile - 1) / kTile);
+  a.rms_eps = norm_eps; a.pre_eps = hc_eps; a.sink_eps = 0.f; a.post_mult = 0.f; a.iters = 0;
+  return launch_stats<kHeadMix>(R, a, logical_rows, s);
 }
 
 #ifdef MHC_TRACE

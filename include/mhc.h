@@ -91,8 +91,8 @@ const char *mhc_last_cuda_error(void);
 size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
- * or nonzero once the stats kernel of mhc_pre gave up a bounded wait (it then
- * returned early and its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
+ * or nonzero once the stats kernel of mhc_pre or mhc_hc_head gave up a bounded
+ * wait (it then returned early and its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
  * the device's pending work.  Returns MHC_OK or MHC_ERR_NULL/MHC_ERR_CUDA. */
 int mhc_kernel_status(uint32_t *status, int reset);
 
@@ -214,6 +214,41 @@ int mhc_post(const uint16_t *R, const uint16_t *y, const float *post, const floa
 int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
                      float norm_eps, int64_t rows, int64_t logical_rows, uint16_t *x_norm,
                      void *stream);
+
+/*
+ * mhc_hc_head -- the model's final collapse of the 4 residual streams into one
+ * hidden state (run once per forward, after the last decoder layer and before
+ * the final norm).
+ *
+ * deepseek_v4.py, make_hc_head_params and hc_head_torch: with x = R[m]
+ * flattened stream-major in fp32,
+ *   rsqrt  = 1 / sqrt(mean_k x_k^2 + norm_eps)
+ *   mix[i] = rsqrt * sum_k x_k * fn[i, k]                      (i < 4)
+ *   pre[i] = sigmoid(mix[i] * scale[0] + base[i]) + hc_eps
+ *   y[m,h] = bf16( sum_i pre[i] * R[m, i, h] )     (fp32 sum, one rounding)
+ *
+ * Two launches: mhc_pre's tensor-core stats kernel built for 4 mixes (the
+ * gates go to the workspace), then a streaming combine.
+ *
+ * Arguments
+ *   R        [rows, 4, 5120] bf16      residual after the last layer
+ *   fn       [4, 20480] fp32           hc_head_fn
+ *   scale    [1] fp32                  hc_head_scale
+ *   base     [4] fp32                  hc_head_base
+ *   norm_eps, hc_eps                   >= 0 and finite (the model's norm_eps
+ *                                      and hc_eps)
+ *   workspace, workspace_bytes  as for mhc_pre: at least
+ *            mhc_pre_workspace_bytes(rows) bytes, 256-byte aligned.
+ * Outputs
+ *   y        [rows, 5120] bf16         collapsed hidden state
+ *   pre_out  [rows, 4] fp32 or NULL    the gates
+ *   mix_out  [rows, 4] fp32 or NULL    the mixes (after rsqrt scaling)
+ * Errors as for mhc_pre.
+ */
+int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const float *base,
+                int64_t rows, int64_t logical_rows, float norm_eps, float hc_eps,
+                void *workspace, size_t workspace_bytes, uint16_t *y, float *pre_out,
+                float *mix_out, void *stream);
 
 #ifdef __cplusplus
 }

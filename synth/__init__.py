@@ -37,6 +37,7 @@ _TWO_M32 = 1.0 / 4294967296.0
 
 # tensor ids of the recipe
 T_R, T_FN, T_BASE, T_SCALE, T_W, T_Y, T_Y2 = 1, 2, 3, 4, 5, 6, 7
+T_HFN, T_HBASE, T_HSCALE = 8, 9, 10          # hc_head's parameters
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -144,6 +145,22 @@ def weights(seed: int) -> Weights:
     scale = (0.01 + 0.05 * uniform(seed, T_SCALE, 3)).astype(np.float32)
     w = f32_to_bf16_bits((1.0 + 0.1 * normal(seed, T_W, H)).astype(np.float32))
     return Weights(fn=fn, base=base, scale=scale, norm_w=w)
+
+
+@dataclass
+class HeadWeights:
+    fn: np.ndarray      # [4, 20480] float32
+    base: np.ndarray    # [4] float32
+    scale: np.ndarray   # [1] float32
+
+
+def head_weights(seed: int) -> HeadWeights:
+    """hc_head's fn [4, 4H], base [4], scale [1] (deepseek_v4.py,
+    make_hc_head_params), drawn like the layer's mixing parameters."""
+    fn = (0.0225 * normal(seed, T_HFN, HC * K)).astype(np.float32).reshape(HC, K)
+    base = (3.0 * normal(seed, T_HBASE, HC)).astype(np.float32)
+    scale = (0.01 + 0.05 * uniform(seed, T_HSCALE, 1)).astype(np.float32)
+    return HeadWeights(fn=fn, base=base, scale=scale)
 
 
 @dataclass

@@ -129,3 +129,29 @@ def test_combine_norm_validation(lib):
     assert f(fake(0), None, fake(2), ctypes.c_float(1e-6), 4, 4, fake(3), None) == ERR_NULL
     assert f(fake(0), fake(1), fake(2), ctypes.c_float(1e-6), 4, 2, fake(3), None) == ERR_SHAPE
     assert f(fake(0), fake(1), fake(2), ctypes.c_float(1e-6), 4, 4, fake(0), None) == ERR_OVERLAP
+
+
+def call_head(lib, rows=4, logical=4, ws=fake(9), ws_bytes=None, norm_eps=1e-6, hc_eps=1e-6,
+              **over):
+    a = dict(R=fake(0), fn=fake(1), scale=fake(2), base=fake(3), y=fake(5), pre=None, mix=None)
+    a.update(over)
+    wsb = lib.mhc_pre_workspace_bytes(rows) if ws_bytes is None else ws_bytes
+    return lib.mhc_hc_head(a["R"], a["fn"], a["scale"], a["base"], rows, logical,
+                           ctypes.c_float(norm_eps), ctypes.c_float(hc_eps), ws, wsb, a["y"],
+                           a["pre"], a["mix"], None)
+
+
+def test_hc_head_validation(lib):
+    assert call_head(lib, rows=-1) == ERR_SHAPE
+    assert call_head(lib, rows=5, logical=4) == ERR_SHAPE
+    assert call_head(lib, norm_eps=-1.0) == ERR_PARAM
+    assert call_head(lib, hc_eps=float("inf")) == ERR_PARAM
+    assert call_head(lib, rows=0, logical=0, R=None) == 0
+    assert call_head(lib, base=None) == ERR_NULL
+    assert call_head(lib, y=fake(5) + 2) == ERR_ALIGN
+    assert call_head(lib, pre=fake(6) + 4) == ERR_ALIGN
+    assert call_head(lib, ws=None) == ERR_WORKSPACE
+    assert call_head(lib, ws_bytes=8) == ERR_WORKSPACE
+    assert call_head(lib, y=fake(0)) == ERR_OVERLAP                       # y on R
+    assert call_head(lib, ws=fake(5)) == ERR_OVERLAP                      # workspace on y
+    assert call_head(lib, pre=fake(6), mix=fake(6)) == ERR_OVERLAP        # two outputs
