@@ -420,6 +420,65 @@ def run_op(args):
         nbytes, launches = M * HEAD_BYTES_ROW + HEAD_BYTES_CALL, 2
         metric = "mhc_hc_head rows/s (final stream collapse) and achieved HBM GB/s"
         workload = f"M={M} rows: R[M,4,5120] bf16, hc_head fn[4,20480] f32 (seed {SEED})"
+    elif args.op == "latency":
+        # decode-size rows: one step = mhc_pre + mhc_post; latency per step,
+        # launched eagerly and replayed from a CUDA graph
+        W = synth.weights(SEED)
+        fn = torch.from_numpy(W.fn).to(dev)
+        scale = torch.from_numpy(W.scale).to(dev)
+        base = torch.from_numpy(W.base).to(dev)
+        w = bf(W.norm_w)
+        yv = bf(synth.sublayer_out(SEED, M))
+        xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        post = torch.empty((M, HC), dtype=torch.float32, device=dev)
+        comb = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
+        R2 = torch.empty_like(R)
+        ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+        side = torch.cuda.Stream(dev)
+
+        LM = args.logical_rows or M
+
+        def launch(st):
+            m.mhc_pre(R, fn, scale, base, w, logical_rows=LM, workspace=ws, x_norm=xn, post=post,
+                      comb=comb, stream=st)
+            m.mhc_post(R, yv, post, comb, logical_rows=LM, out=R2, stream=st)
+
+        def timed(fn_, n):
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(side)
+            for _ in range(n):
+                fn_()
+            b.record(side)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / n * 1e3          # us per step
+
+        with torch.cuda.stream(side):
+            for _ in range(args.warmup):
+                launch(side)
+            eager_us = timed(lambda: launch(side), args.steps)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                launch(side)
+            for _ in range(args.warmup):
+                g.replay()
+            graph_us = timed(g.replay, args.steps)
+        nbytes = M * (PRE_BYTES_ROW + POST_BYTES_ROW) + PRE_BYTES_CALL
+        line = {
+            "metric": f"mhc_pre + mhc_post latency at M={M} rows (decode-size step)",
+            "value": graph_us, "unit": "us/step", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": graph_us / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"M={M} rows of R[M,4,5120] bf16 (seed {SEED}); inputs "
+                                   "L2-resident between steps (decode-size, latency-bound)",
+                       "op": "latency", "rows": M, "logical_rows": LM, "eager_us": eager_us,
+                       "graph_us": graph_us},
+            "roofline": {"bound": "latency", "algorithmic_bytes_per_step": nbytes,
+                         "achieved_gbs_graph": nbytes / (graph_us * 1e-6) / 1e9},
+            "gpu_launches": 3 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+        return
     else:
         raise SystemExit(f"unknown --op {args.op}")
 
@@ -463,9 +522,11 @@ def main():
     ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["step", "hc_head"], default="step",
+    ap.add_argument("--op", choices=["step", "hc_head", "latency"], default="step",
                     help="step: mhc_pre + mhc_post (the headline); others time one entry "
                          "point alone")
+    ap.add_argument("--logical-rows", type=int, default=0,
+                    help="--op latency: the chunk's row count (default: --rows)")
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows per GPU (default: the 16384-row chunk); other sizes are "
                          "for profiling runs")

@@ -87,10 +87,17 @@ const char *mhc_strerror(int code) {
 
 const char *mhc_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
+namespace {
+size_t gate_bytes(int64_t rows) {
+  return ((size_t)rows * MHC_HC * sizeof(float) + 255) & ~(size_t)255;
+}
+}  // namespace
+
 size_t mhc_pre_workspace_bytes(int64_t rows) {
   if (rows <= 0) return 0;
-  // the pre gates [rows, 4] fp32, handed from the stats launch to the combine
-  return ((size_t)rows * MHC_HC * sizeof(float) + 255) & ~(size_t)255;
+  // the pre gates [rows, 4] fp32, handed from the stats launch to the
+  // combine (the decode-size path uses none of it)
+  return gate_bytes(rows);
 }
 
 int mhc_kernel_status_detail(uint32_t *where64) {
@@ -151,10 +158,18 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
   if (int e = check_device()) return e;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *pre_ws = static_cast<float *>(workspace);
-  cudaError_t ce = mhc::launch_pre_stats(R, fn, scale, base, rows, logical_rows, p, pre_ws, post,
-                                         comb, pre_out, mix_out, s);
-  if (ce == cudaSuccess)
-    ce = mhc::launch_combine_norm(R, pre_ws, norm_w, p.norm_eps, rows, logical_rows, x_norm, s);
+  cudaError_t ce;
+  if (logical_rows <= mhc::kDecodeMaxRows) {
+    // decode-size chunk: latency-shaped CUDA-core path (keyed on the chunk's
+    // row count, so every shard of the chunk takes it)
+    ce = mhc::launch_pre_decode(R, fn, scale, base, norm_w, rows, logical_rows, p, x_norm, post,
+                                comb, pre_out, mix_out, s);
+  } else {
+    ce = mhc::launch_pre_stats(R, fn, scale, base, rows, logical_rows, p, pre_ws, post, comb,
+                               pre_out, mix_out, s);
+    if (ce == cudaSuccess)
+      ce = mhc::launch_combine_norm(R, pre_ws, norm_w, p.norm_eps, rows, logical_rows, x_norm, s);
+  }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 

@@ -65,6 +65,16 @@ cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *sca
                             uint16_t *x_norm, float *post, float *comb, float *pre_out,
                             float *mix_out, cudaStream_t s);
 
+// decode-size chunks (logical_rows <= kDecodeMaxRows): all of mhc_pre in one
+// launch of 16-CTA clusters, up to 8 rows per cluster pass, no scratch
+// (pre_decode.cu)
+constexpr int64_t kDecodeMaxRows = 48;
+cudaError_t launch_pre_decode(const uint16_t *R, const float *fn, const float *scale,
+                              const float *base, const uint16_t *norm_w, int64_t rows,
+                              int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
+                              float *post, float *comb, float *pre_out, float *mix_out,
+                              cudaStream_t s);
+
 // tensor-core stats half of mhc_pre (cluster of 16 CTAs): writes the pre gates
 // to pre_ws [rows, 4] for the combine launch, and post, comb (+ pre_out, mix_out)
 cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,

@@ -146,16 +146,13 @@ constexpr int kCnThreads = 128;
 constexpr int kCnChunks = kChunksPerStream / kCnThreads;   // 5
 static_assert(kChunksPerStream % kCnThreads == 0, "");
 
+// One row by one 128-thread block: y = sum_i pv_i R_i in fp32, then x_norm
+// (kNorm) or y itself, cast once to bf16.
 template <bool kNorm>
-__global__ void __launch_bounds__(kCnThreads)
-combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
-                    const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out) {
-  // last rows first: after mhc_pre's stats launch the most recently read rows
-  // are the ones still in L2
-  const int64_t row = (int64_t)gridDim.x - 1 - blockIdx.x;
+__device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const float (&pv)[kHC],
+                                            const uint4 *__restrict__ w, float norm_eps,
+                                            uint4 *__restrict__ out, int64_t row) {
   const int tid = threadIdx.x;
-  const float4 pq = __ldg(pre + row);
-  const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
   const uint4 *r = R + row * (kHC * kChunksPerStream);
 
   float y[kCnChunks][8];
@@ -203,6 +200,18 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
       st_stream(o + c, pack8_rn(v));
     }
   }
+}
+
+template <bool kNorm>
+__global__ void __launch_bounds__(kCnThreads)
+combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
+                    const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out) {
+  // last rows first: after mhc_pre's stats launch the most recently read rows
+  // are the ones still in L2
+  const int64_t row = (int64_t)gridDim.x - 1 - blockIdx.x;
+  const float4 pq = __ldg(pre + row);
+  const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
+  combine_row<kNorm>(R, pv, w, norm_eps, out, row);
 }
 
 }  // namespace

@@ -123,11 +123,15 @@ int mhc_kernel_status_detail(uint32_t *where64);
  * (RMSNorm fused without rounding y first, as the fused combine+norm gate of
  * prefill_sp.py, _combine_norm_fused, requires.)
  *
- * Two launches: (1) stats (pre_stats.cu): a cluster of 16 CTAs splits each
- * 128-row tile by hidden columns, streams R once with TMA, runs the 24
- * projections on the tensor cores against fn split into bf16 hi + lo, and
- * finalises the gates and the Sinkhorn per row; (2) combine + RMSNorm
- * (pre_simt.cu, combine_norm_kernel), streaming R again with the gates.
+ * Chunks of more than 48 rows (logical_rows > 48) take two launches:
+ * (1) stats (pre_stats.cu): a cluster of 16 CTAs splits each 128-row tile by
+ * hidden columns, streams R once with TMA, runs the 24 projections on the
+ * tensor cores against fn split into bf16 hi + lo, and finalises the gates
+ * and the Sinkhorn per row; (2) combine + RMSNorm (pre_simt.cu,
+ * combine_norm_kernel), streaming R again with the gates.  Decode-size
+ * chunks (logical_rows <= 48) take one latency-shaped launch (pre_decode.cu):
+ * 16-CTA clusters of CUDA-core work, up to 8 rows per cluster pass, that
+ * leave the workspace untouched.
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual rows

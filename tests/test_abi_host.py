@@ -64,6 +64,7 @@ def test_strerror_and_defaults(lib):
     assert lib.mhc_pre_workspace_bytes(0) == 0
     assert lib.mhc_pre_workspace_bytes(1000) == 16128   # the pre gates, 256-byte rounded
     assert lib.mhc_pre_workspace_bytes(1) == 256
+    assert lib.mhc_pre_workspace_bytes(257) == 4352
 
 
 A = 1 << 32          # fake, 256-byte aligned device addresses, far apart
