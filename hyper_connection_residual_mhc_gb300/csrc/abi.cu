@@ -91,13 +91,17 @@ namespace {
 size_t gate_bytes(int64_t rows) {
   return ((size_t)rows * MHC_HC * sizeof(float) + 255) & ~(size_t)255;
 }
+size_t logit_bytes(int64_t rows) {
+  return ((size_t)rows * 16 * sizeof(float) + 255) & ~(size_t)255;
+}
 }  // namespace
 
 size_t mhc_pre_workspace_bytes(int64_t rows) {
   if (rows <= 0) return 0;
-  // the pre gates [rows, 4] fp32, handed from the stats launch to the
-  // combine (the decode-size path uses none of it)
-  return gate_bytes(rows);
+  // handed from the stats launch to the combine launch: the pre gates
+  // [rows, 4] fp32, then the comb logits [rows, 16] fp32, each 256-byte
+  // rounded (the decode-size path uses none of it)
+  return gate_bytes(rows) + logit_bytes(rows);
 }
 
 int mhc_kernel_status_detail(uint32_t *where64) {
@@ -165,10 +169,12 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
     ce = mhc::launch_pre_decode(R, fn, scale, base, norm_w, rows, logical_rows, p, x_norm, post,
                                 comb, pre_out, mix_out, s);
   } else {
-    ce = mhc::launch_pre_stats(R, fn, scale, base, rows, logical_rows, p, pre_ws, post, comb,
+    float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
+    ce = mhc::launch_pre_stats(R, fn, scale, base, rows, logical_rows, p, pre_ws, logit_ws, post,
                                pre_out, mix_out, s);
     if (ce == cudaSuccess)
-      ce = mhc::launch_combine_norm(R, pre_ws, norm_w, p.norm_eps, rows, logical_rows, x_norm, s);
+      ce = mhc::launch_combine_norm_sinkhorn(R, pre_ws, norm_w, p.norm_eps, logit_ws, comb,
+                                             p.hc_sinkhorn_eps, p.sinkhorn_iters, rows, x_norm, s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }

@@ -76,11 +76,19 @@ cudaError_t launch_pre_decode(const uint16_t *R, const float *fn, const float *s
                               cudaStream_t s);
 
 // tensor-core stats half of mhc_pre (cluster of 16 CTAs): writes the pre gates
-// to pre_ws [rows, 4] for the combine launch, and post, comb (+ pre_out, mix_out)
+// to pre_ws [rows, 4] and the comb logits to logit_ws [rows, 16] for the
+// combine launch, and post (+ pre_out, mix_out)
 cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
                              const float *base, int64_t rows, int64_t logical_rows,
-                             const mhc_params &p, float *pre_ws, float *post, float *comb,
+                             const mhc_params &p, float *pre_ws, float *logit_ws, float *post,
                              float *pre_out, float *mix_out, cudaStream_t s);
+// combine + RMSNorm with a fifth warp per row block for the Sinkhorn of the
+// comb logits (writes comb [rows, 4, 4])
+cudaError_t launch_combine_norm_sinkhorn(const uint16_t *R, const float *pre,
+                                         const uint16_t *norm_w, float norm_eps,
+                                         const float *logit, float *comb, float sink_eps,
+                                         int iters, int64_t rows, uint16_t *x_norm,
+                                         cudaStream_t s);
 // the same stats kernel built for hc_head's 4 mixes: writes the gates to
 // pre_ws [rows, 4] (+ pre_out, mix_out [rows, 4])
 cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *scale,

@@ -185,7 +185,8 @@ __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const f
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     if ((tid & 31) == 0) red[tid >> 5] = ss;
-    __syncthreads();
+    // the 4 combine warps only (a block may carry a Sinkhorn warp besides)
+    asm volatile("bar.sync 1, %0;" ::"n"(kCnThreads) : "memory");
     const float tot = ((red[0] + red[1]) + red[2]) + red[3];
     const float rn = 1.0f / sqrtf(tot / (float)kH + norm_eps);
 
@@ -202,13 +203,42 @@ __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const f
   }
 }
 
-template <bool kNorm>
-__global__ void __launch_bounds__(kCnThreads)
+// The row's 4x4 Sinkhorn (hc_split_sinkhorn) from its 16 comb logits, by one
+// warp: lane e holds comb[e/4][e%4] (lanes 16..31 mirror 0..15); each
+// iteration divides by the row sums (pairs (c0 + c1) + (c2 + c3)), then by
+// the column sums, eps added to every sum.
+__device__ __forceinline__ void sinkhorn_row(const float *__restrict__ logit,
+                                             float *__restrict__ comb, int64_t row, float eps,
+                                             int iters) {
+  const int lane = threadIdx.x & 31, e = lane & 15;
+  const unsigned full = 0xffffffffu;
+  float cm = expf(__ldg(logit + row * 16 + e));
+  for (int k = 0; k < iters; ++k) {
+    float rs = cm + __shfl_xor_sync(full, cm, 1);
+    rs = rs + __shfl_xor_sync(full, rs, 2);
+    cm = cm / (rs + eps);
+    float cs = cm + __shfl_xor_sync(full, cm, 4);
+    cs = cs + __shfl_xor_sync(full, cs, 8);
+    cm = cm / (cs + eps);
+  }
+  if (lane < 16) comb[row * 16 + e] = cm;
+}
+
+// kSink: a fifth warp runs the row's Sinkhorn while the four combine warps
+// stream R (the stats launch leaves the comb logits in the workspace).
+template <bool kNorm, bool kSink>
+__global__ void __launch_bounds__(kCnThreads + 32)
 combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
-                    const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out) {
+                    const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out,
+                    const float *__restrict__ logit, float *__restrict__ comb, float sink_eps,
+                    int iters) {
   // last rows first: after mhc_pre's stats launch the most recently read rows
   // are the ones still in L2
   const int64_t row = (int64_t)gridDim.x - 1 - blockIdx.x;
+  if (threadIdx.x >= kCnThreads) {
+    if constexpr (kSink) sinkhorn_row(logit, comb, row, sink_eps, iters);
+    return;
+  }
   const float4 pq = __ldg(pre + row);
   const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
   combine_row<kNorm>(R, pv, w, norm_eps, out, row);
@@ -226,17 +256,30 @@ size_t pre_simt_workspace_bytes(int64_t rows) {
 cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
                                 float norm_eps, int64_t rows, int64_t /*logical_rows*/,
                                 uint16_t *x_norm, cudaStream_t s) {
-  combine_norm_kernel<true><<<(unsigned)rows, kCnThreads, 0, s>>>(
+  combine_norm_kernel<true, false><<<(unsigned)rows, kCnThreads, 0, s>>>(
       reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
-      reinterpret_cast<const uint4 *>(norm_w), norm_eps, reinterpret_cast<uint4 *>(x_norm));
+      reinterpret_cast<const uint4 *>(norm_w), norm_eps, reinterpret_cast<uint4 *>(x_norm),
+      nullptr, nullptr, 0.f, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_norm_sinkhorn(const uint16_t *R, const float *pre,
+                                         const uint16_t *norm_w, float norm_eps,
+                                         const float *logit, float *comb, float sink_eps,
+                                         int iters, int64_t rows, uint16_t *x_norm,
+                                         cudaStream_t s) {
+  combine_norm_kernel<true, true><<<(unsigned)rows, kCnThreads + 32, 0, s>>>(
+      reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
+      reinterpret_cast<const uint4 *>(norm_w), norm_eps, reinterpret_cast<uint4 *>(x_norm),
+      logit, comb, sink_eps, iters);
   return cudaGetLastError();
 }
 
 cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows, uint16_t *y,
                                 cudaStream_t s) {
-  combine_norm_kernel<false><<<(unsigned)rows, kCnThreads, 0, s>>>(
+  combine_norm_kernel<false, false><<<(unsigned)rows, kCnThreads, 0, s>>>(
       reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre), nullptr, 0.f,
-      reinterpret_cast<uint4 *>(y));
+      reinterpret_cast<uint4 *>(y), nullptr, nullptr, 0.f, 0);
   return cudaGetLastError();
 }
 

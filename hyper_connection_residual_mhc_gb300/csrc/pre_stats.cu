@@ -22,17 +22,18 @@
 //   * one thread of warp 1 issues tcgen05.mma (M=128 rows, N = 48 or 16,
 //     K=16, bf16 -> fp32) into one of two accumulators in tensor memory;
 //   * row warps 4..7 (one thread per tile row) accumulate sum x^2 from the
-//     same stages;
+//     same stages (one accumulator per 16-byte chunk, summed in a fixed tree);
 //   * readout warps 8..11 load the accumulator (tcgen05.ld) and push each
 //     row's NM mix partials and its sum of squares into the receive buffer of
 //     the CTA that finalises the row (CTA s owns tile rows 8s..8s+7), then
 //     signal all 16 CTAs with one cluster fence and relaxed remote arrives;
 //   * owner warps 2, 3, 12, 13 reduce the 16 partials of a row in CTA order,
-//     compute rsqrt, the mixes and the gates (and the 4x4 Sinkhorn, 16 lanes
-//     per row) and write them.
+//     compute rsqrt, the mixes and the gates (and, for the pre pass, the 16
+//     comb logits) and write them.
 // The combine (x_norm, or hc_head's y) runs as a second, streaming launch
 // (pre_simt.cu, combine_norm_kernel) that reads the pre gates this kernel
-// writes.
+// writes; for the pre pass a fifth warp per row there runs the 4x4 Sinkhorn
+// on the comb logits.
 //
 // Every row is reduced in one fixed order that depends only on its own data
 // (same MMA sequence, same lanes, CTA-ordered cross-CTA sums), so any row
@@ -338,7 +339,7 @@ struct StatsArgs {
   const float *base;
   float *pre_ws;     // [rows, 4] pre gates for the combine launch
   float *post;       // pre pass only
-  float *comb;       // pre pass only
+  float *logit_ws;   // pre pass only: [rows, 16] comb logits for the combine launch
   float *pre_out;
   float *mix_out;
   int64_t rows;
@@ -528,20 +529,26 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     uint32_t phase = 0;
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
-      float ss = 0.f;
+      // one accumulator per 16-byte chunk of the 128-byte row slice: eight
+      // short FMA chains instead of one long one (summed in a fixed tree)
+      float ssq[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ssq[q] = 0.f;
       for (int j = 0; j < kKb; ++j) {
         if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, it)) { ok = false; break; }
         if (j == 0 && warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 2);
         const uint8_t *st = sm + C::kOffStage + stage * kStageBytes + row * 128;
+        uint4 cq[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) cq[q] = *reinterpret_cast<const uint4 *>(st + ((q ^ sw) << 4));
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const uint4 c = *reinterpret_cast<const uint4 *>(st + ((q ^ sw) << 4));
-          const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+          const uint32_t w4[4] = {cq[q].x, cq[q].y, cq[q].z, cq[q].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float x0 = lo_bf(w4[e]), x1 = hi_bf(w4[e]);
-            ss = fmaf(x0, x0, ss);
-            ss = fmaf(x1, x1, ss);
+            ssq[q] = fmaf(x0, x0, ssq[q]);
+            ssq[q] = fmaf(x1, x1, ssq[q]);
           }
         }
         // the stage is released only after every lane has used its data
@@ -555,6 +562,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
       // was read out)
       const int buf = it & 1;
       if (!waitw(bar(B_TEMPTY + buf), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 10, it)) break;
+      const float ss = ((ssq[0] + ssq[1]) + (ssq[2] + ssq[3])) + ((ssq[4] + ssq[5]) + (ssq[6] + ssq[7]));
       ssbuf[buf * kTile + row] = ss;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_SSREADY + buf));
@@ -673,25 +681,17 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         }
         (void)sc1; (void)sc2; (void)bcomb; (void)full;
       } else {
-        // gates: lanes 0..3 pre, 4..7 post
+        // gates: lanes 0..3 pre, 4..7 post; lane e's comb logit (the combine
+        // launch runs the Sinkhorn on them)
         float gate = 0.f;
         if (e < 8) {
           const float l = fmaf(rq[e] * rsq, e < 4 ? sc0 : sc1, bgate);
           const float sg = 1.0f / (1.0f + expf(-l));
           gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
         }
-        // Sinkhorn on exp(logits): lane e holds comb[e/4][e%4]
-        float cm = expf(fmaf(rq[8 + e] * rsq, sc2, bcomb));
-        for (int k = 0; k < a.iters; ++k) {
-          float rs = cm + __shfl_xor_sync(full, cm, 1);
-          rs = rs + __shfl_xor_sync(full, rs, 2);
-          cm = cm / (rs + a.sink_eps);
-          float cs = cm + __shfl_xor_sync(full, cm, 4);
-          cs = cs + __shfl_xor_sync(full, cs, 8);
-          cm = cm / (cs + a.sink_eps);
-        }
+        const float lc = fmaf(rq[8 + e] * rsq, sc2, bcomb);
         if (grow < a.rows) {
-          a.comb[grow * 16 + e] = cm;
+          a.logit_ws[grow * 16 + e] = lc;
           if (e < 4) a.pre_ws[grow * kHC + e] = gate;
           if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
           if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
@@ -700,6 +700,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
             if (e < 8) a.mix_out[grow * NM + 16 + e] = rq[16 + e] * rsq;
           }
         }
+        (void)full;
       }
       if (warp == kOwnerLead && lane == 0) MHC_TRACE_AT(it, 6);
       (void)gb;
@@ -825,11 +826,11 @@ cudaError_t launch_stats(const uint16_t *R, const StatsArgs &a, int64_t logical_
 
 cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
                              const float *base, int64_t rows, int64_t logical_rows,
-                             const mhc_params &p, float *pre_ws, float *post, float *comb,
+                             const mhc_params &p, float *pre_ws, float *logit_ws, float *post,
                              float *pre_out, float *mix_out, cudaStream_t s) {
   StatsArgs a;
   a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
-  a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out;
+  a.post = post; a.logit_ws = logit_ws; a.pre_out = pre_out; a.mix_out = mix_out;
   a.rows = rows;
   a.num_tiles = (int)((rows + kTile - 1) / kTile);
   a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.sink_eps = p.hc_sinkhorn_eps;
@@ -843,7 +844,7 @@ cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *s
                               float *mix_out, cudaStream_t s) {
   StatsArgs a;
   a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
-  a.post = nullptr; a.comb = nullptr; a.pre_out = pre_out; a.mix_out = mix_out;
+  a.post = nullptr; a.logit_ws = nullptr; a.pre_out = pre_out; a.mix_out = mix_out;
   a.rows = rows;
   a.num_tiles = (int)((rows + kTile - 1) / kTile);
   a.rms_eps = norm_eps; a.pre_eps = hc_eps; a.sink_eps = 0.f; a.post_mult = 0.f; a.iters = 0;

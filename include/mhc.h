@@ -85,9 +85,10 @@ const char *mhc_strerror(int code);
 /* Text of the last CUDA error seen by this thread inside libmhc ("" if none). */
 const char *mhc_last_cuda_error(void);
 
-/* Bytes of device scratch mhc_pre needs for a call on `rows` rows: the pre
- * gates [rows, 4] fp32 handed from its stats launch to its combine launch,
- * rounded up to 256 bytes (0 for rows <= 0). */
+/* Bytes of device scratch mhc_pre needs for a call on `rows` rows: what its
+ * stats launch hands to its combine launch, the pre gates [rows, 4] fp32 and
+ * the comb logits [rows, 16] fp32, each rounded up to 256 bytes (0 for
+ * rows <= 0).  mhc_hc_head takes the same amount and uses the first part. */
 size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
@@ -127,8 +128,9 @@ int mhc_kernel_status_detail(uint32_t *where64);
  * (1) stats (pre_stats.cu): a cluster of 16 CTAs splits each 128-row tile by
  * hidden columns, streams R once with TMA, runs the 24 projections on the
  * tensor cores against fn split into bf16 hi + lo, and finalises the gates
- * and the Sinkhorn per row; (2) combine + RMSNorm (pre_simt.cu,
- * combine_norm_kernel), streaming R again with the gates.  Decode-size
+ * and the comb logits per row; (2) combine + RMSNorm (pre_simt.cu,
+ * combine_norm_kernel), streaming R again with the gates, while a fifth warp
+ * per row runs the Sinkhorn.  Decode-size
  * chunks (logical_rows <= 48) take one latency-shaped launch (pre_decode.cu):
  * 16-CTA clusters of CUDA-core work, up to 8 rows per cluster pass, that
  * leave the workspace untouched.

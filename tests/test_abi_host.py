@@ -62,9 +62,11 @@ def test_strerror_and_defaults(lib):
     assert p.sinkhorn_iters == 20 and p.post_mult == 2.0
     assert abs(p.rms_eps - 1e-6) < 1e-12 and abs(p.norm_eps - 1e-6) < 1e-12
     assert lib.mhc_pre_workspace_bytes(0) == 0
-    assert lib.mhc_pre_workspace_bytes(1000) == 16128   # the pre gates, 256-byte rounded
-    assert lib.mhc_pre_workspace_bytes(1) == 256
-    assert lib.mhc_pre_workspace_bytes(257) == 4352
+    # the pre gates [rows, 4] then the comb logits [rows, 16], fp32, each
+    # 256-byte rounded
+    assert lib.mhc_pre_workspace_bytes(1000) == 16128 + 64000
+    assert lib.mhc_pre_workspace_bytes(1) == 256 + 256
+    assert lib.mhc_pre_workspace_bytes(257) == 4352 + 16640
 
 
 A = 1 << 32          # fake, 256-byte aligned device addresses, far apart
