@@ -420,6 +420,46 @@ def run_op(args):
         nbytes, launches = M * HEAD_BYTES_ROW + HEAD_BYTES_CALL, 2
         metric = "mhc_hc_head rows/s (final stream collapse) and achieved HBM GB/s"
         workload = f"M={M} rows: R[M,4,5120] bf16, hc_head fn[4,20480] f32 (seed {SEED})"
+    elif args.op == "fused_post_pre":
+        # hc_post of one sublayer + hc_pre of the next on its result, fused,
+        # against the same work as mhc_post then mhc_pre (timed the same way)
+        W = synth.weights(SEED)
+        Wn = synth.weights(SEED + 100)
+        t_ = lambda a: torch.from_numpy(a).to(dev)
+        fn, scale, base, w = t_(Wn.fn), t_(Wn.scale), t_(Wn.base), bf(Wn.norm_w)
+        yv = bf(synth.sublayer_out(SEED, M))
+        _, post, comb = m.mhc_pre(R, t_(W.fn), t_(W.scale), t_(W.base), bf(W.norm_w))
+        R2 = torch.empty_like(R)
+        xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        po = torch.empty((M, HC), dtype=torch.float32, device=dev)
+        co = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
+        ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+
+        def step():
+            m.mhc_fused_post_pre(R, yv, post, comb, fn, scale, base, w, logical_rows=M,
+                                 workspace=ws, R_out=R2, x_norm=xn, post_out=po, comb_out=co,
+                                 stream=stream)
+
+        def unfused():
+            m.mhc_post(R, yv, post, comb, logical_rows=M, out=R2, stream=stream)
+            m.mhc_pre(R2, fn, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
+                      post=po, comb=co, stream=stream)
+        for _ in range(args.warmup):
+            unfused()
+        torch.cuda.synchronize(dev)
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(args.steps):
+            unfused()
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        unfused_ms = a_.elapsed_time(b_) / args.steps
+        # minimal traffic of the pair: read R, y, post, comb; write R', x_norm,
+        # post', comb' (the fused launch reads R' once more, for the combine)
+        nbytes, launches = M * (2 * (K * 2 + H * 2 + HC * 4 + HC * HC * 4)) + PRE_BYTES_CALL, 2
+        metric = "mhc_fused_post_pre rows/s (hc_post + next hc_pre) and achieved HBM GB/s"
+        workload = (f"M={M} rows: R[M,4,5120], y[M,5120] bf16, next fn[24,20480] f32 "
+                    f"(seed {SEED}); unfused mhc_post+mhc_pre: {unfused_ms:.4f} ms/step")
     elif args.op == "latency":
         # decode-size rows: one step = mhc_pre + mhc_post; latency per step,
         # launched eagerly and replayed from a CUDA graph
@@ -522,7 +562,8 @@ def main():
     ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["step", "hc_head", "latency"], default="step",
+    ap.add_argument("--op", choices=["step", "hc_head", "latency", "fused_post_pre"],
+                    default="step",
                     help="step: mhc_pre + mhc_post (the headline); others time one entry "
                          "point alone")
     ap.add_argument("--logical-rows", type=int, default=0,

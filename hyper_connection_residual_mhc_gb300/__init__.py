@@ -60,6 +60,9 @@ SIGNATURES = {
     "mhc_pre_noalloc_max_rows": (ctypes.c_int64, []),
     "mhc_post": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp]),
     "mhc_combine_norm": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp]),
+    "mhc_fused_post_pre": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                          ctypes.POINTER(MhcParams), _vp, ctypes.c_size_t, _vp,
+                                          _vp, _vp, _vp, _vp, _vp, _vp]),
     "mhc_hc_head": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
                                    ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
 }
@@ -278,3 +281,46 @@ def mhc_hc_head(R, fn, scale, base, *, norm_eps=1e-6, hc_eps=1e-6, logical_rows=
         _ptr(workspace), ws_bytes, _ptr(out), _ptr(pre_out), _ptr(mix_out), _stream(stream))
     _check("mhc_hc_head", code)
     return out
+
+
+def mhc_fused_post_pre(R, y, post, comb, fn, scale, base, norm_w, *, logical_rows=None,
+                       params=None, workspace=None, R_out=None, x_norm=None, post_out=None,
+                       comb_out=None, pre_out=None, mix_out=None, stream=None):
+    """hc_post then the next hc_pre on its result (see mhc_fused_post_pre in
+    include/mhc.h).  Returns ``(R_out, x_norm, post_out, comb_out)``."""
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(y, "y", torch.bfloat16, (rows, H))
+    _need(post, "post", torch.float32, (rows, HC))
+    _need(comb, "comb", torch.float32, (rows, HC, HC))
+    _need(fn, "fn", torch.float32, (MIX, K))
+    _need(scale, "scale", torch.float32, (3,))
+    _need(base, "base", torch.float32, (MIX,))
+    _need(norm_w, "norm_w", torch.bfloat16, (H,))
+    dev = R.device
+    R_out = torch.empty_like(R) if R_out is None else R_out
+    x_norm = torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if x_norm is None else x_norm
+    post_out = torch.empty((rows, HC), dtype=torch.float32, device=dev) if post_out is None else post_out
+    comb_out = (torch.empty((rows, HC, HC), dtype=torch.float32, device=dev)
+                if comb_out is None else comb_out)
+    _need(R_out, "R_out", torch.bfloat16, (rows, HC, H))
+    _need(x_norm, "x_norm", torch.bfloat16, (rows, H))
+    _need(post_out, "post_out", torch.float32, (rows, HC))
+    _need(comb_out, "comb_out", torch.float32, (rows, HC, HC))
+    if pre_out is not None:
+        _need(pre_out, "pre_out", torch.float32, (rows, HC))
+    if mix_out is not None:
+        _need(mix_out, "mix_out", torch.float32, (rows, MIX))
+    need = mhc_pre_workspace_bytes(rows)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    p = default_params() if params is None else params
+    code = lib().mhc_fused_post_pre(
+        _ptr(R), _ptr(y), _ptr(post), _ptr(comb), _ptr(fn), _ptr(scale), _ptr(base),
+        _ptr(norm_w), rows, rows if logical_rows is None else int(logical_rows), ctypes.byref(p),
+        _ptr(workspace), ws_bytes, _ptr(R_out), _ptr(x_norm), _ptr(post_out), _ptr(comb_out),
+        _ptr(pre_out), _ptr(mix_out), _stream(stream))
+    _check("mhc_fused_post_pre", code)
+    return R_out, x_norm, post_out, comb_out

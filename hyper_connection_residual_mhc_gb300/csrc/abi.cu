@@ -112,10 +112,11 @@ int mhc_kernel_status_detail(uint32_t *where64) {
 
 int mhc_kernel_status(uint32_t *status, int reset) {
   if (!status) return MHC_ERR_NULL;
-  unsigned int w = 0;
+  unsigned int w = 0, w2 = 0;
   cudaError_t e = mhc::fused_error_word(&w, reset != 0);
+  if (e == cudaSuccess) e = mhc::fused_post_pre_error_word(&w2, reset != 0);
   if (e != cudaSuccess) return cuda_fail(e);
-  *status = w;
+  *status = w | w2;
   return MHC_OK;
 }
 
@@ -263,6 +264,71 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
   if (int e = check_device()) return e;
   cudaError_t ce = mhc::launch_combine_norm(R, pre, norm_w, norm_eps, rows, logical_rows,
                                             x_norm, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+
+int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
+                       const float *comb, const float *fn, const float *scale, const float *base,
+                       const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+                       const mhc_params *p_in, void *workspace, size_t workspace_bytes,
+                       uint16_t *R_out, uint16_t *x_norm, float *post_out, float *comb_out,
+                       float *pre_out, float *mix_out, void *stream) {
+  mhc_params p;
+  if (p_in) p = *p_in; else mhc_default_params(&p);
+  if (int e = check_rows(rows, logical_rows)) return e;
+  if (!finite_nonneg(p.rms_eps) || !finite_nonneg(p.hc_pre_eps) ||
+      !finite_nonneg(p.hc_sinkhorn_eps) || !finite_nonneg(p.norm_eps) ||
+      !std::isfinite(p.post_mult) || p.sinkhorn_iters < 1 || p.sinkhorn_iters > 100000)
+    return MHC_ERR_PARAM;
+  if (rows == 0) return MHC_OK;
+  if (!R || !y || !post || !comb || !fn || !scale || !base || !norm_w || !R_out || !x_norm ||
+      !post_out || !comb_out)
+    return MHC_ERR_NULL;
+  const void *al[] = {R, y, post, comb, fn, scale, base, norm_w, R_out, x_norm, post_out, comb_out};
+  for (const void *q : al)
+    if (!aligned16(q)) return MHC_ERR_ALIGN;
+  if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
+  const size_t need = mhc_pre_workspace_bytes(rows);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MHC_ERR_WORKSPACE;
+  const size_t nr = (size_t)rows;
+  const Span ins[] = {span(R, nr * MHC_K * 2), span(y, nr * MHC_HIDDEN * 2),
+                      span(post, nr * MHC_HC * 4), span(comb, nr * MHC_HC * MHC_HC * 4),
+                      span(fn, (size_t)MHC_MIX * MHC_K * 4), span(scale, 12),
+                      span(base, MHC_MIX * 4), span(norm_w, MHC_HIDDEN * 2)};
+  Span outs[7];
+  int n_out = 0;
+  outs[n_out++] = span(R_out, nr * MHC_K * 2);
+  outs[n_out++] = span(x_norm, nr * MHC_HIDDEN * 2);
+  outs[n_out++] = span(post_out, nr * MHC_HC * 4);
+  outs[n_out++] = span(comb_out, nr * MHC_HC * MHC_HC * 4);
+  outs[n_out++] = span(workspace, need);
+  if (pre_out) outs[n_out++] = span(pre_out, nr * MHC_HC * 4);
+  if (mix_out) outs[n_out++] = span(mix_out, nr * MHC_MIX * 4);
+  for (int a = 0; a < n_out; ++a) {
+    for (const Span &b : ins)
+      if (overlap(outs[a], b)) return MHC_ERR_OVERLAP;
+    for (int b = a + 1; b < n_out; ++b)
+      if (overlap(outs[a], outs[b])) return MHC_ERR_OVERLAP;
+  }
+  if (int e = check_device()) return e;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t ce;
+  if (logical_rows <= mhc::kDecodeMaxRows) {
+    // decode-size chunk: hc_post, then the one-launch decode pre on R'
+    ce = mhc::launch_post(R, y, post, comb, rows, logical_rows, R_out, s);
+    if (ce == cudaSuccess)
+      ce = mhc::launch_pre_decode(R_out, fn, scale, base, norm_w, rows, logical_rows, p, x_norm,
+                                  post_out, comb_out, pre_out, mix_out, s);
+  } else {
+    float *pre_ws = static_cast<float *>(workspace);
+    float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
+    ce = mhc::launch_post_pre_fused(R, y, post, comb, fn, scale, base, rows, logical_rows, p,
+                                    pre_ws, logit_ws, R_out, post_out, pre_out, mix_out, s);
+    if (ce == cudaSuccess)
+      ce = mhc::launch_combine_norm_sinkhorn(R_out, pre_ws, norm_w, p.norm_eps, logit_ws, comb_out,
+                                             p.hc_sinkhorn_eps, p.sinkhorn_iters, rows, x_norm, s);
+  }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 

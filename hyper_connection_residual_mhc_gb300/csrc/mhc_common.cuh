@@ -43,6 +43,30 @@ __device__ __forceinline__ uint4 pack8_rn(const float (&f)[8]) {
   return v;
 }
 
+// hc_post on one 8-column chunk of a row (deepseek_v4.py, hc_post_torch_impl):
+// out_i = bf16( post_i * y + sum_j comb[j][i] * R_j ), fp32 arithmetic in a
+// fixed order, one rounding.  cb[j][i] = comb[j][i].
+__device__ __forceinline__ void post_chunk(const uint4 (&rv)[kHC], const uint4 &yv,
+                                           const float (&pv)[kHC], const float (&cb)[kHC][kHC],
+                                           uint4 (&out)[kHC]) {
+  float yf[8], rf[kHC][8];
+  unpack8(yv, yf);
+#pragma unroll
+  for (int j = 0; j < kHC; ++j) unpack8(rv[j], rf[j]);
+#pragma unroll
+  for (int i = 0; i < kHC; ++i) {
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float a = pv[i] * yf[e];
+#pragma unroll
+      for (int j = 0; j < kHC; ++j) a = fmaf(cb[j][i], rf[j][e], a);
+      acc[e] = a;
+    }
+    out[i] = pack8_rn(acc);
+  }
+}
+
 // Streaming (evict-first) 16-byte global accesses for data touched once.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
@@ -98,6 +122,16 @@ cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *s
 // y = bf16(sum_i pre_i R_i), one block per row (hc_head's combine)
 cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows, uint16_t *y,
                                 cudaStream_t s);
+// hc_post fused with the next pre's stats (post_pre_fused.cu): writes R_out,
+// the next pre's gates to pre_ws [rows, 4], its comb logits to logit_ws
+// [rows, 16] and its post gates (+ pre_out, mix_out)
+cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const float *post,
+                                  const float *comb, const float *fn, const float *scale,
+                                  const float *base, int64_t rows, int64_t logical_rows,
+                                  const mhc_params &p, float *pre_ws, float *logit_ws,
+                                  uint16_t *R_out, float *post_out, float *pre_out,
+                                  float *mix_out, cudaStream_t s);
+cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset);
 // the stats kernel's error word (nonzero once a bounded wait expired)
 cudaError_t fused_error_word(unsigned int *out, bool reset);
 cudaError_t fused_error_where(unsigned int *out32);

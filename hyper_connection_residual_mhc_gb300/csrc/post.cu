@@ -39,24 +39,11 @@ post_kernel(const uint4 *__restrict__ R, const uint4 *__restrict__ y,
   }
   const float pv[kHC] = {pw.x, pw.y, pw.z, pw.w};
 
-  float yf[8], rf[kHC][8];
-  unpack8(yv, yf);
-#pragma unroll
-  for (int j = 0; j < kHC; ++j) unpack8(rv[j], rf[j]);
-
+  uint4 ov[kHC];
+  post_chunk(rv, yv, pv, cb, ov);
   uint4 *o = out + row * (kHC * kChunksPerStream) + c;
 #pragma unroll
-  for (int i = 0; i < kHC; ++i) {
-    float acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float a = pv[i] * yf[e];
-#pragma unroll
-      for (int j = 0; j < kHC; ++j) a = fmaf(cb[j][i], rf[j][e], a);
-      acc[e] = a;
-    }
-    st_stream(o + i * kChunksPerStream, pack8_rn(acc));
-  }
+  for (int i = 0; i < kHC; ++i) st_stream(o + i * kChunksPerStream, ov[i]);
 }
 
 }  // namespace

@@ -1,0 +1,509 @@
+// post_pre_fused.cu -- hc_post of one sublayer fused with the stats half of
+// the next sublayer's hc_pre, on GB300.
+//
+// Definitions: deepseek_v4.py (sglang), DeepseekV4DecoderLayer.hc_post
+// (hc_post_torch_impl: R'_i = post_i * y + sum_j comb[j][i] * R_j, one bf16
+// rounding) followed by DeepseekV4DecoderLayer.hc_pre on R' (rsqrt of
+// mean(x^2) + rms_eps, mixes = (x @ fn^T) * rsqrt, hc_split_sinkhorn); the
+// pages run the pair as one call (mhc_fused_post_pre) between sublayers.
+//
+// Unfused, R' is written by hc_post and read back by the stats; here the
+// stats consume R' straight from the registers that computed it, so R' costs
+// one write and no read.  The decomposition follows the stats kernel
+// (pre_stats.cu): a cluster of 16 CTAs owns a 128-row tile at a time, CTA s
+// owns hidden columns [320 s, 320 s + 320) of all four streams, and its fn
+// slice (bf16 hi + lo, 120 KB) stays in shared memory.  The TMA producer and
+// the row warps are replaced by eight converter warps:
+//   * per 64-column block of the CTA's columns (a "set": the 4 streams'
+//     16 KB stages), each converter thread loads R_0..3 and y for four
+//     (row, 8-column) items, forms R' (the same arithmetic as mhc_post, so
+//     R' has mhc_post's bits), writes it to HBM, writes it into the set's
+//     128-byte-swizzled stages for the tensor core, and adds its squares to
+//     the row's sum of squares;
+//   * one thread issues tcgen05.mma (M=128 rows, N=48, K=16) per stage;
+//   * four readout warps load the accumulator, push each row's 24 partials
+//     and sum of squares to the row's owner CTA, then, as owners, reduce the
+//     16 CTAs' partials in CTA order and write the gates and comb logits.
+// The combine + RMSNorm and the Sinkhorn of the next pre then run as the
+// pre pass's streaming launch (pre_simt.cu) on R'.
+//
+// Every wait is bounded (~2 s); on expiry a CTA raises an abort flag, records
+// the site in this kernel's error word, drains its MMAs, frees its tensor
+// memory and returns.
+#include "mhc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace mhc {
+
+__device__ unsigned int g_fpp_error;
+__device__ unsigned int g_fpp_where[32];
+__device__ unsigned int g_fpp_where_aborted[32];
+
+namespace {
+using namespace ptx;
+
+constexpr int kCl = 16;                       // CTAs per cluster (K split)
+constexpr int kTile = 128;                    // rows per tile = UMMA M
+constexpr int kHs = kH / kCl;                 // 320 columns per CTA
+constexpr int kBk = 64;                       // columns per stage
+constexpr int kHb = kHs / kBk;                // 5 sets per tile
+constexpr int kKb = kHC * kHb;                // 20 fn k-blocks
+constexpr int kN = 2 * kMix;                  // fn hi (24) + lo (24)
+constexpr int kStageBytes = kTile * kBk * 2;  // 16384
+constexpr int kFnBlkBytes = kN * kBk * 2;     // 6144
+constexpr int kRw = 28;                       // receive words per row
+constexpr int kOwn = kTile / kCl;             // 8 rows finalised per CTA
+constexpr int kTmemCols = 128;
+constexpr int kPc = kHC + kHC * kHC;          // post + comb floats per row
+
+// warps: 0 MMA; 1..8 converters; 9..12 readout, then owners
+constexpr int kMmaWarp = 0;
+constexpr int kConv0 = 1, kConvN = 8;
+constexpr int kRead0 = 9, kReadN = 4;
+constexpr int kWarps = 13;
+constexpr int kThreads = kWarps * 32;         // 416
+constexpr int kItems = 4;                     // (row, chunk) items per converter thread per set
+// 13 warps put 4 on one SM sub-partition, whose 16K registers then allow at
+// most 128 a thread: the launch bound keeps the kernel within it
+static_assert(kWarps <= 16, "");
+
+static_assert(kConvN * 32 * kItems == kTile * (kBk / 8), "one item per (row, 8 columns)");
+
+// shared memory (from a 1024-byte aligned base)
+constexpr int kOffFn = 0;
+constexpr int kOffSet = kOffFn + kKb * kFnBlkBytes;           // 4 stages, one per stream
+constexpr int kOffPc = kOffSet + kHC * kStageBytes;           // [8 warps][16 rows][20] post, comb
+constexpr int kOffRecv = kOffPc + kTile * kPc * 4;            // [16 src][8 rows][kRw]
+constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;      // [8 rows][kRw]
+constexpr int kOffSs = kOffRed + kOwn * kRw * 4;              // [2][128] sum x^2
+constexpr int kOffBar = kOffSs + 2 * kTile * 4;
+enum Bar : int {
+  B_SFULL = 0,                   // the set's 4 stages written (8 converter warps)
+  B_SEMPTY = B_SFULL + 1,        // the set consumed by the MMAs (commit)
+  B_TFULL = B_SEMPTY + 1,        // [2] accumulator complete
+  B_TEMPTY = B_TFULL + 2,        // [2] accumulator and sum x^2 read out
+  B_SSREADY = B_TEMPTY + 2,      // [2] the converters wrote a tile's sum x^2
+  B_PREADY = B_SSREADY + 2,      // all 16 CTAs pushed partials to us (remote)
+  B_PFREE = B_PREADY + 1,        // all 16 owners pulled our previous push (remote)
+  B_GALL = B_PFREE + 1,          // the readout warps pushed
+  B_OPULL = B_GALL + 1,          // the owner warps read the receive buffer
+  B_DRAIN = B_OPULL + 1,         // final MMA drain
+  B_COUNT = B_DRAIN + 1
+};
+static_assert(B_COUNT == 1 + 1 + 2 + 2 + 2 + 5, "barrier slots overlap");
+constexpr int kOffMisc = kOffBar + B_COUNT * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
+static_assert(kOffSet % 1024 == 0 && kStageBytes % 1024 == 0 && kFnBlkBytes % 1024 == 0, "");
+static_assert(kOffRecv % 16 == 0 && kOffPc % 16 == 0, "");
+
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) |
+                            ((uint32_t)(kTile >> 4) << 24);
+
+struct FusedArgs {
+  const uint4 *R;          // [rows, 4, 640] 16-byte chunks
+  const uint4 *y;          // [rows, 640]
+  const float *post_in;    // [rows, 4]
+  const float *comb_in;    // [rows, 4, 4]
+  uint4 *R_out;            // [rows, 4, 640]
+  const float *fn;
+  const float *scale;
+  const float *base;
+  float *pre_ws;           // [rows, 4] pre gates of R'
+  float *logit_ws;         // [rows, 16] comb logits of R'
+  float *post_out;         // [rows, 4]
+  float *pre_out;
+  float *mix_out;
+  int64_t rows;
+  int num_tiles;
+  float rms_eps, pre_eps, post_mult;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) post_pre_fused_kernel(const FusedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_addr(sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();
+  const int cid = (int)cluster_id(), ncl = (int)cluster_count();
+  const int T = cid < a.num_tiles ? (a.num_tiles - 1 - cid) / ncl + 1 : 0;
+  auto bar = [&](int i) -> uint32_t { return sb + kOffBar + 8u * (uint32_t)i; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+  Abort ab{reinterpret_cast<volatile int *>(sm + kOffMisc + 4), crank, &g_fpp_error, g_fpp_where,
+           g_fpp_where_aborted};
+
+  // ---- set-up ---------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    *ab.flag = 0;
+    mbar_init(bar(B_SFULL), kConvN);
+    mbar_init(bar(B_SEMPTY), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_TFULL + b), 1);
+      mbar_init(bar(B_TEMPTY + b), kReadN);
+      mbar_init(bar(B_SSREADY + b), kConvN);
+    }
+    mbar_init(bar(B_PREADY), kCl);
+    mbar_init(bar(B_PFREE), kCl);
+    mbar_init(bar(B_GALL), kReadN);
+    mbar_init(bar(B_OPULL), kReadN);
+    mbar_init(bar(B_DRAIN), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  // fn columns of this CTA -> bf16 hi/lo B tiles (K-major, 128-byte swizzle),
+  // by all warps: k-block j covers k = (j%4)*5120 + 320*crank + 64*(j/4) + [0, 64)
+  {
+    constexpr int kFnItems = kMix * kKb * 8;   // items of 8 consecutive k
+    for (int item = threadIdx.x; item < kFnItems; item += kThreads) {
+      const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
+      const int k0 = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk + 8 * q;
+      const float4 f0 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0));
+      const float4 f1 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0 + 4));
+      const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * e]);
+        const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * e + 1]);
+        hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
+        lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
+      }
+      uint8_t *tile = sm + kOffFn + j * kFnBlkBytes;
+      const int nh = c, nlo = c + kMix;
+      *reinterpret_cast<uint4 *>(tile + (nh >> 3) * 1024 + (nh & 7) * 128 + ((q ^ (nh & 7)) << 4)) =
+          make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4 *>(tile + (nlo >> 3) * 1024 + (nlo & 7) * 128 +
+                                 ((q ^ (nlo & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    // generic-proxy writes -> visible to the tensor core (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync_all();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- roles -------------------------------------------------------------------
+  if (warp == kMmaWarp) {
+    // whole warp walks the loops (warp-collective waits); lane 0 issues
+    uint32_t g = 0;                              // set counter
+    bool ok = true;
+    for (int it = 0; it < T && ok; ++it) {
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!waitw(bar(B_TEMPTY + buf), (use & 1) ^ 1, false, ab, 2, it)) break;
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(buf * 64);
+      for (int hb = 0; hb < kHb; ++hb, ++g) {
+        if (!waitw(bar(B_SFULL), g & 1, false, ab, 3, it)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll 1
+          for (int i = 0; i < kHC; ++i) {
+            const int j = i + kHC * hb;
+            const uint64_t ad = sw128_desc(sb + kOffSet + i * kStageBytes);
+            const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBk / 16; ++kk)
+              tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (hb | i | kk) != 0);
+          }
+          tc_commit(bar(B_SEMPTY));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(bar(B_TFULL + buf));
+      __syncwarp();
+    }
+    // all issued MMAs complete before TMEM is freed
+    if (lane == 0) tc_commit(bar(B_DRAIN));
+    __syncwarp();
+    drain1(bar(B_DRAIN), 0);
+    __syncwarp();
+  } else if (warp >= kConv0 && warp < kConv0 + kConvN) {
+    // ---- converters: R' = post(R, y), to HBM and to the tensor core ---------
+    const int cw = warp - kConv0, rsub = lane >> 3, q = lane & 7;
+    // this warp's 16 rows' post and comb (warp-private: only __syncwarp
+    // orders it, so no warp ever waits at a barrier another may have left)
+    float *pcw = reinterpret_cast<float *>(sm + kOffPc) + cw * 16 * kPc;
+    float *ssbuf = reinterpret_cast<float *>(sm + kOffSs);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int it = 0; it < T && ok; ++it) {
+      const int64_t row0 = (int64_t)(cid + it * ncl) * kTile;
+      __syncwarp();                             // the previous tile's reads are done
+      for (int t = lane; t < 16 * kPc; t += 32) {
+        const int rl = t / kPc, c = t % kPc;
+        const int64_t gr = row0 + cw * 16 + rl;
+        float v = 0.f;
+        if (gr < a.rows) v = c < kHC ? __ldg(a.post_in + gr * kHC + c) : __ldg(a.comb_in + gr * 16 + (c - kHC));
+        pcw[t] = v;
+      }
+      __syncwarp();
+      float ssq[kItems];
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) ssq[k] = 0.f;
+      for (int hb = 0; hb < kHb; ++hb, ++g) {
+        const int h8 = (int)crank * (kHs / 8) + hb * (kBk / 8) + q;   // 16-byte column index
+        uint4 rv[kItems][kHC], yv[kItems];
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+          const int r = cw * 16 + 4 * k + rsub;
+          const int64_t gr = row0 + r;
+          if (gr < a.rows) {
+#pragma unroll
+            for (int i = 0; i < kHC; ++i) rv[k][i] = ld_stream(a.R + (gr * kHC + i) * kChunksPerStream + h8);
+            yv[k] = ld_stream(a.y + gr * kChunksPerStream + h8);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kHC; ++i) rv[k][i] = make_uint4(0u, 0u, 0u, 0u);
+            yv[k] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        // the set's stages are free once the previous set's MMAs completed
+        if (!waitw(bar(B_SEMPTY), (g & 1) ^ 1, false, ab, 1, it)) { ok = false; break; }
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+          const int r = cw * 16 + 4 * k + rsub;
+          const int64_t gr = row0 + r;
+          const float *pr = pcw + (4 * k + rsub) * kPc;
+          const float pv[kHC] = {pr[0], pr[1], pr[2], pr[3]};
+          float cb[kHC][kHC];
+#pragma unroll
+          for (int j = 0; j < kHC; ++j)
+#pragma unroll
+            for (int i = 0; i < kHC; ++i) cb[j][i] = pr[kHC + 4 * j + i];
+          uint4 ov[kHC];
+          post_chunk(rv[k], yv[k], pv, cb, ov);
+          float si[kHC];                        // per stream: 8 squares
+#pragma unroll
+          for (int i = 0; i < kHC; ++i) {
+            *reinterpret_cast<uint4 *>(sm + kOffSet + i * kStageBytes + r * 128 + ((q ^ (r & 7)) << 4)) = ov[i];
+            float of[8];
+            unpack8(ov[i], of);
+            si[i] = of[0] * of[0];
+#pragma unroll
+            for (int e = 1; e < 8; ++e) si[i] = fmaf(of[e], of[e], si[i]);
+            if (gr < a.rows) st_stream(a.R_out + (gr * kHC + i) * kChunksPerStream + h8, ov[i]);
+          }
+          // short chains: 8 squares, a pairwise sum of the 4 streams, 5 sets
+          ssq[k] += (si[0] + si[1]) + (si[2] + si[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SFULL));
+      }
+      if (!ok) break;
+      // the rows' sums of squares: the 8 lanes of a row (q = 0..7), fixed tree
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        ssq[k] += __shfl_xor_sync(0xffffffffu, ssq[k], 1);
+        ssq[k] += __shfl_xor_sync(0xffffffffu, ssq[k], 2);
+        ssq[k] += __shfl_xor_sync(0xffffffffu, ssq[k], 4);
+      }
+      const int buf = it & 1;
+      if (!waitw(bar(B_TEMPTY + buf), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 10, it)) break;
+      if (q == 0) {
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) ssbuf[buf * kTile + cw * 16 + 4 * k + rsub] = ssq[k];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SSREADY + buf));
+    }
+  } else {
+    // ---- readout (one thread per tile row), then owners of 8 rows ------------
+    const int quarter = warp & 3;               // a warp reads TMEM lanes 32*(warp%4) .. +31
+    const int row = 32 * quarter + lane;
+    const float *ssbuf = reinterpret_cast<const float *>(sm + kOffSs);
+    const int o = (warp - kRead0) * 32 + lane; // owner thread 0..127
+    const int oq = o >> 4, e = o & 15;          // owned row (of 8), lane of 16
+    const int row_t = (int)crank * kOwn + oq;
+    const float *recv = reinterpret_cast<const float *>(sm + kOffRecv);
+    float *red = reinterpret_cast<float *>(sm + kOffRed);
+    const float sc0 = __ldg(a.scale), sc1 = __ldg(a.scale + 1), sc2 = __ldg(a.scale + 2);
+    const float bcomb = __ldg(a.base + 8 + e);
+    const float bgate = e < 8 ? __ldg(a.base + e) : 0.f;
+    for (int t = 0; t < T; ++t) {
+      const int buf = t & 1;
+      const uint32_t use = (uint32_t)(t >> 1);
+      if (!waitw(bar(B_TFULL + buf), use & 1, false, ab, 5, t)) break;
+      if (!waitw(bar(B_SSREADY + buf), use & 1, false, ab, 11, t)) break;
+      tc_fence_after();
+      const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * 64);
+      float a0[16], a1[16], a2[16];             // columns 0..47: hi 0..23, lo 24..47
+      tc_ld16(ta + 0, a0);
+      tc_ld16(ta + 16, a1);
+      tc_ld16(ta + 32, a2);
+      tc_wait_ld();
+      const float ss = ssbuf[buf * kTile + row];
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_TEMPTY + buf));
+      float mix[kMix];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mix[c] = a0[c] + a1[c + 8];
+#pragma unroll
+      for (int c = 8; c < 16; ++c) mix[c] = a0[c] + a2[c - 8];
+#pragma unroll
+      for (int c = 16; c < 24; ++c) mix[c] = a1[c - 16] + a2[c - 8];
+      if (!waitw(bar(B_PFREE), (uint32_t)(t & 1) ^ 1, true, ab, 6, t)) break;
+      const uint32_t dm = mapa(sb + kOffRecv + (uint32_t)(((crank * kOwn + (row & 7)) * kRw) * 4),
+                               (uint32_t)(row >> 3));
+#pragma unroll
+      for (int v = 0; v < 6; ++v)
+        st_cluster_v4(dm + 16 * v, mix[4 * v], mix[4 * v + 1], mix[4 * v + 2], mix[4 * v + 3]);
+      st_cluster_f32(dm + 4 * kMix, ss);
+      fence_cluster();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_GALL));
+      if (warp == kRead0) {
+        if (!waitw(bar(B_GALL), (uint32_t)(t & 1), false, ab, 7, t)) break;
+        if (lane == 0) arrive_all_ctas(bar(B_PREADY), kCl);
+        __syncwarp();
+      }
+      // ---- as owners: the 16 CTAs' partials of row oq, in CTA order ----------
+      const int64_t grow = (int64_t)(cid + t * ncl) * kTile + row_t;
+      if (!waitw(bar(B_PREADY), (uint32_t)(t & 1), true, ab, 8, t)) break;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int src = 0; src < kCl; ++src) acc0 += recv[(src * kOwn + oq) * kRw + e];
+      if (e + 16 <= kMix) {
+#pragma unroll
+        for (int src = 0; src < kCl; ++src) acc1 += recv[(src * kOwn + oq) * kRw + e + 16];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_OPULL));
+      if (warp == kRead0) {
+        if (!waitw(bar(B_OPULL), (uint32_t)(t & 1), false, ab, 9, t)) break;
+        if (lane == 0) arrive_all_ctas(bar(B_PFREE), kCl);
+        __syncwarp();
+      }
+      float *rq = red + oq * kRw;
+      rq[e] = acc0;
+      if (e + 16 <= kMix) rq[e + 16] = acc1;
+      __syncwarp();
+      const float rsq = 1.0f / sqrtf(rq[kMix] / (float)kK + a.rms_eps);
+      float gate = 0.f;
+      if (e < 8) {
+        const float l = fmaf(rq[e] * rsq, e < 4 ? sc0 : sc1, bgate);
+        const float sg = 1.0f / (1.0f + expf(-l));
+        gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
+      }
+      const float lc = fmaf(rq[8 + e] * rsq, sc2, bcomb);
+      if (grow < a.rows) {
+        a.logit_ws[grow * 16 + e] = lc;
+        if (e < 4) a.pre_ws[grow * kHC + e] = gate;
+        if (e >= 4 && e < 8) a.post_out[grow * kHC + (e - 4)] = gate;
+        if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
+        if (a.mix_out) {
+          a.mix_out[grow * kMix + e] = rq[e] * rsq;
+          if (e < 8) a.mix_out[grow * kMix + 16 + e] = rq[16 + e] * rsq;
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  // ---- teardown: no CTA leaves while its shared memory may still be addressed
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  __syncwarp();
+  cluster_sync_all();
+}
+
+std::mutex g_fpp_mu;
+int g_fpp_clusters[64];   // per device: co-resident clusters (0: not configured)
+
+cudaError_t fpp_configure(int dev, int *max_clusters) {
+  std::lock_guard<std::mutex> lock(g_fpp_mu);
+  if (g_fpp_clusters[dev] > 0) {
+    *max_clusters = g_fpp_clusters[dev];
+    return cudaSuccess;
+  }
+  cudaError_t e = cudaFuncSetAttribute(post_pre_fused_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(post_pre_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  cfg.gridDim = dim3(kCl);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, post_pre_fused_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  g_fpp_clusters[dev] = n;
+  *max_clusters = n;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const float *post,
+                                  const float *comb, const float *fn, const float *scale,
+                                  const float *base, int64_t rows, int64_t logical_rows,
+                                  const mhc_params &p, float *pre_ws, float *logit_ws,
+                                  uint16_t *R_out, float *post_out, float *pre_out,
+                                  float *mix_out, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int max_clusters = 0;
+  e = fpp_configure(dev, &max_clusters);
+  if (e != cudaSuccess) return e;
+  FusedArgs a;
+  a.R = reinterpret_cast<const uint4 *>(R);
+  a.y = reinterpret_cast<const uint4 *>(y);
+  a.post_in = post;
+  a.comb_in = comb;
+  a.R_out = reinterpret_cast<uint4 *>(R_out);
+  a.fn = fn; a.scale = scale; a.base = base;
+  a.pre_ws = pre_ws; a.logit_ws = logit_ws; a.post_out = post_out;
+  a.pre_out = pre_out; a.mix_out = mix_out;
+  a.rows = rows;
+  a.num_tiles = (int)((rows + kTile - 1) / kTile);
+  a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.post_mult = p.post_mult;
+  // grid from the chunk's row count only (per-row arithmetic never depends on it)
+  const int64_t chunk_tiles = (logical_rows + kTile - 1) / kTile;
+  const int clusters = (int)(chunk_tiles < max_clusters ? chunk_tiles : max_clusters);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  cfg.gridDim = dim3((unsigned)(clusters * kCl));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, post_pre_fused_kernel, a);
+}
+
+cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_fpp_error, sizeof(unsigned int));
+  if (e == cudaSuccess && reset) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_fpp_error, &z, sizeof z);
+  }
+  return e;
+}
+
+}  // namespace mhc

@@ -22,7 +22,8 @@
 //   * one thread of warp 1 issues tcgen05.mma (M=128 rows, N = 48 or 16,
 //     K=16, bf16 -> fp32) into one of two accumulators in tensor memory;
 //   * row warps 4..7 (one thread per tile row) accumulate sum x^2 from the
-//     same stages (one accumulator per 16-byte chunk, summed in a fixed tree);
+//     same stages (per 16-byte chunk an 8-square chain added to one of eight
+//     accumulators, summed in a fixed tree);
 //   * readout warps 8..11 load the accumulator (tcgen05.ld) and push each
 //     row's NM mix partials and its sum of squares into the receive buffer of
 //     the CTA that finalises the row (CTA s owns tile rows 8s..8s+7), then
@@ -47,6 +48,7 @@
 #include <mutex>
 
 #include "mhc_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace mhc {
 
@@ -73,6 +75,7 @@ __device__ unsigned long long *g_trace;
 #endif
 
 namespace {
+using namespace ptx;
 
 // ---- geometry -------------------------------------------------------------
 constexpr int kCl = 16;                       // CTAs per cluster (K split)
@@ -148,191 +151,6 @@ struct Cfg {
   static_assert(NM % 4 == 0 && (2 * NM) % 8 == 0, "pushes of 4 mixes; padding starts on an 8-row group");
 };
 
-constexpr uint64_t kTimeoutNs = 2000000000ull;
-
-// ---- PTX wrappers -----------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t cta) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(cta));
-  return r;
-}
-__device__ __forceinline__ void mbar_init(uint32_t b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(n) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
-}
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-// Arrive on the barrier at the same offset in every CTA of the cluster: one
-// cluster-scope fence orders this thread's earlier writes (and those it has
-// observed) before the arrivals, which are then relaxed.  (A release arrive
-// per CTA would fence 16 times.)
-__device__ __forceinline__ void arrive_all_ctas(uint32_t b, uint32_t n_cta) {
-  fence_cluster();
-  for (uint32_t dst = 0; dst < n_cta; ++dst)
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa(b, dst))
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
-  return ok != 0;
-}
-// acquire at cluster scope: for barriers completed by other CTAs' arrivals
-__device__ __forceinline__ bool mbar_test_cluster(uint32_t b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(b), "r"(parity) : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// tcgen05 (5th-generation tensor core, accumulator in tensor memory)
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-               "r"(cols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 B apart (SBO), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;                 // LBO (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;       // SBO
-  d |= (uint64_t)1 << 46;                 // version
-  d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
-  return d;
-}
-
-// ---- bounded waits ------------------------------------------------------------
-struct Abort {
-  volatile int *flag;
-  uint32_t rank;
-  // a wait at `site` expired on tile `it`: stop the CTA, record where
-  __device__ bool raise(int site, int it) const {
-    *flag = 1;
-    atomicOr(&g_fused_error, 1u << site);
-    g_fused_where[site] = ((uint32_t)it << 8) | rank;
-    return false;
-  }
-  // a wait at `site` gave up because the CTA aborted elsewhere
-  __device__ bool follow(int site, int it) const {
-    atomicOr(&g_fused_error, 1u << (16 + site));
-    g_fused_where_aborted[site] = ((uint32_t)it << 8) | rank;
-    return false;
-  }
-};
-
-// whole warp; the outcome is warp-uniform
-__device__ __forceinline__ bool waitw(uint32_t b, uint32_t parity, bool cl, const Abort &ab,
-                                      int site, int it) {
-  const uint64_t t0 = now_ns();
-  for (;;) {
-    const bool done = cl ? mbar_test_cluster(b, parity) : mbar_test(b, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    const bool expired = now_ns() - t0 > kTimeoutNs;
-    if (__any_sync(0xffffffffu, expired || *ab.flag)) {
-      const bool any_expired = __any_sync(0xffffffffu, expired);
-      if ((threadIdx.x & 31) == 0) {
-        if (any_expired) ab.raise(site, it);
-        else ab.follow(site, it);
-      }
-      return false;
-    }
-  }
-}
-
-// bounded wait that ignores the abort flag: drains copies/MMAs already issued
-__device__ __forceinline__ void drain1(uint32_t b, uint32_t parity) {
-  const uint64_t t0 = now_ns();
-  while (!mbar_test(b, parity) && now_ns() - t0 <= kTimeoutNs) {
-  }
-}
-
-__device__ __forceinline__ float lo_bf(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float hi_bf(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 struct StatsArgs {
   const float *fn;
   const float *scale;
@@ -348,15 +166,6 @@ struct StatsArgs {
   int iters;
 };
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
-}
-
 template <int NM>
 __global__ void __launch_bounds__(kThreads, 1)
 pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
@@ -371,7 +180,8 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
   const int T = cid < a.num_tiles ? (a.num_tiles - 1 - cid) / ncl + 1 : 0;   // our tiles
   auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * (uint32_t)i; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kOffMisc);
-  Abort ab{reinterpret_cast<volatile int *>(sm + C::kOffMisc + 4), crank};
+  Abort ab{reinterpret_cast<volatile int *>(sm + C::kOffMisc + 4), crank, &g_fused_error,
+           g_fused_where, g_fused_where_aborted};
 
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
@@ -529,8 +339,9 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     uint32_t phase = 0;
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
-      // one accumulator per 16-byte chunk of the 128-byte row slice: eight
-      // short FMA chains instead of one long one (summed in a fixed tree)
+      // one accumulator per 16-byte chunk of the 128-byte row slice, one add
+      // per stage of that chunk's 8 squares (short chains, summed in a fixed
+      // tree at the end)
       float ssq[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) ssq[q] = 0.f;
@@ -543,13 +354,16 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         for (int q = 0; q < 8; ++q) cq[q] = *reinterpret_cast<const uint4 *>(st + ((q ^ sw) << 4));
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
+          // the chunk's 8 squares in a short chain, then one add per stage
           const uint32_t w4[4] = {cq[q].x, cq[q].y, cq[q].z, cq[q].w};
+          float c8 = lo_bf(w4[0]) * lo_bf(w4[0]);
+          c8 = fmaf(hi_bf(w4[0]), hi_bf(w4[0]), c8);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = lo_bf(w4[e]), x1 = hi_bf(w4[e]);
-            ssq[q] = fmaf(x0, x0, ssq[q]);
-            ssq[q] = fmaf(x1, x1, ssq[q]);
+          for (int e = 1; e < 4; ++e) {
+            c8 = fmaf(lo_bf(w4[e]), lo_bf(w4[e]), c8);
+            c8 = fmaf(hi_bf(w4[e]), hi_bf(w4[e]), c8);
           }
+          ssq[q] += c8;
         }
         // the stage is released only after every lane has used its data
         __syncwarp();
@@ -721,25 +535,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
 }
 
 // ---- host side -------------------------------------------------------------------
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-  static EncodeTiled fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  });
-  return fn;
-}
-
 constexpr int kMaxDev = 64;
 std::mutex g_dev_mu;
 template <int NM>

@@ -92,8 +92,9 @@ const char *mhc_last_cuda_error(void);
 size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
- * or nonzero once the stats kernel of mhc_pre or mhc_hc_head gave up a bounded
- * wait (it then returned early and its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
+ * or nonzero once a tensor-core kernel (the stats of mhc_pre or mhc_hc_head,
+ * or mhc_fused_post_pre) gave up a bounded wait (it then returned early and
+ * its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
  * the device's pending work.  Returns MHC_OK or MHC_ERR_NULL/MHC_ERR_CUDA. */
 int mhc_kernel_status(uint32_t *status, int reset);
 
@@ -220,6 +221,40 @@ int mhc_post(const uint16_t *R, const uint16_t *y, const float *post, const floa
 int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
                      float norm_eps, int64_t rows, int64_t logical_rows, uint16_t *x_norm,
                      void *stream);
+
+/*
+ * mhc_fused_post_pre -- hc_post of one sublayer and hc_pre of the next on its
+ * result, in one call (the pages' mhc_fused_post_pre between sublayers).
+ *
+ * deepseek_v4.py, DeepseekV4DecoderLayer forward (the use_fused_mhc_post_pre
+ * path): R_out = hc_post(R, y, post, comb) exactly as mhc_post computes it
+ * (same bits), then everything mhc_pre computes, on R_out, with the next
+ * sublayer's fn, scale, base and norm weight.
+ *
+ * Chunks of more than 48 rows: one launch computes R_out from registers,
+ * writes it once and feeds it straight to the tensor-core stats (R_out is
+ * never read back for them), then the pre pass's streaming combine + RMSNorm
+ * (with the Sinkhorn) reads R_out.  Decode-size chunks (<= 48 rows): mhc_post
+ * then the decode-size mhc_pre.
+ *
+ * Arguments
+ *   R, y, post, comb        as for mhc_post (post [rows, 4] and comb
+ *                           [rows, 4, 4] of the sublayer just run)
+ *   fn, scale, base, norm_w as for mhc_pre (of the next sublayer)
+ *   p, workspace, workspace_bytes  as for mhc_pre
+ * Outputs
+ *   R_out    [rows, 4, 5120] bf16   the new residual
+ *   x_norm   [rows, 5120] bf16      the next sublayer's input
+ *   post_out [rows, 4], comb_out [rows, 4, 4] fp32   the next sublayer's gates
+ *   pre_out  [rows, 4] or NULL, mix_out [rows, 24] or NULL
+ * No output may overlap an input or another output.  Errors as for mhc_pre.
+ */
+int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
+                       const float *comb, const float *fn, const float *scale, const float *base,
+                       const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+                       const mhc_params *p, void *workspace, size_t workspace_bytes,
+                       uint16_t *R_out, uint16_t *x_norm, float *post_out, float *comb_out,
+                       float *pre_out, float *mix_out, void *stream);
 
 /*
  * mhc_hc_head -- the model's final collapse of the 4 residual streams into one

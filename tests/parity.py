@@ -3,7 +3,13 @@ host cores, and the element-wise tolerance checks.
 
 Tolerances (GPU vs the fp64 oracle on identical inputs):
   mix      |d| <= 1e-4 * max(|ref|, rms of the row's 24 mixes)
-  pre/post |d| <= 1e-6 absolute
+  pre/post |d| <= 1e-6 absolute, or what the kernels' arithmetic allows:
+           the tensor-core dots hold fn as bf16 hi + bf16 lo, whose residual
+           is at most 2^-17 of each fn element; taken as independent uniform
+           errors, a dot's error has sigma = 2^-17/sqrt(3) * ||x o fn_c||_2.
+           Six sigma of that, times rsqrt, times |scale|, plus the fp32
+           rounding of the logit (8 * 2^-24 of its largest term), times the
+           gate's slope, is also accepted
   comb     |d| <= 1e-6 absolute
   bf16 outputs (x_norm, R_out): |d| <= 2 bf16 ulp of the reference value, or
            |d| <= 2e-2 on the scaled columns 0..63 of a stream, or
@@ -76,6 +82,30 @@ def check_mix(gpu, ref, name="mix"):
     tol = 1e-4 * np.maximum(np.abs(ref), rms)
     d = np.abs(gpu - ref)
     _report(name, d > tol, d)
+
+
+def check_gates(gpu_pre, gpu_post, o, scale, R_bits, fn, post_mult=2.0, rms_eps=1e-6):
+    """pre and post gates against the oracle dict `o` (mix, logits, pre, post)
+    of the rows R_bits, whose stats used fn [24, 20480]."""
+    mix = np.asarray(o["mix"], np.float64)
+    logit = np.asarray(o["logits"], np.float64)
+    scale = np.asarray(scale, np.float64).reshape(-1)
+    g_of_c = np.where(np.arange(MIX) < 4, scale[0], np.where(np.arange(MIX) < 8, scale[1], scale[2]))
+    base = logit - mix * g_of_c
+    x = unbf(np.asarray(R_bits).reshape(len(mix), -1))
+    rsq = 1.0 / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + rms_eps)
+    f8 = np.asarray(fn, np.float64).reshape(MIX, -1)[:8]
+    sig_dot = np.sqrt((x * x) @ (f8 * f8).T)                   # [rows, 8]
+    dmix = 6.0 * 2.0 ** -17 / np.sqrt(3.0) * sig_dot * rsq
+    for name, gpu, ref, lo, mult in (("pre", gpu_pre, o["pre"], 0, 1.0),
+                                     ("post", gpu_post, o["post"], 4, post_mult)):
+        l = logit[:, lo:lo + 4]
+        sc = scale[0] if lo == 0 else scale[1]
+        term = np.maximum(np.abs(mix[:, lo:lo + 4] * sc), np.abs(base[:, lo:lo + 4]))
+        sg = 1.0 / (1.0 + np.exp(-l))
+        dl = abs(sc) * dmix[:, lo:lo + 4] + 8 * 2.0 ** -24 * term
+        d = np.abs(np.asarray(gpu, np.float64) - np.asarray(ref, np.float64))
+        _report(name, d > np.maximum(1e-6, mult * sg * (1 - sg) * dl), d)
 
 
 def check_abs(gpu, ref, tol, name):

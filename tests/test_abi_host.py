@@ -158,3 +158,29 @@ def test_hc_head_validation(lib):
     assert call_head(lib, y=fake(0)) == ERR_OVERLAP                       # y on R
     assert call_head(lib, ws=fake(5)) == ERR_OVERLAP                      # workspace on y
     assert call_head(lib, pre=fake(6), mix=fake(6)) == ERR_OVERLAP        # two outputs
+
+
+def call_fpp(lib, rows=4, logical=4, ws=fake(20), ws_bytes=None, **over):
+    import hyper_connection_residual_mhc_gb300 as m
+    a = dict(R=fake(0), y=fake(1), post=fake(2), comb=fake(3), fn=fake(4), scale=fake(5),
+             base=fake(6), w=fake(7), R_out=fake(8), xn=fake(9), post_out=fake(10),
+             comb_out=fake(11), pre=None, mix=None)
+    a.update(over)
+    p = m.default_params()
+    wsb = lib.mhc_pre_workspace_bytes(rows) if ws_bytes is None else ws_bytes
+    return lib.mhc_fused_post_pre(a["R"], a["y"], a["post"], a["comb"], a["fn"], a["scale"],
+                                  a["base"], a["w"], rows, logical, ctypes.byref(p), ws, wsb,
+                                  a["R_out"], a["xn"], a["post_out"], a["comb_out"], a["pre"],
+                                  a["mix"], None)
+
+
+def test_fused_post_pre_validation(lib):
+    assert call_fpp(lib, rows=-1) == ERR_SHAPE
+    assert call_fpp(lib, rows=0, logical=0, R=None) == 0
+    assert call_fpp(lib, y=None) == ERR_NULL
+    assert call_fpp(lib, comb_out=fake(11) + 4) == ERR_ALIGN
+    assert call_fpp(lib, ws=None) == ERR_WORKSPACE
+    assert call_fpp(lib, post_out=fake(2)) == ERR_OVERLAP      # next post on this post
+    assert call_fpp(lib, R_out=fake(0)) == ERR_OVERLAP         # in-place residual
+    assert call_fpp(lib, xn=fake(8)) == ERR_OVERLAP            # two outputs
+    assert call_fpp(lib, ws=fake(1)) == ERR_OVERLAP            # workspace on y

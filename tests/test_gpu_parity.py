@@ -84,10 +84,9 @@ def _bits(torch, t):
 def _check_pre(torch, g, o, c, rows_idx=None):
     sel = (lambda a: a) if rows_idx is None else (lambda a: a[rows_idx])
     P.check_mix(sel(host_f(g["mix"])), o["mix"])
-    P.check_abs(sel(host_f(g["pre"])), o["pre"], 1e-6, "pre")
-    P.check_abs(sel(host_f(g["post"])), o["post"], 1e-6, "post")
-    P.check_abs(sel(host_f(g["comb"])), o["comb"], 1e-6, "comb")
     R = c.R if rows_idx is None else c.R[rows_idx]
+    P.check_gates(sel(host_f(g["pre"])), sel(host_f(g["post"])), o, c.W.scale, R, c.W.fn)
+    P.check_abs(sel(host_f(g["comb"])), o["comb"], 1e-6, "comb")
     P.check_bf16(sel(_bits(torch, g["x_norm"])), o["x_norm"], "x_norm",
                  term_mag=P.combine_term_magnitude(R, o["pre"], c.W.norm_w, 1e-6))
 
