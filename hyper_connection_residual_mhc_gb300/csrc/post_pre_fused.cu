@@ -8,28 +8,30 @@
 // pages run the pair as one call (mhc_fused_post_pre) between sublayers.
 //
 // Unfused, R' is written by hc_post and read back by the stats; here the
-// stats consume R' straight from the registers that computed it, so R' costs
-// one write and no read.  The decomposition follows the stats kernel
+// stats take R' from shared memory where it was just formed, so for them R'
+// costs one write and no read.  The decomposition follows the stats kernel
 // (pre_stats.cu): a cluster of 16 CTAs owns a 128-row tile at a time, CTA s
 // owns hidden columns [320 s, 320 s + 320) of all four streams, and its fn
-// slice (bf16 hi + lo, 120 KB) stays in shared memory.  The TMA producer and
-// the row warps are replaced by eight converter warps:
-//   * per 64-column block of the CTA's columns (a "set": the 4 streams'
-//     16 KB stages), each converter thread loads R_0..3 and y for four
-//     (row, 8-column) items, forms R' (the same arithmetic as mhc_post, so
-//     R' has mhc_post's bits), writes it to HBM, writes it into the set's
-//     128-byte-swizzled stages for the tensor core, and adds its squares to
-//     the row's sum of squares;
-//   * one thread issues tcgen05.mma (M=128 rows, N=48, K=16) per stage;
+// slice (bf16 hi + lo, 120 KB) stays in shared memory.  Per tile and CTA the
+// 320 columns go through in ten "half-sets" of 32 columns, double-buffered:
+//   * a TMA producer loads a half-set -- R_0..3 and y, 128 rows x 32
+//     columns each, 64-byte swizzle, 40 KB -- into a free buffer;
+//   * eight converter warps form R' in place (the same arithmetic as
+//     mhc_post, so R' has mhc_post's bits) and add its squares to the rows'
+//     sums of squares;
+//   * the converters also write R' to R_out from their registers (the TMA
+//     unit carries only the loads);
+//   * one thread issues tcgen05.mma (M=128 rows, N=48, K=16) on the four R'
+//     stages; the buffer is refilled once those MMAs have completed;
 //   * four readout warps load the accumulator, push each row's 24 partials
 //     and sum of squares to the row's owner CTA, then, as owners, reduce the
 //     16 CTAs' partials in CTA order and write the gates and comb logits.
 // The combine + RMSNorm and the Sinkhorn of the next pre then run as the
-// pre pass's streaming launch (pre_simt.cu) on R'.
+// pre pass's streaming launch (pre_simt.cu) on R_out.
 //
 // Every wait is bounded (~2 s); on expiry a CTA raises an abort flag, records
-// the site in this kernel's error word, drains its MMAs, frees its tensor
-// memory and returns.
+// the site in this kernel's error word, drains its copies and MMAs, frees its
+// tensor memory and returns.
 #include "mhc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -45,42 +47,39 @@ using namespace ptx;
 constexpr int kCl = 16;                       // CTAs per cluster (K split)
 constexpr int kTile = 128;                    // rows per tile = UMMA M
 constexpr int kHs = kH / kCl;                 // 320 columns per CTA
-constexpr int kBk = 64;                       // columns per stage
-constexpr int kHb = kHs / kBk;                // 5 sets per tile
-constexpr int kKb = kHC * kHb;                // 20 fn k-blocks
+constexpr int kBh = 32;                       // columns per half-set (64-byte rows)
+constexpr int kNh = kHs / kBh;                // 10 half-sets per tile
+constexpr int kKb = kHC * (kHs / 64);         // 20 fn k-blocks of 64
 constexpr int kN = 2 * kMix;                  // fn hi (24) + lo (24)
-constexpr int kStageBytes = kTile * kBk * 2;  // 16384
-constexpr int kFnBlkBytes = kN * kBk * 2;     // 6144
+constexpr int kStageBytes = kTile * kBh * 2;  // 8192: one stream (or y), 128 rows x 32
+constexpr int kSetBytes = (kHC + 1) * kStageBytes;   // R_0..3 and y: 40960
+constexpr int kFnBlkBytes = kN * 64 * 2;      // 6144
 constexpr int kRw = 28;                       // receive words per row
 constexpr int kOwn = kTile / kCl;             // 8 rows finalised per CTA
 constexpr int kTmemCols = 128;
-constexpr int kPc = kHC + kHC * kHC;          // post + comb floats per row
 
-// warps: 0 MMA; 1..8 converters; 9..12 readout, then owners
-constexpr int kMmaWarp = 0;
-constexpr int kConv0 = 1, kConvN = 8;
-constexpr int kRead0 = 9, kReadN = 4;
-constexpr int kWarps = 13;
-constexpr int kThreads = kWarps * 32;         // 416
-constexpr int kItems = 4;                     // (row, chunk) items per converter thread per set
-// 13 warps put 4 on one SM sub-partition, whose 16K registers then allow at
-// most 128 a thread: the launch bound keeps the kernel within it
-static_assert(kWarps <= 16, "");
-
-static_assert(kConvN * 32 * kItems == kTile * (kBk / 8), "one item per (row, 8 columns)");
+// warps: 0 TMA producer; 1 MMA; 2..9 converters; 10..13 readout, then owners
+// (14 warps: at most 4 on a sub-partition, 128 registers each)
+constexpr int kProdWarp = 0, kMmaWarp = 1;
+constexpr int kConv0 = 2, kConvN = 8;
+constexpr int kRead0 = 10, kReadN = 4;
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;         // 448
+constexpr int kItems = 2;                     // (row, 8 columns) items per converter thread
+static_assert(kConvN * 32 * kItems == kTile * (kBh / 8), "one item per (row, 8 columns)");
 
 // shared memory (from a 1024-byte aligned base)
 constexpr int kOffFn = 0;
-constexpr int kOffSet = kOffFn + kKb * kFnBlkBytes;           // 4 stages, one per stream
-constexpr int kOffPc = kOffSet + kHC * kStageBytes;           // [8 warps][16 rows][20] post, comb
-constexpr int kOffRecv = kOffPc + kTile * kPc * 4;            // [16 src][8 rows][kRw]
+constexpr int kOffBuf = kOffFn + kKb * kFnBlkBytes;           // [2][5 stages]
+constexpr int kOffRecv = kOffBuf + 2 * kSetBytes;             // [16 src][8 rows][kRw]
 constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;      // [8 rows][kRw]
 constexpr int kOffSs = kOffRed + kOwn * kRw * 4;              // [2][128] sum x^2
 constexpr int kOffBar = kOffSs + 2 * kTile * 4;
 enum Bar : int {
-  B_SFULL = 0,                   // the set's 4 stages written (8 converter warps)
-  B_SEMPTY = B_SFULL + 1,        // the set consumed by the MMAs (commit)
-  B_TFULL = B_SEMPTY + 1,        // [2] accumulator complete
+  B_FULL = 0,                    // [2] a half-set landed (TMA bytes)
+  B_CONV = B_FULL + 2,           // [2] converted to R' (8 converter warps)
+  B_FREE = B_CONV + 2,           // [2] the MMAs on it completed (commit)
+  B_TFULL = B_FREE + 2,          // [2] accumulator complete
   B_TEMPTY = B_TFULL + 2,        // [2] accumulator and sum x^2 read out
   B_SSREADY = B_TEMPTY + 2,      // [2] the converters wrote a tile's sum x^2
   B_PREADY = B_SSREADY + 2,      // all 16 CTAs pushed partials to us (remote)
@@ -90,22 +89,20 @@ enum Bar : int {
   B_DRAIN = B_OPULL + 1,         // final MMA drain
   B_COUNT = B_DRAIN + 1
 };
-static_assert(B_COUNT == 1 + 1 + 2 + 2 + 2 + 5, "barrier slots overlap");
+static_assert(B_COUNT == 6 * 2 + 5, "barrier slots overlap");
 constexpr int kOffMisc = kOffBar + B_COUNT * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
-static_assert(kOffSet % 1024 == 0 && kStageBytes % 1024 == 0 && kFnBlkBytes % 1024 == 0, "");
-static_assert(kOffRecv % 16 == 0 && kOffPc % 16 == 0, "");
+static_assert(kOffBuf % 1024 == 0 && kStageBytes % 1024 == 0 && kFnBlkBytes % 1024 == 0, "");
+static_assert(kOffRecv % 16 == 0, "");
 
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) |
                             ((uint32_t)(kTile >> 4) << 24);
 
 struct FusedArgs {
-  const uint4 *R;          // [rows, 4, 640] 16-byte chunks
-  const uint4 *y;          // [rows, 640]
   const float *post_in;    // [rows, 4]
   const float *comb_in;    // [rows, 4, 4]
-  uint4 *R_out;            // [rows, 4, 640]
+  uint4 *R_out;            // [rows, 4, 640] 16-byte chunks
   const float *fn;
   const float *scale;
   const float *base;
@@ -119,7 +116,9 @@ struct FusedArgs {
   float rms_eps, pre_eps, post_mult;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) post_pre_fused_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
+                      const __grid_constant__ CUtensorMap map_y, const FusedArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -136,9 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1) post_pre_fused_kernel(const Fused
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
     *ab.flag = 0;
-    mbar_init(bar(B_SFULL), kConvN);
-    mbar_init(bar(B_SEMPTY), 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_FULL + b), 1);
+      mbar_init(bar(B_CONV + b), kConvN);
+      mbar_init(bar(B_FREE + b), 1);
       mbar_init(bar(B_TFULL + b), 1);
       mbar_init(bar(B_TEMPTY + b), kReadN);
       mbar_init(bar(B_SSREADY + b), kConvN);
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) post_pre_fused_kernel(const Fused
     constexpr int kFnItems = kMix * kKb * 8;   // items of 8 consecutive k
     for (int item = threadIdx.x; item < kFnItems; item += kThreads) {
       const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
-      const int k0 = (j & 3) * kH + (int)crank * kHs + (j >> 2) * kBk + 8 * q;
+      const int k0 = (j & 3) * kH + (int)crank * kHs + (j >> 2) * 64 + 8 * q;
       const float4 f0 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0));
       const float4 f1 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0 + 4));
       const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
@@ -186,30 +186,59 @@ __global__ void __launch_bounds__(kThreads, 1) post_pre_fused_kernel(const Fused
   const uint32_t tmem = *tmem_slot;
 
   // ---- roles -------------------------------------------------------------------
-  if (warp == kMmaWarp) {
-    // whole warp walks the loops (warp-collective waits); lane 0 issues
-    uint32_t g = 0;                              // set counter
+  if (warp == kProdWarp) {
+    // whole warp walks the loop (warp-collective waits); lane 0 issues
+    uint32_t g = 0;
+    int last[2] = {-1, -1};
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
+      const int y0 = (cid + it * ncl) * kTile;
+      for (int hh = 0; hh < kNh; ++hh, ++g) {
+        const int b = (int)(g & 1);
+        if (!waitw(bar(B_FREE + b), ((g >> 1) & 1) ^ 1, false, ab, 1, it)) { ok = false; break; }
+        if (lane == 0) {
+          const uint32_t dst = sb + kOffBuf + b * kSetBytes;
+          const int xc = (int)crank * kHs + hh * kBh;
+          mbar_expect_tx(bar(B_FULL + b), kSetBytes);
+#pragma unroll
+          for (int i = 0; i < kHC; ++i)
+            tma_load_2d(dst + i * kStageBytes, &map_r, i * kH + xc, y0, bar(B_FULL + b));
+          tma_load_2d(dst + kHC * kStageBytes, &map_y, xc, y0, bar(B_FULL + b));
+        }
+        __syncwarp();
+        last[b] = (int)((g >> 1) & 1);
+      }
+    }
+    // every copy issued must have landed before the CTA may exit
+    for (int b = 0; b < 2; ++b)
+      if (last[b] >= 0) drain1(bar(B_FULL + b), (uint32_t)last[b]);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    uint32_t g = 0;
+    bool ok = true;
+    for (int it = 0; it < T && ok; ++it) {
+      const int y0 = (cid + it * ncl) * kTile;
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       if (!waitw(bar(B_TEMPTY + buf), (use & 1) ^ 1, false, ab, 2, it)) break;
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)(buf * 64);
-      for (int hb = 0; hb < kHb; ++hb, ++g) {
-        if (!waitw(bar(B_SFULL), g & 1, false, ab, 3, it)) { ok = false; break; }
+      for (int hh = 0; hh < kNh; ++hh, ++g) {
+        const int b = (int)(g & 1);
+        if (!waitw(bar(B_CONV + b), (g >> 1) & 1, false, ab, 3, it)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
+          const uint32_t src = sb + kOffBuf + b * kSetBytes;
 #pragma unroll 1
           for (int i = 0; i < kHC; ++i) {
-            const int j = i + kHC * hb;
-            const uint64_t ad = sw128_desc(sb + kOffSet + i * kStageBytes);
-            const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes);
+            const int j = i + kHC * (hh >> 1);
+            const uint64_t ad = sw64_desc(src + i * kStageBytes);
+            const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes) + 4 * (hh & 1);
 #pragma unroll
-            for (int kk = 0; kk < kBk / 16; ++kk)
-              tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (hb | i | kk) != 0);
+            for (int kk = 0; kk < kBh / 16; ++kk)
+              tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (hh | i | kk) != 0);
           }
-          tc_commit(bar(B_SEMPTY));
+          tc_commit(bar(B_FREE + b));
         }
         __syncwarp();
       }
@@ -217,100 +246,84 @@ __global__ void __launch_bounds__(kThreads, 1) post_pre_fused_kernel(const Fused
       if (lane == 0) tc_commit(bar(B_TFULL + buf));
       __syncwarp();
     }
-    // all issued MMAs complete before TMEM is freed
-    if (lane == 0) tc_commit(bar(B_DRAIN));
+    if (lane == 0) tc_commit(bar(B_DRAIN));   // all issued MMAs complete before TMEM is freed
     __syncwarp();
     drain1(bar(B_DRAIN), 0);
     __syncwarp();
   } else if (warp >= kConv0 && warp < kConv0 + kConvN) {
-    // ---- converters: R' = post(R, y), to HBM and to the tensor core ---------
-    const int cw = warp - kConv0, rsub = lane >> 3, q = lane & 7;
-    // this warp's 16 rows' post and comb (warp-private: only __syncwarp
-    // orders it, so no warp ever waits at a barrier another may have left)
-    float *pcw = reinterpret_cast<float *>(sm + kOffPc) + cw * 16 * kPc;
+    // ---- converters: R' = post(R, y) in place, and the rows' sums of squares
+    const int cw = warp - kConv0, c = lane & 3, rs = lane >> 2;
     float *ssbuf = reinterpret_cast<float *>(sm + kOffSs);
     uint32_t g = 0;
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
       const int64_t row0 = (int64_t)(cid + it * ncl) * kTile;
-      __syncwarp();                             // the previous tile's reads are done
-      for (int t = lane; t < 16 * kPc; t += 32) {
-        const int rl = t / kPc, c = t % kPc;
-        const int64_t gr = row0 + cw * 16 + rl;
-        float v = 0.f;
-        if (gr < a.rows) v = c < kHC ? __ldg(a.post_in + gr * kHC + c) : __ldg(a.comb_in + gr * 16 + (c - kHC));
-        pcw[t] = v;
-      }
-      __syncwarp();
-      float ssq[kItems];
+      // post and comb of this thread's two rows (zeros past the last row)
+      float pv[kItems][kHC], cb[kItems][kHC][kHC];
 #pragma unroll
-      for (int k = 0; k < kItems; ++k) ssq[k] = 0.f;
-      for (int hb = 0; hb < kHb; ++hb, ++g) {
-        const int h8 = (int)crank * (kHs / 8) + hb * (kBk / 8) + q;   // 16-byte column index
-        uint4 rv[kItems][kHC], yv[kItems];
+      for (int k = 0; k < kItems; ++k) {
+        const int64_t gr = row0 + cw * 16 + 8 * k + rs;
+        const bool in = gr < a.rows;
+        const float4 p4 = in ? __ldg(reinterpret_cast<const float4 *>(a.post_in + gr * kHC))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        pv[k][0] = p4.x; pv[k][1] = p4.y; pv[k][2] = p4.z; pv[k][3] = p4.w;
 #pragma unroll
-        for (int k = 0; k < kItems; ++k) {
-          const int r = cw * 16 + 4 * k + rsub;
-          const int64_t gr = row0 + r;
-          if (gr < a.rows) {
-#pragma unroll
-            for (int i = 0; i < kHC; ++i) rv[k][i] = ld_stream(a.R + (gr * kHC + i) * kChunksPerStream + h8);
-            yv[k] = ld_stream(a.y + gr * kChunksPerStream + h8);
-          } else {
-#pragma unroll
-            for (int i = 0; i < kHC; ++i) rv[k][i] = make_uint4(0u, 0u, 0u, 0u);
-            yv[k] = make_uint4(0u, 0u, 0u, 0u);
-          }
+        for (int j = 0; j < kHC; ++j) {
+          const float4 c4 = in ? __ldg(reinterpret_cast<const float4 *>(a.comb_in + gr * 16 + 4 * j))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          cb[k][j][0] = c4.x; cb[k][j][1] = c4.y; cb[k][j][2] = c4.z; cb[k][j][3] = c4.w;
         }
-        // the set's stages are free once the previous set's MMAs completed
-        if (!waitw(bar(B_SEMPTY), (g & 1) ^ 1, false, ab, 1, it)) { ok = false; break; }
+      }
+      float ssq[kItems] = {0.f, 0.f};
+      for (int hh = 0; hh < kNh; ++hh, ++g) {
+        const int b = (int)(g & 1);
+        const int h8c = (int)crank * (kHs / 8) + hh * (kBh / 8);   // first 16-byte column
+        if (!waitw(bar(B_FULL + b), (g >> 1) & 1, false, ab, 4, it)) { ok = false; break; }
+        uint8_t *buf = sm + kOffBuf + b * kSetBytes;
 #pragma unroll
         for (int k = 0; k < kItems; ++k) {
-          const int r = cw * 16 + 4 * k + rsub;
-          const int64_t gr = row0 + r;
-          const float *pr = pcw + (4 * k + rsub) * kPc;
-          const float pv[kHC] = {pr[0], pr[1], pr[2], pr[3]};
-          float cb[kHC][kHC];
+          const int r = cw * 16 + 8 * k + rs;
+          const int off = r * 64 + ((c ^ ((r >> 1) & 3)) << 4);   // 64-byte swizzle
+          uint4 rv[kHC];
 #pragma unroll
-          for (int j = 0; j < kHC; ++j)
-#pragma unroll
-            for (int i = 0; i < kHC; ++i) cb[j][i] = pr[kHC + 4 * j + i];
+          for (int i = 0; i < kHC; ++i) rv[i] = *reinterpret_cast<const uint4 *>(buf + i * kStageBytes + off);
+          const uint4 yv = *reinterpret_cast<const uint4 *>(buf + kHC * kStageBytes + off);
           uint4 ov[kHC];
-          post_chunk(rv[k], yv[k], pv, cb, ov);
+          post_chunk(rv, yv, pv[k], cb[k], ov);
           float si[kHC];                        // per stream: 8 squares
 #pragma unroll
           for (int i = 0; i < kHC; ++i) {
-            *reinterpret_cast<uint4 *>(sm + kOffSet + i * kStageBytes + r * 128 + ((q ^ (r & 7)) << 4)) = ov[i];
+            *reinterpret_cast<uint4 *>(buf + i * kStageBytes + off) = ov[i];
+            if (row0 + r < a.rows)
+              st_stream(a.R_out + ((row0 + r) * kHC + i) * kChunksPerStream + h8c + c, ov[i]);
             float of[8];
             unpack8(ov[i], of);
             si[i] = of[0] * of[0];
 #pragma unroll
             for (int e = 1; e < 8; ++e) si[i] = fmaf(of[e], of[e], si[i]);
-            if (gr < a.rows) st_stream(a.R_out + (gr * kHC + i) * kChunksPerStream + h8, ov[i]);
           }
-          // short chains: 8 squares, a pairwise sum of the 4 streams, 5 sets
           ssq[k] += (si[0] + si[1]) + (si[2] + si[3]);
         }
+        // generic-proxy writes -> visible to the tensor core
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_SFULL));
+        if (lane == 0) mbar_arrive(bar(B_CONV + b));
       }
       if (!ok) break;
-      // the rows' sums of squares: the 8 lanes of a row (q = 0..7), fixed tree
+      // the rows' sums of squares: the 4 lanes of a row (c = 0..3), fixed tree
 #pragma unroll
       for (int k = 0; k < kItems; ++k) {
         ssq[k] += __shfl_xor_sync(0xffffffffu, ssq[k], 1);
         ssq[k] += __shfl_xor_sync(0xffffffffu, ssq[k], 2);
-        ssq[k] += __shfl_xor_sync(0xffffffffu, ssq[k], 4);
       }
-      const int buf = it & 1;
-      if (!waitw(bar(B_TEMPTY + buf), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 10, it)) break;
-      if (q == 0) {
+      const int tb = it & 1;
+      if (!waitw(bar(B_TEMPTY + tb), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 10, it)) break;
+      if (c == 0) {
 #pragma unroll
-        for (int k = 0; k < kItems; ++k) ssbuf[buf * kTile + cw * 16 + 4 * k + rsub] = ssq[k];
+        for (int k = 0; k < kItems; ++k) ssbuf[tb * kTile + cw * 16 + 8 * k + rs] = ssq[k];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SSREADY + buf));
+      if (lane == 0) mbar_arrive(bar(B_SSREADY + tb));
     }
   } else {
     // ---- readout (one thread per tile row), then owners of 8 rows ------------
@@ -454,6 +467,22 @@ cudaError_t fpp_configure(int dev, int *max_clusters) {
 
 }  // namespace
 
+namespace {
+// 2D bf16 tensor map over [rows, cols] (row-major), 128-row x 32-column
+// boxes, 64-byte swizzle
+bool encode_rows(CUtensorMap *map, const uint16_t *base, int64_t cols, int64_t rows) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBh, (cuuint32_t)kTile};
+  const cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), gdim, gstride,
+             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const float *post,
                                   const float *comb, const float *fn, const float *scale,
                                   const float *base, int64_t rows, int64_t logical_rows,
@@ -467,9 +496,10 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   int max_clusters = 0;
   e = fpp_configure(dev, &max_clusters);
   if (e != cudaSuccess) return e;
+  CUtensorMap map_r, map_y;
+  if (!encode_rows(&map_r, R, kK, rows) || !encode_rows(&map_y, y, kH, rows))
+    return cudaErrorInvalidValue;
   FusedArgs a;
-  a.R = reinterpret_cast<const uint4 *>(R);
-  a.y = reinterpret_cast<const uint4 *>(y);
   a.post_in = post;
   a.comb_in = comb;
   a.R_out = reinterpret_cast<uint4 *>(R_out);
@@ -494,7 +524,7 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, post_pre_fused_kernel, a);
+  return cudaLaunchKernelEx(&cfg, post_pre_fused_kernel, map_r, map_y, a);
 }
 
 cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset) {
