@@ -481,7 +481,8 @@ def run_op(args):
         xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
         po = torch.empty((M, HC), dtype=torch.float32, device=dev)
         co = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
-        ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+        ws = torch.empty((max(256, m.mhc_fused_post_pre_workspace_bytes(M)),), dtype=torch.uint8,
+                         device=dev)
 
         def step():
             m.mhc_fused_post_pre(R, yv, post, comb, fn, scale, base, w, logical_rows=M,

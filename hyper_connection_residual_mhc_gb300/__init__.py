@@ -63,6 +63,7 @@ SIGNATURES = {
     "mhc_fused_post_pre": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                                           ctypes.POINTER(MhcParams), _vp, ctypes.c_size_t, _vp,
                                           _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mhc_fused_post_pre_workspace_bytes": (ctypes.c_size_t, [_i64]),
     "mhc_hc_head": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
                                    ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
 }
@@ -147,6 +148,10 @@ def mhc_kernel_status_detail() -> dict:
 
 def mhc_pre_workspace_bytes(rows: int) -> int:
     return int(lib().mhc_pre_workspace_bytes(int(rows)))
+
+
+def mhc_fused_post_pre_workspace_bytes(rows: int) -> int:
+    return int(lib().mhc_fused_post_pre_workspace_bytes(int(rows)))
 
 
 def mhc_pre(R, fn, scale, base, norm_w, *, logical_rows=None, params=None, workspace=None,
@@ -312,7 +317,7 @@ def mhc_fused_post_pre(R, y, post, comb, fn, scale, base, norm_w, *, logical_row
         _need(pre_out, "pre_out", torch.float32, (rows, HC))
     if mix_out is not None:
         _need(mix_out, "mix_out", torch.float32, (rows, MIX))
-    need = mhc_pre_workspace_bytes(rows)
+    need = mhc_fused_post_pre_workspace_bytes(rows)
     if workspace is None and need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

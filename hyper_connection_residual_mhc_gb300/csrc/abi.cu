@@ -104,6 +104,13 @@ size_t mhc_pre_workspace_bytes(int64_t rows) {
   return gate_bytes(rows) + logit_bytes(rows);
 }
 
+size_t mhc_fused_post_pre_workspace_bytes(int64_t rows) {
+  if (rows <= 0) return 0;
+  // what mhc_pre's launches hand each other, then fn in the fused kernel's
+  // B-operand image (written by the call itself)
+  return mhc_pre_workspace_bytes(rows) + mhc::fused_fn_bytes();
+}
+
 int mhc_kernel_status_detail(uint32_t *where64) {
   if (!where64) return MHC_ERR_NULL;
   cudaError_t e = mhc::fused_error_where(where64);
@@ -288,7 +295,7 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
   for (const void *q : al)
     if (!aligned16(q)) return MHC_ERR_ALIGN;
   if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
-  const size_t need = mhc_pre_workspace_bytes(rows);
+  const size_t need = mhc_fused_post_pre_workspace_bytes(rows);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return MHC_ERR_WORKSPACE;
   const size_t nr = (size_t)rows;
@@ -323,8 +330,9 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
   } else {
     float *pre_ws = static_cast<float *>(workspace);
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
+    uint8_t *fnp = static_cast<uint8_t *>(workspace) + mhc_pre_workspace_bytes(rows);
     ce = mhc::launch_post_pre_fused(R, y, post, comb, fn, scale, base, rows, logical_rows, p,
-                                    pre_ws, logit_ws, R_out, post_out, pre_out, mix_out, s);
+                                    pre_ws, logit_ws, fnp, R_out, post_out, pre_out, mix_out, s);
     if (ce == cudaSuccess)
       ce = mhc::launch_combine_norm_sinkhorn(R_out, pre_ws, norm_w, p.norm_eps, logit_ws, comb_out,
                                              p.hc_sinkhorn_eps, p.sinkhorn_iters, rows, x_norm, s);

@@ -125,11 +125,13 @@ cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t row
 // hc_post fused with the next pre's stats (post_pre_fused.cu): writes R_out,
 // the next pre's gates to pre_ws [rows, 4], its comb logits to logit_ws
 // [rows, 16] and its post gates (+ pre_out, mix_out)
+// (fnp: fused_fn_bytes() of scratch for fn in the kernel's B-operand image)
+size_t fused_fn_bytes();
 cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const float *post,
                                   const float *comb, const float *fn, const float *scale,
                                   const float *base, int64_t rows, int64_t logical_rows,
                                   const mhc_params &p, float *pre_ws, float *logit_ws,
-                                  uint16_t *R_out, float *post_out, float *pre_out,
+                                  uint8_t *fnp, uint16_t *R_out, float *post_out, float *pre_out,
                                   float *mix_out, cudaStream_t s);
 cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset);
 // the stats kernel's error word (nonzero once a bounded wait expired)

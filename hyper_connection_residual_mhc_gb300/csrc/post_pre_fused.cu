@@ -49,11 +49,12 @@ constexpr int kTile = 128;                    // rows per tile = UMMA M
 constexpr int kHs = kH / kCl;                 // 320 columns per CTA
 constexpr int kBh = 32;                       // columns per half-set (64-byte rows)
 constexpr int kNh = kHs / kBh;                // 10 half-sets per tile
-constexpr int kKb = kHC * (kHs / 64);         // 20 fn k-blocks of 64
 constexpr int kN = 2 * kMix;                  // fn hi (24) + lo (24)
 constexpr int kStageBytes = kTile * kBh * 2;  // 8192: one stream (or y), 128 rows x 32
-constexpr int kSetBytes = (kHC + 1) * kStageBytes;   // R_0..3 and y: 40960
-constexpr int kFnBlkBytes = kN * 64 * 2;      // 6144
+constexpr int kFnBlkBytes = kN * kBh * 2;     // 3072: fn hi/lo for 32 k (64-byte rows)
+constexpr int kSetBytes = (kHC + 1) * kStageBytes + kHC * kFnBlkBytes;  // R_0..3, y, 4 fn blocks
+constexpr int kBufs = 4;                      // half-sets in flight
+constexpr int kFnBlocks = kK / kBh;           // 640 fn blocks of 32 k
 constexpr int kRw = 28;                       // receive words per row
 constexpr int kOwn = kTile / kCl;             // 8 rows finalised per CTA
 constexpr int kTmemCols = 128;
@@ -69,17 +70,16 @@ constexpr int kItems = 2;                     // (row, 8 columns) items per conv
 static_assert(kConvN * 32 * kItems == kTile * (kBh / 8), "one item per (row, 8 columns)");
 
 // shared memory (from a 1024-byte aligned base)
-constexpr int kOffFn = 0;
-constexpr int kOffBuf = kOffFn + kKb * kFnBlkBytes;           // [2][5 stages]
-constexpr int kOffRecv = kOffBuf + 2 * kSetBytes;             // [16 src][8 rows][kRw]
+constexpr int kOffBuf = 0;                                    // [kBufs][R_0..3, y, fn x 4]
+constexpr int kOffRecv = kOffBuf + kBufs * kSetBytes;         // [16 src][8 rows][kRw]
 constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;      // [8 rows][kRw]
 constexpr int kOffSs = kOffRed + kOwn * kRw * 4;              // [2][128] sum x^2
 constexpr int kOffBar = kOffSs + 2 * kTile * 4;
 enum Bar : int {
-  B_FULL = 0,                    // [2] a half-set landed (TMA bytes)
-  B_CONV = B_FULL + 2,           // [2] converted to R' (8 converter warps)
-  B_FREE = B_CONV + 2,           // [2] the MMAs on it completed (commit)
-  B_TFULL = B_FREE + 2,          // [2] accumulator complete
+  B_FULL = 0,                    // [kBufs] a half-set landed (copy bytes)
+  B_CONV = B_FULL + kBufs,       // [kBufs] converted to R' (8 converter warps)
+  B_FREE = B_CONV + kBufs,       // [kBufs] the MMAs on it completed (commit)
+  B_TFULL = B_FREE + kBufs,      // [2] accumulator complete
   B_TEMPTY = B_TFULL + 2,        // [2] accumulator and sum x^2 read out
   B_SSREADY = B_TEMPTY + 2,      // [2] the converters wrote a tile's sum x^2
   B_PREADY = B_SSREADY + 2,      // all 16 CTAs pushed partials to us (remote)
@@ -89,21 +89,22 @@ enum Bar : int {
   B_DRAIN = B_OPULL + 1,         // final MMA drain
   B_COUNT = B_DRAIN + 1
 };
-static_assert(B_COUNT == 6 * 2 + 5, "barrier slots overlap");
+static_assert(B_COUNT == 3 * kBufs + 3 * 2 + 5, "barrier slots overlap");
 constexpr int kOffMisc = kOffBar + B_COUNT * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
-static_assert(kOffBuf % 1024 == 0 && kStageBytes % 1024 == 0 && kFnBlkBytes % 1024 == 0, "");
+static_assert(kOffBuf % 1024 == 0 && kStageBytes % 1024 == 0 && kFnBlkBytes % 1024 == 0 &&
+                  kSetBytes % 1024 == 0, "64-byte swizzle tiles need 512-byte alignment");
 static_assert(kOffRecv % 16 == 0, "");
 
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) |
                             ((uint32_t)(kTile >> 4) << 24);
 
 struct FusedArgs {
+  const uint8_t *fnp;      // fn as bf16 hi/lo 32-k blocks in their shared-memory image
   const float *post_in;    // [rows, 4]
   const float *comb_in;    // [rows, 4, 4]
   uint4 *R_out;            // [rows, 4, 640] 16-byte chunks
-  const float *fn;
   const float *scale;
   const float *base;
   float *pre_ws;           // [rows, 4] pre gates of R'
@@ -135,10 +136,12 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
   // ---- set-up ---------------------------------------------------------------
   if (threadIdx.x == 0) {
     *ab.flag = 0;
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kBufs; ++b) {
       mbar_init(bar(B_FULL + b), 1);
       mbar_init(bar(B_CONV + b), kConvN);
       mbar_init(bar(B_FREE + b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_TFULL + b), 1);
       mbar_init(bar(B_TEMPTY + b), kReadN);
       mbar_init(bar(B_SSREADY + b), kConvN);
@@ -151,34 +154,6 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-  // fn columns of this CTA -> bf16 hi/lo B tiles (K-major, 128-byte swizzle),
-  // by all warps: k-block j covers k = (j%4)*5120 + 320*crank + 64*(j/4) + [0, 64)
-  {
-    constexpr int kFnItems = kMix * kKb * 8;   // items of 8 consecutive k
-    for (int item = threadIdx.x; item < kFnItems; item += kThreads) {
-      const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
-      const int k0 = (j & 3) * kH + (int)crank * kHs + (j >> 2) * 64 + 8 * q;
-      const float4 f0 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0));
-      const float4 f1 = __ldg(reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + k0 + 4));
-      const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * e]);
-        const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * e + 1]);
-        hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
-        lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
-      }
-      uint8_t *tile = sm + kOffFn + j * kFnBlkBytes;
-      const int nh = c, nlo = c + kMix;
-      *reinterpret_cast<uint4 *>(tile + (nh >> 3) * 1024 + (nh & 7) * 128 + ((q ^ (nh & 7)) << 4)) =
-          make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4 *>(tile + (nlo >> 3) * 1024 + (nlo & 7) * 128 +
-                                 ((q ^ (nlo & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    // generic-proxy writes -> visible to the tensor core (async proxy)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -189,13 +164,16 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
   if (warp == kProdWarp) {
     // whole warp walks the loop (warp-collective waits); lane 0 issues
     uint32_t g = 0;
-    int last[2] = {-1, -1};
+    int last[kBufs];
+#pragma unroll
+    for (int b = 0; b < kBufs; ++b) last[b] = -1;
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
       const int y0 = (cid + it * ncl) * kTile;
       for (int hh = 0; hh < kNh; ++hh, ++g) {
-        const int b = (int)(g & 1);
-        if (!waitw(bar(B_FREE + b), ((g >> 1) & 1) ^ 1, false, ab, 1, it)) { ok = false; break; }
+        const int b = (int)(g % kBufs);
+        const uint32_t use = g / kBufs;
+        if (!waitw(bar(B_FREE + b), (use & 1) ^ 1, false, ab, 1, it)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t dst = sb + kOffBuf + b * kSetBytes;
           const int xc = (int)crank * kHs + hh * kBh;
@@ -204,13 +182,19 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
           for (int i = 0; i < kHC; ++i)
             tma_load_2d(dst + i * kStageBytes, &map_r, i * kH + xc, y0, bar(B_FULL + b));
           tma_load_2d(dst + kHC * kStageBytes, &map_y, xc, y0, bar(B_FULL + b));
+          // the 4 streams' fn blocks of these 32 columns: block i * 160 + xc / 32
+#pragma unroll
+          for (int i = 0; i < kHC; ++i)
+            bulk_load(dst + (kHC + 1) * kStageBytes + i * kFnBlkBytes,
+                      a.fnp + (size_t)(i * (kH / kBh) + xc / kBh) * kFnBlkBytes, kFnBlkBytes,
+                      bar(B_FULL + b));
         }
         __syncwarp();
-        last[b] = (int)((g >> 1) & 1);
+        last[b] = (int)(use & 1);
       }
     }
     // every copy issued must have landed before the CTA may exit
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < kBufs; ++b)
       if (last[b] >= 0) drain1(bar(B_FULL + b), (uint32_t)last[b]);
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -224,16 +208,15 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)(buf * 64);
       for (int hh = 0; hh < kNh; ++hh, ++g) {
-        const int b = (int)(g & 1);
-        if (!waitw(bar(B_CONV + b), (g >> 1) & 1, false, ab, 3, it)) { ok = false; break; }
+        const int b = (int)(g % kBufs);
+        if (!waitw(bar(B_CONV + b), (g / kBufs) & 1, false, ab, 3, it)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
           const uint32_t src = sb + kOffBuf + b * kSetBytes;
 #pragma unroll 1
           for (int i = 0; i < kHC; ++i) {
-            const int j = i + kHC * (hh >> 1);
             const uint64_t ad = sw64_desc(src + i * kStageBytes);
-            const uint64_t bd = sw128_desc(sb + kOffFn + j * kFnBlkBytes) + 4 * (hh & 1);
+            const uint64_t bd = sw64_desc(src + (kHC + 1) * kStageBytes + i * kFnBlkBytes);
 #pragma unroll
             for (int kk = 0; kk < kBh / 16; ++kk)
               tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (hh | i | kk) != 0);
@@ -276,9 +259,9 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
       }
       float ssq[kItems] = {0.f, 0.f};
       for (int hh = 0; hh < kNh; ++hh, ++g) {
-        const int b = (int)(g & 1);
+        const int b = (int)(g % kBufs);
         const int h8c = (int)crank * (kHs / 8) + hh * (kBh / 8);   // first 16-byte column
-        if (!waitw(bar(B_FULL + b), (g >> 1) & 1, false, ab, 4, it)) { ok = false; break; }
+        if (!waitw(bar(B_FULL + b), (g / kBufs) & 1, false, ab, 4, it)) { ok = false; break; }
         uint8_t *buf = sm + kOffBuf + b * kSetBytes;
 #pragma unroll
         for (int k = 0; k < kItems; ++k) {
@@ -431,6 +414,34 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
   cluster_sync_all();
 }
 
+// fn [24, 20480] -> 640 blocks of 32 k (block i * 160 + h/32 for stream i):
+// a 48 x 32 bf16 tile in 64-byte-swizzled K-major layout, row c = bf16(fn[c])
+// (hi), row 24 + c = bf16(fn[c] - hi) (lo)
+__global__ void __launch_bounds__(256) fn_prep_sw64_kernel(const float *__restrict__ fn,
+                                                            uint8_t *__restrict__ fnp) {
+  const int t = blockIdx.x * 256 + threadIdx.x;
+  if (t >= kFnBlocks * kMix * 4) return;
+  const int q = t & 3, c = (t >> 2) % kMix, kb = t / (4 * kMix);
+  const int k0 = (kb / (kH / kBh)) * kH + (kb % (kH / kBh)) * kBh + 8 * q;
+  const float4 f0 = __ldg(reinterpret_cast<const float4 *>(fn + (int64_t)c * kK + k0));
+  const float4 f1 = __ldg(reinterpret_cast<const float4 *>(fn + (int64_t)c * kK + k0 + 4));
+  const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * e]);
+    const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * e + 1]);
+    hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
+    lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
+  }
+  uint8_t *blk = fnp + (size_t)kb * kFnBlkBytes;
+  const int rh = c, rl = c + kMix;
+  *reinterpret_cast<uint4 *>(blk + (rh >> 3) * 512 + (rh & 7) * 64 + ((q ^ ((rh >> 1) & 3)) << 4)) =
+      make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4 *>(blk + (rl >> 3) * 512 + (rl & 7) * 64 + ((q ^ ((rl >> 1) & 3)) << 4)) =
+      make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
 std::mutex g_fpp_mu;
 int g_fpp_clusters[64];   // per device: co-resident clusters (0: not configured)
 
@@ -483,11 +494,13 @@ bool encode_rows(CUtensorMap *map, const uint16_t *base, int64_t cols, int64_t r
 }
 }  // namespace
 
+size_t fused_fn_bytes() { return (size_t)kFnBlocks * kFnBlkBytes; }
+
 cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const float *post,
                                   const float *comb, const float *fn, const float *scale,
                                   const float *base, int64_t rows, int64_t logical_rows,
                                   const mhc_params &p, float *pre_ws, float *logit_ws,
-                                  uint16_t *R_out, float *post_out, float *pre_out,
+                                  uint8_t *fnp, uint16_t *R_out, float *post_out, float *pre_out,
                                   float *mix_out, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -499,11 +512,15 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   CUtensorMap map_r, map_y;
   if (!encode_rows(&map_r, R, kK, rows) || !encode_rows(&map_y, y, kH, rows))
     return cudaErrorInvalidValue;
+  constexpr int kPrepItems = kFnBlocks * kMix * 4;
+  fn_prep_sw64_kernel<<<(kPrepItems + 255) / 256, 256, 0, s>>>(fn, fnp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   FusedArgs a;
   a.post_in = post;
   a.comb_in = comb;
   a.R_out = reinterpret_cast<uint4 *>(R_out);
-  a.fn = fn; a.scale = scale; a.base = base;
+  a.fnp = fnp; a.scale = scale; a.base = base;
   a.pre_ws = pre_ws; a.logit_ws = logit_ws; a.post_out = post_out;
   a.pre_out = pre_out; a.mix_out = mix_out;
   a.rows = rows;

@@ -231,17 +231,22 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
  * (same bits), then everything mhc_pre computes, on R_out, with the next
  * sublayer's fn, scale, base and norm weight.
  *
- * Chunks of more than 48 rows: one launch computes R_out from registers,
- * writes it once and feeds it straight to the tensor-core stats (R_out is
- * never read back for them), then the pre pass's streaming combine + RMSNorm
- * (with the Sinkhorn) reads R_out.  Decode-size chunks (<= 48 rows): mhc_post
+ * Chunks of more than 48 rows: a short launch converts fn into the fused
+ * kernel's operand image, then one launch computes R_out, writes it once and
+ * feeds it straight to the tensor-core stats (R_out is never read back for
+ * them), then the pre pass's streaming combine + RMSNorm (with the Sinkhorn)
+ * reads R_out.  Decode-size chunks (<= 48 rows): mhc_post
  * then the decode-size mhc_pre.
  *
  * Arguments
  *   R, y, post, comb        as for mhc_post (post [rows, 4] and comb
  *                           [rows, 4, 4] of the sublayer just run)
  *   fn, scale, base, norm_w as for mhc_pre (of the next sublayer)
- *   p, workspace, workspace_bytes  as for mhc_pre
+ *   p        as for mhc_pre
+ *   workspace, workspace_bytes  device scratch of at least
+ *            mhc_fused_post_pre_workspace_bytes(rows) bytes, 256-byte aligned
+ *            (what the pre launches hand each other, plus fn converted by the
+ *            call into the fused kernel's operand image, 1.97 MB)
  * Outputs
  *   R_out    [rows, 4, 5120] bf16   the new residual
  *   x_norm   [rows, 5120] bf16      the next sublayer's input
@@ -249,6 +254,7 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
  *   pre_out  [rows, 4] or NULL, mix_out [rows, 24] or NULL
  * No output may overlap an input or another output.  Errors as for mhc_pre.
  */
+size_t mhc_fused_post_pre_workspace_bytes(int64_t rows);
 int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
                        const float *comb, const float *fn, const float *scale, const float *base,
                        const uint16_t *norm_w, int64_t rows, int64_t logical_rows,

@@ -167,7 +167,7 @@ def call_fpp(lib, rows=4, logical=4, ws=fake(20), ws_bytes=None, **over):
              comb_out=fake(11), pre=None, mix=None)
     a.update(over)
     p = m.default_params()
-    wsb = lib.mhc_pre_workspace_bytes(rows) if ws_bytes is None else ws_bytes
+    wsb = lib.mhc_fused_post_pre_workspace_bytes(rows) if ws_bytes is None else ws_bytes
     return lib.mhc_fused_post_pre(a["R"], a["y"], a["post"], a["comb"], a["fn"], a["scale"],
                                   a["base"], a["w"], rows, logical, ctypes.byref(p), ws, wsb,
                                   a["R_out"], a["xn"], a["post_out"], a["comb_out"], a["pre"],
@@ -180,6 +180,9 @@ def test_fused_post_pre_validation(lib):
     assert call_fpp(lib, y=None) == ERR_NULL
     assert call_fpp(lib, comb_out=fake(11) + 4) == ERR_ALIGN
     assert call_fpp(lib, ws=None) == ERR_WORKSPACE
+    assert call_fpp(lib, ws_bytes=lib.mhc_pre_workspace_bytes(4)) == ERR_WORKSPACE   # no fn image room
+    assert (lib.mhc_fused_post_pre_workspace_bytes(4)
+            == lib.mhc_pre_workspace_bytes(4) + 640 * 48 * 64)
     assert call_fpp(lib, post_out=fake(2)) == ERR_OVERLAP      # next post on this post
     assert call_fpp(lib, R_out=fake(0)) == ERR_OVERLAP         # in-place residual
     assert call_fpp(lib, xn=fake(8)) == ERR_OVERLAP            # two outputs
