@@ -10,12 +10,16 @@
 // Unfused, R' is written by hc_post and read back by the stats; here the
 // stats take R' from shared memory where it was just formed, so for them R'
 // costs one write and no read.  The decomposition follows the stats kernel
-// (pre_stats.cu): a cluster of 16 CTAs owns a 128-row tile at a time, CTA s
-// owns hidden columns [320 s, 320 s + 320) of all four streams, and its fn
-// slice (bf16 hi + lo, 120 KB) stays in shared memory.  Per tile and CTA the
-// 320 columns go through in ten "half-sets" of 32 columns, double-buffered:
-//   * a TMA producer loads a half-set -- R_0..3 and y, 128 rows x 32
-//     columns each, 64-byte swizzle, 40 KB -- into a free buffer;
+// (pre_stats.cu): a cluster of 16 CTAs owns a 128-row tile at a time and CTA
+// s owns hidden columns [320 s, 320 s + 320) of all four streams.  Per tile
+// and CTA the 320 columns go through in ten "half-sets" of 32 columns, four
+// in flight:
+//   * a producer thread loads a half-set -- R_0..3 and y, 128 rows x 32
+//     columns each, 64-byte swizzle, 40 KB, by TMA, and the four streams' fn
+//     blocks for those columns (bf16 hi + lo, 12 KB) by bulk copy from an
+//     image of fn in the operand layout that fn_prep_sw64_kernel writes
+//     once per call -- into a free buffer (fn is not held in shared memory,
+//     which leaves room for four 52 KB buffers);
 //   * eight converter warps form R' in place (the same arithmetic as
 //     mhc_post, so R' has mhc_post's bits) and add its squares to the rows'
 //     sums of squares;
