@@ -286,9 +286,14 @@ def run_mhc(args):
         sample = M
         t0 = time.perf_counter()
         v = oracle_rows_per_s(Rh, yh, W, sample, threads)
+        wall = time.perf_counter() - t0
+        # the single-threaded oracle on the first 1024 rows (about a second)
+        one = oracle_rows_per_s(Rh, yh, W, min(M, 1024), 1)
         cpu = {"value": v, "unit": "rows/s", "cores": threads, "kind": "oracle",
                "sample": f"oracle pre+post on all {sample} rows of the M={M} workload "
-                         f"({time.perf_counter() - t0:.1f} s wall on {threads} threads)"}
+                         f"({wall:.1f} s wall on {threads} threads); single-threaded on "
+                         f"the first {min(M, 1024)} rows: {one:.0f} rows/s",
+               "single_thread_value": one}
     return finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, dist)
 
 
@@ -603,6 +608,105 @@ def run_op(args):
     print(json.dumps(line), flush=True)
 
 
+SWEEP = [(0, 128), (1, 1500), (2, 2048), (3, 4096), (4, 16384)]   # (seed, M)
+FLUSH_BYTES = 512 << 20                                           # > 129 MB of L2
+
+
+def run_sweep(args):
+    """mhc_pre + mhc_post at every prefill size (M = 128, 1500, 2048, 4096,
+    16384; seeds 0..4), one JSON line per size.  Before each timed step a
+    512 MB memset evicts L2, so R never starts L2-resident (fn and norm_w are
+    re-read from L2 or HBM as they fall); events bracket each step alone and
+    the line reports the median over the steps.  At M=4096 mhc_post is also
+    timed alone on a second-seed y."""
+    import torch
+    import hyper_connection_residual_mhc_gb300 as m
+    from hyper_connection_residual_mhc_gb300 import build as b
+    b.build()
+    m.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, peak_src = peaks()
+    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    steps = max(20, args.steps)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def per_step(fns):
+        """Median ms of each of fns (run back to back) and of their sum."""
+        for _ in range(args.warmup):
+            for f in fns:
+                f()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+              for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            for j, f in enumerate(fns):
+                f()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        parts = [statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev)
+                 for j in range(len(fns))]
+        total = statistics.median(e[0].elapsed_time(e[-1]) for e in ev)
+        return total, parts
+
+    for seed, M in SWEEP:
+        W = synth.weights(seed)
+        R = bf(synth.residual(seed, M))
+        y = bf(synth.sublayer_out(seed, M))
+        t_ = lambda a: torch.from_numpy(a).to(dev)
+        fn, scale, base, w = t_(W.fn), t_(W.scale), t_(W.base), bf(W.norm_w)
+        xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        post = torch.empty((M, HC), dtype=torch.float32, device=dev)
+        comb = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
+        R2 = torch.empty_like(R)
+        ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+
+        def pre():
+            m.mhc_pre(R, fn, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn, post=post,
+                      comb=comb, stream=stream)
+
+        def post_(yy=y):
+            m.mhc_post(R, yy, post, comb, logical_rows=M, out=R2, stream=stream)
+
+        with ClockSampler(0) as clk:
+            ms, (pre_ms, post_ms) = per_step([pre, post_])
+            extra = {}
+            if M == 4096:
+                y2 = bf(synth.sublayer_out(seed + 1, M))
+                alone, _ = per_step([lambda: post_(y2)])
+                extra = {"post_alone_ms": alone,
+                         "post_alone_gbs": M * POST_BYTES_ROW / (alone / 1e3) / 1e9}
+        nbytes = M * (PRE_BYTES_ROW + POST_BYTES_ROW) + PRE_BYTES_CALL
+        gbs = nbytes / (ms / 1e3) / 1e9
+        line = {
+            "metric": f"mHC pre+post rows/s and achieved HBM GB/s at M={M}",
+            "value": M / (ms / 1e3), "unit": "rows/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"M={M} rows: R[M,4,5120] bf16, fn[24,20480] f32, "
+                                   f"y[M,5120] bf16 (seed {seed}); one step = mhc_pre + "
+                                   "mhc_post; median of per-step event times",
+                       "op": "sweep", "rows": M,
+                       "l2": "512 MB memset before every timed step (outside the events)",
+                       "pre_ms": pre_ms, "post_ms": post_ms,
+                       "pre_gbs": (M * PRE_BYTES_ROW + PRE_BYTES_CALL) / (pre_ms / 1e3) / 1e9,
+                       "post_gbs": M * POST_BYTES_ROW / (post_ms / 1e3) / 1e9, **extra},
+            "roofline": {"bound": "hbm", "kernel": "mhc_pre+mhc_post", "achieved": gbs,
+                         "peak": hbm_peak, "peak_source": f"{peak_src} (hbm_gbs)",
+                         "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None,
+                         "algorithmic_bytes_per_launch": nbytes},
+            "gpu_launches": (PRE_LAUNCHES if M > 48 else 1) * steps + POST_LAUNCHES * steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+        del R, y, R2, xn
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -611,7 +715,7 @@ def main():
     ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["step", "hc_head", "latency", "fused_post_pre"],
+    ap.add_argument("--op", choices=["step", "hc_head", "latency", "fused_post_pre", "sweep"],
                     default="step",
                     help="step: mhc_pre + mhc_post (the headline); others time one entry "
                          "point alone")
@@ -625,6 +729,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "sweep":
+        run_sweep(args)
     elif args.op != "step":
         run_op(args)
     else:
