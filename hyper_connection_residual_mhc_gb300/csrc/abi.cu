@@ -182,7 +182,8 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
                                pre_out, mix_out, s);
     if (ce == cudaSuccess)
       ce = mhc::launch_combine_norm_sinkhorn(R, pre_ws, norm_w, p.norm_eps, logit_ws, comb,
-                                             p.hc_sinkhorn_eps, p.sinkhorn_iters, rows, x_norm, s);
+                                             p.hc_sinkhorn_eps, p.sinkhorn_iters, rows,
+                                             logical_rows, x_norm, s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
@@ -335,7 +336,8 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
                                     pre_ws, logit_ws, fnp, R_out, post_out, pre_out, mix_out, s);
     if (ce == cudaSuccess)
       ce = mhc::launch_combine_norm_sinkhorn(R_out, pre_ws, norm_w, p.norm_eps, logit_ws, comb_out,
-                                             p.hc_sinkhorn_eps, p.sinkhorn_iters, rows, x_norm, s);
+                                             p.hc_sinkhorn_eps, p.sinkhorn_iters, rows,
+                                             logical_rows, x_norm, s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
@@ -375,7 +377,7 @@ int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const fl
   float *pre_ws = static_cast<float *>(workspace);
   cudaError_t ce = mhc::launch_head_stats(R, fn, scale, base, rows, logical_rows, norm_eps,
                                           hc_eps, pre_ws, pre_out, mix_out, s);
-  if (ce == cudaSuccess) ce = mhc::launch_head_combine(R, pre_ws, rows, y, s);
+  if (ce == cudaSuccess) ce = mhc::launch_head_combine(R, pre_ws, rows, logical_rows, y, s);
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(kPostThreads)
 post_kernel(const uint4 *__restrict__ R, const uint4 *__restrict__ y,
             const float4 *__restrict__ post, const float4 *__restrict__ comb,
             uint4 *__restrict__ out, int64_t n_chunks) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = (int64_t)blockIdx.x * kPostThreads + threadIdx.x;
   if (t >= n_chunks) return;
   const int64_t row = t / kChunksPerStream;
@@ -49,15 +51,15 @@ post_kernel(const uint4 *__restrict__ R, const uint4 *__restrict__ y,
 }  // namespace
 
 cudaError_t launch_post(const uint16_t *R, const uint16_t *y, const float *post,
-                        const float *comb, int64_t rows, int64_t /*logical_rows*/,
+                        const float *comb, int64_t rows, int64_t logical_rows,
                         uint16_t *R_out, cudaStream_t s) {
   const int64_t n_chunks = rows * kChunksPerStream;
   const int64_t blocks = (n_chunks + kPostThreads - 1) / kPostThreads;
-  post_kernel<<<(unsigned)blocks, kPostThreads, 0, s>>>(
-      reinterpret_cast<const uint4 *>(R), reinterpret_cast<const uint4 *>(y),
-      reinterpret_cast<const float4 *>(post), reinterpret_cast<const float4 *>(comb),
-      reinterpret_cast<uint4 *>(R_out), n_chunks);
-  return cudaGetLastError();
+  return launch_pdl(post_kernel, dim3((unsigned)blocks), dim3(kPostThreads), 0, s, 1,
+                    use_pdl(logical_rows),
+                    reinterpret_cast<const uint4 *>(R), reinterpret_cast<const uint4 *>(y),
+                    reinterpret_cast<const float4 *>(post), reinterpret_cast<const float4 *>(comb),
+                    reinterpret_cast<uint4 *>(R_out), n_chunks);
 }
 
 }  // namespace mhc

@@ -163,6 +163,7 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
   tc_fence_after();
   cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
 
   // ---- roles -------------------------------------------------------------------
   if (warp == kProdWarp) {
@@ -406,6 +407,10 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
     }
   }
 
+  // this CTA's work is done: the next launch may start scheduling (earlier,
+  // its waiting CTAs would sit beside this persistent grid for its whole run)
+  pdl_trigger();
+
   // ---- teardown: no CTA leaves while its shared memory may still be addressed
   tc_fence_before();
   __syncthreads();
@@ -423,6 +428,8 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
 // (hi), row 24 + c = bf16(fn[c] - hi) (lo)
 __global__ void __launch_bounds__(256) fn_prep_sw64_kernel(const float *__restrict__ fn,
                                                             uint8_t *__restrict__ fnp) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * 256 + threadIdx.x;
   if (t >= kFnBlocks * kMix * 4) return;
   const int q = t & 3, c = (t >> 2) % kMix, kb = t / (4 * kMix);
@@ -517,8 +524,8 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   if (!encode_rows(&map_r, R, kK, rows) || !encode_rows(&map_y, y, kH, rows))
     return cudaErrorInvalidValue;
   constexpr int kPrepItems = kFnBlocks * kMix * 4;
-  fn_prep_sw64_kernel<<<(kPrepItems + 255) / 256, 256, 0, s>>>(fn, fnp);
-  e = cudaGetLastError();
+  e = launch_pdl(fn_prep_sw64_kernel, dim3((kPrepItems + 255) / 256), dim3(256), 0, s, 1,
+                 use_pdl(logical_rows), fn, fnp);
   if (e != cudaSuccess) return e;
   FusedArgs a;
   a.post_in = post;
@@ -533,19 +540,8 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   // grid from the chunk's row count only (per-row arithmetic never depends on it)
   const int64_t chunk_tiles = (logical_rows + kTile - 1) / kTile;
   const int clusters = (int)(chunk_tiles < max_clusters ? chunk_tiles : max_clusters);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  cfg.gridDim = dim3((unsigned)(clusters * kCl));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCl;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, post_pre_fused_kernel, map_r, map_y, a);
+  return launch_pdl(post_pre_fused_kernel, dim3((unsigned)(clusters * kCl)), dim3(kThreads),
+                    kSmemBytes, s, kCl, use_pdl(logical_rows), map_r, map_y, a);
 }
 
 cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset) {

@@ -139,6 +139,7 @@ pre_decode_kernel(const DecArgs a) {
   const int si = tid / kDQ, q = tid % kDQ;          // stream, 4-column group
   const int k0 = si * kH + (int)rank * kDHs + 4 * q;
   const int h0 = (int)rank * kDHs + 4 * q;          // threads tid < 80: their columns
+  pdl_wait();
   MHC_DTRACE(0);
 
   float f[kMix][4];
@@ -347,6 +348,8 @@ pre_decode_kernel(const DecArgs a) {
     }
     MHC_DTRACE(8);
   }
+  // the next launch may start scheduling once every CTA got here
+  pdl_trigger();
 }
 
 std::mutex g_dec_mu;
@@ -405,8 +408,9 @@ cudaError_t launch_pre_decode(const uint16_t *R, const float *fn, const float *s
   a.R = R; a.fn = fn; a.scale = scale; a.base = base; a.norm_w = norm_w; a.x_norm = x_norm;
   a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out; a.rows = rows;
   a.group = (int)grp; a.p = p;
-  pre_decode_kernel<<<clusters * kDCl, kDThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  // (the cluster shape is the kernel's compile-time __cluster_dims__)
+  return launch_pdl(pre_decode_kernel, dim3((unsigned)(clusters * kDCl)), dim3(kDThreads), 0, s, 1,
+                    use_pdl(logical_rows), a);
 }
 
 #ifdef MHC_TRACE

@@ -232,6 +232,8 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
                     const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out,
                     const float *__restrict__ logit, float *__restrict__ comb, float sink_eps,
                     int iters) {
+  pdl_wait();
+  pdl_trigger();
   // last rows first: after mhc_pre's stats launch the most recently read rows
   // are the ones still in L2
   const int64_t row = (int64_t)gridDim.x - 1 - blockIdx.x;
@@ -254,33 +256,30 @@ size_t pre_simt_workspace_bytes(int64_t rows) {
 }
 
 cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
-                                float norm_eps, int64_t rows, int64_t /*logical_rows*/,
+                                float norm_eps, int64_t rows, int64_t logical_rows,
                                 uint16_t *x_norm, cudaStream_t s) {
-  combine_norm_kernel<true, false><<<(unsigned)rows, kCnThreads, 0, s>>>(
-      reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
-      reinterpret_cast<const uint4 *>(norm_w), norm_eps, reinterpret_cast<uint4 *>(x_norm),
-      nullptr, nullptr, 0.f, 0);
-  return cudaGetLastError();
+  return launch_pdl(combine_norm_kernel<true, false>, dim3((unsigned)rows), dim3(kCnThreads), 0, s,
+                    1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
+                    reinterpret_cast<const uint4 *>(norm_w), norm_eps,
+                    reinterpret_cast<uint4 *>(x_norm), nullptr, nullptr, 0.f, 0);
 }
 
 cudaError_t launch_combine_norm_sinkhorn(const uint16_t *R, const float *pre,
                                          const uint16_t *norm_w, float norm_eps,
                                          const float *logit, float *comb, float sink_eps,
-                                         int iters, int64_t rows, uint16_t *x_norm,
-                                         cudaStream_t s) {
-  combine_norm_kernel<true, true><<<(unsigned)rows, kCnThreads + 32, 0, s>>>(
-      reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
-      reinterpret_cast<const uint4 *>(norm_w), norm_eps, reinterpret_cast<uint4 *>(x_norm),
-      logit, comb, sink_eps, iters);
-  return cudaGetLastError();
+                                         int iters, int64_t rows, int64_t logical_rows,
+                                         uint16_t *x_norm, cudaStream_t s) {
+  return launch_pdl(combine_norm_kernel<true, true>, dim3((unsigned)rows), dim3(kCnThreads + 32),
+                    0, s, 1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R),
+                    reinterpret_cast<const float4 *>(pre), reinterpret_cast<const uint4 *>(norm_w),
+                    norm_eps, reinterpret_cast<uint4 *>(x_norm), logit, comb, sink_eps, iters);
 }
 
-cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows, uint16_t *y,
-                                cudaStream_t s) {
-  combine_norm_kernel<false, false><<<(unsigned)rows, kCnThreads, 0, s>>>(
-      reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre), nullptr, 0.f,
-      reinterpret_cast<uint4 *>(y), nullptr, nullptr, 0.f, 0);
-  return cudaGetLastError();
+cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows,
+                                int64_t logical_rows, uint16_t *y, cudaStream_t s) {
+  return launch_pdl(combine_norm_kernel<false, false>, dim3((unsigned)rows), dim3(kCnThreads), 0, s,
+                    1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
+                    nullptr, 0.f, reinterpret_cast<uint4 *>(y), nullptr, nullptr, 0.f, 0);
 }
 
 cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *scale,

@@ -209,6 +209,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
   tc_fence_after();
   cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
 
   // fn columns of this CTA -> bf16 hi/lo B tiles (K-major, 128-byte swizzle),
   // written by the MMA, readout and owner warps while the producer starts
@@ -522,6 +523,10 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     }
   }
 
+  // this CTA's work is done: the next launch may start scheduling (earlier,
+  // its waiting CTAs would sit beside this persistent grid for its whole run)
+  pdl_trigger();
+
   // ---- teardown: no CTA leaves while its shared memory may still be addressed
   tc_fence_before();
   __syncthreads();
@@ -602,19 +607,8 @@ cudaError_t launch_stats(const uint16_t *R, const StatsArgs &a, int64_t logical_
   const int64_t chunk_tiles = (logical_rows + kTile - 1) / kTile;
   const int clusters = (int)(chunk_tiles < max_clusters ? chunk_tiles : max_clusters);
 
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
-  cfg.gridDim = dim3((unsigned)(clusters * kCl));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<NM>::kSmemBytes;
-  cfg.stream = s;
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kCl;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pre_stats_kernel<NM>, map, a);
+  return launch_pdl(pre_stats_kernel<NM>, dim3((unsigned)(clusters * kCl)), dim3(kThreads),
+                    Cfg<NM>::kSmemBytes, s, kCl, use_pdl(logical_rows), map, a);
 }
 
 }  // namespace
