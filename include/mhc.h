@@ -18,6 +18,12 @@
  *    cudaStream_t; NULL means the legacy default stream) and never
  *    synchronise.  Device-side faults surface at the caller's next
  *    synchronisation, as with any CUDA launch.
+ *  - For chunks of at most 2048 rows (logical_rows) the kernels are launched
+ *    with programmatic stream serialization: a kernel's blocks may be
+ *    scheduled before the previous work on the stream has finished, but each
+ *    waits for it to complete (griddepcontrol.wait) before touching memory,
+ *    so stream order holds for every caller.  It also holds under stream
+ *    capture.
  *  - `rows` is the number of rows this call processes (a row-range shard
  *    passes pointers already offset to its first row).  `logical_rows` is
  *    the row count of the whole chunk the rows belong to; launch heuristics
