@@ -537,8 +537,20 @@ def run_op(args):
         side = torch.cuda.Stream(dev)
 
         LM = args.logical_rows or M
+        if args.fused:
+            # one sublayer boundary of a decode loop: hc_post of this sublayer
+            # and hc_pre of the next in one call (gates from a pre of R)
+            m.mhc_pre(R, fn, scale, base, w, x_norm=xn, post=post, comb=comb)
+            po2, co2 = torch.empty_like(post), torch.empty_like(comb)
+            wsf = torch.empty((max(256, m.mhc_fused_post_pre_workspace_bytes(M)),),
+                              dtype=torch.uint8, device=dev)
 
         def launch(st):
+            if args.fused:
+                m.mhc_fused_post_pre(R, yv, post, comb, fn, scale, base, w, logical_rows=LM,
+                                     workspace=wsf, R_out=R2, x_norm=xn, post_out=po2,
+                                     comb_out=co2, stream=st)
+                return
             m.mhc_pre(R, fn, scale, base, w, logical_rows=LM, workspace=ws, x_norm=xn, post=post,
                       comb=comb, stream=st)
             m.mhc_post(R, yv, post, comb, logical_rows=LM, out=R2, stream=st)
@@ -565,17 +577,20 @@ def run_op(args):
             graph_us = timed(g.replay, args.steps)
         nbytes = M * (PRE_BYTES_ROW + POST_BYTES_ROW) + PRE_BYTES_CALL
         line = {
-            "metric": f"mhc_pre + mhc_post latency at M={M} rows (decode-size step)",
+            "metric": (f"mhc_fused_post_pre latency at M={M} rows (one decode sublayer boundary)"
+                       if args.fused else
+                       f"mhc_pre + mhc_post latency at M={M} rows (decode-size step)"),
             "value": graph_us, "unit": "us/step", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": graph_us / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"M={M} rows of R[M,4,5120] bf16 (seed {SEED}); inputs "
                                    "L2-resident between steps (decode-size, latency-bound)",
-                       "op": "latency", "rows": M, "logical_rows": LM, "eager_us": eager_us,
+                       "op": "latency", "fused": bool(args.fused), "rows": M,
+                       "logical_rows": LM, "eager_us": eager_us,
                        "graph_us": graph_us},
             "roofline": {"bound": "latency", "algorithmic_bytes_per_step": nbytes,
                          "achieved_gbs_graph": nbytes / (graph_us * 1e-6) / 1e9},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (3 if LM > 48 else (1 if args.fused else 2)) * args.steps,
         }
         print(json.dumps(line), flush=True)
         return
@@ -725,6 +740,8 @@ def main():
                     default="step",
                     help="step: mhc_pre + mhc_post (the headline); others time one entry "
                          "point alone")
+    ap.add_argument("--fused", action="store_true",
+                    help="--op latency: time mhc_fused_post_pre (one decode sublayer boundary)")
     ap.add_argument("--logical-rows", type=int, default=0,
                     help="--op latency: the chunk's row count (default: --rows)")
     ap.add_argument("--rows", type=int, default=ROWS,

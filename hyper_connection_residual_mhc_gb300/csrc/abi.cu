@@ -323,11 +323,11 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t ce;
   if (logical_rows <= mhc::kDecodeMaxRows) {
-    // decode-size chunk: hc_post, then the one-launch decode pre on R'
-    ce = mhc::launch_post(R, y, post, comb, rows, logical_rows, R_out, s);
-    if (ce == cudaSuccess)
-      ce = mhc::launch_pre_decode(R_out, fn, scale, base, norm_w, rows, logical_rows, p, x_norm,
-                                  post_out, comb_out, pre_out, mix_out, s);
+    // decode-size chunk: one launch, hc_post on the loaded columns and the
+    // decode pre on R'
+    ce = mhc::launch_post_pre_decode(R, y, post, comb, fn, scale, base, norm_w, rows,
+                                     logical_rows, p, R_out, x_norm, post_out, comb_out, pre_out,
+                                     mix_out, s);
   } else {
     float *pre_ws = static_cast<float *>(workspace);
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));

@@ -119,11 +119,49 @@ struct DecArgs {
   const uint16_t *norm_w;
   uint16_t *x_norm;
   float *post, *comb, *pre_out, *mix_out;
+  // kPost: hc_post of the previous sublayer first, x = R_out
+  const uint16_t *y;
+  const float *post_in, *comb_in;
+  uint16_t *R_out;
   int64_t rows;
   int group;          // rows per cluster pass (1..8)
   mhc_params p;
 };
 
+// kPost: the thread's 4 columns of stream si of R' = hc_post(R, y, post,
+// comb) for row `row`, written to R_out and returned as the pre's x.  Per
+// element: post_si * y, then one fma per stream j in order, one rounding --
+// the arithmetic of post_chunk, so R_out has mhc_post's bits.
+__device__ __forceinline__ uint2 post_cols(const DecArgs &a, int64_t row, int si, int k0, int h0) {
+  const uint16_t *rr = a.R + row * kK + h0;
+  uint2 rv[kHC];
+#pragma unroll
+  for (int j = 0; j < kHC; ++j) rv[j] = __ldg(reinterpret_cast<const uint2 *>(rr + j * kH));
+  const uint2 yv = __ldg(reinterpret_cast<const uint2 *>(a.y + row * kH + h0));
+  const float pv = __ldg(a.post_in + row * kHC + si);
+  float cb[kHC];
+#pragma unroll
+  for (int j = 0; j < kHC; ++j) cb[j] = __ldg(a.comb_in + row * kHC * kHC + j * kHC + si);
+  const float yf[4] = {__uint_as_float(yv.x << 16), __uint_as_float(yv.x & 0xFFFF0000u),
+                       __uint_as_float(yv.y << 16), __uint_as_float(yv.y & 0xFFFF0000u)};
+  float acc[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float s = pv * yf[e];
+#pragma unroll
+    for (int j = 0; j < kHC; ++j) {
+      const uint32_t w = (e < 2) ? rv[j].x : rv[j].y;
+      const float rf = (e & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+      s = fmaf(cb[j], rf, s);
+    }
+    acc[e] = s;
+  }
+  const uint2 o = make_uint2(pack2_rn(acc[0], acc[1]), pack2_rn(acc[2], acc[3]));
+  *reinterpret_cast<uint2 *>(a.R_out + row * kK + k0) = o;
+  return o;
+}
+
+template <bool kPost>
 __global__ void __cluster_dims__(kDCl, 1, 1) __launch_bounds__(kDThreads, 1)
 pre_decode_kernel(const DecArgs a) {
   __shared__ float red[kDWarps][kDRows][32];        // per-warp row partials
@@ -162,9 +200,13 @@ pre_decode_kernel(const DecArgs a) {
     const int nr = (int)(a.rows - row0 < G ? a.rows - row0 : G);
     uint2 xr[kDRows];
 #pragma unroll
-    for (int r = 0; r < kDRows; ++r)
-      xr[r] = r < nr ? __ldg(reinterpret_cast<const uint2 *>(a.R + (row0 + r) * kK + k0))
-                     : make_uint2(0u, 0u);
+    for (int r = 0; r < kDRows; ++r) {
+      if constexpr (kPost)
+        xr[r] = r < nr ? post_cols(a, row0 + r, si, k0, h0) : make_uint2(0u, 0u);
+      else
+        xr[r] = r < nr ? __ldg(reinterpret_cast<const uint2 *>(a.R + (row0 + r) * kK + k0))
+                       : make_uint2(0u, 0u);
+    }
     MHC_DTRACE(1);
 
     // ---- 1. partials (row loops unrolled with a uniform guard, so the
@@ -353,17 +395,18 @@ pre_decode_kernel(const DecArgs a) {
 }
 
 std::mutex g_dec_mu;
-int g_dec_clusters[64];   // per device: co-resident clusters (0: not configured)
+int g_dec_clusters[2][64];   // [kPost][device]: co-resident clusters (0: not configured)
 
+template <bool kPost>
 cudaError_t dec_configure(int dev, int *ncl) {
   std::lock_guard<std::mutex> lock(g_dec_mu);
-  if (g_dec_clusters[dev] > 0) {
-    *ncl = g_dec_clusters[dev];
+  if (g_dec_clusters[kPost][dev] > 0) {
+    *ncl = g_dec_clusters[kPost][dev];
     return cudaSuccess;
   }
   // a cluster of 16 is a non-portable size
-  cudaError_t e =
-      cudaFuncSetAttribute(pre_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaFuncSetAttribute(pre_decode_kernel<kPost>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
@@ -376,12 +419,34 @@ cudaError_t dec_configure(int dev, int *ncl) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, pre_decode_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, pre_decode_kernel<kPost>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
-  g_dec_clusters[dev] = n;
+  g_dec_clusters[kPost][dev] = n;
   *ncl = n;
   return cudaSuccess;
+}
+
+template <bool kPost>
+cudaError_t launch_decode(DecArgs a, int64_t logical_rows, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int ncl_max = 0;
+  e = dec_configure<kPost>(dev, &ncl_max);
+  if (e != cudaSuccess) return e;
+  // rows per cluster pass from the chunk's row count: spread the chunk over
+  // all co-resident clusters, at most 8 rows a pass (the per-row arithmetic
+  // does not depend on the grouping)
+  int64_t grp = (logical_rows + ncl_max - 1) / ncl_max;
+  grp = grp < 1 ? 1 : (grp > kDRows ? kDRows : grp);
+  const int64_t groups = (a.rows + grp - 1) / grp;
+  const int clusters = (int)(groups < ncl_max ? groups : ncl_max);
+  a.group = (int)grp;
+  // (the cluster shape is the kernel's compile-time __cluster_dims__)
+  return launch_pdl(pre_decode_kernel<kPost>, dim3((unsigned)(clusters * kDCl)), dim3(kDThreads),
+                    0, s, 1, use_pdl(logical_rows), a);
 }
 
 }  // namespace
@@ -391,26 +456,25 @@ cudaError_t launch_pre_decode(const uint16_t *R, const float *fn, const float *s
                               int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
                               float *post, float *comb, float *pre_out, float *mix_out,
                               cudaStream_t s) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int ncl_max = 0;
-  e = dec_configure(dev, &ncl_max);
-  if (e != cudaSuccess) return e;
-  // rows per cluster pass from the chunk's row count: spread the chunk over
-  // all co-resident clusters, at most 8 rows a pass
-  int64_t grp = (logical_rows + ncl_max - 1) / ncl_max;
-  grp = grp < 1 ? 1 : (grp > kDRows ? kDRows : grp);
-  const int64_t groups = (rows + grp - 1) / grp;
-  const int clusters = (int)(groups < ncl_max ? groups : ncl_max);
-  DecArgs a;
+  DecArgs a = {};
   a.R = R; a.fn = fn; a.scale = scale; a.base = base; a.norm_w = norm_w; a.x_norm = x_norm;
   a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out; a.rows = rows;
-  a.group = (int)grp; a.p = p;
-  // (the cluster shape is the kernel's compile-time __cluster_dims__)
-  return launch_pdl(pre_decode_kernel, dim3((unsigned)(clusters * kDCl)), dim3(kDThreads), 0, s, 1,
-                    use_pdl(logical_rows), a);
+  a.p = p;
+  return launch_decode<false>(a, logical_rows, s);
+}
+
+cudaError_t launch_post_pre_decode(const uint16_t *R, const uint16_t *y, const float *post_in,
+                                   const float *comb_in, const float *fn, const float *scale,
+                                   const float *base, const uint16_t *norm_w, int64_t rows,
+                                   int64_t logical_rows, const mhc_params &p, uint16_t *R_out,
+                                   uint16_t *x_norm, float *post, float *comb, float *pre_out,
+                                   float *mix_out, cudaStream_t s) {
+  DecArgs a = {};
+  a.R = R; a.fn = fn; a.scale = scale; a.base = base; a.norm_w = norm_w; a.x_norm = x_norm;
+  a.post = post; a.comb = comb; a.pre_out = pre_out; a.mix_out = mix_out; a.rows = rows;
+  a.y = y; a.post_in = post_in; a.comb_in = comb_in; a.R_out = R_out;
+  a.p = p;
+  return launch_decode<true>(a, logical_rows, s);
 }
 
 #ifdef MHC_TRACE

@@ -241,8 +241,9 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
  * kernel's operand image, then one launch computes R_out, writes it once and
  * feeds it straight to the tensor-core stats (R_out is never read back for
  * them), then the pre pass's streaming combine + RMSNorm (with the Sinkhorn)
- * reads R_out.  Decode-size chunks (<= 48 rows): mhc_post
- * then the decode-size mhc_pre.
+ * reads R_out.  Decode-size chunks (<= 48 rows): one launch of the decode
+ * kernel that forms R_out on the columns it loads and runs mhc_pre on it
+ * (R_out and every output bit-identical to mhc_post then mhc_pre).
  *
  * Arguments
  *   R, y, post, comb        as for mhc_post (post [rows, 4] and comb

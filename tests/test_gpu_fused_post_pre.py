@@ -111,6 +111,24 @@ def test_fused_R_out_has_mhc_post_bits(torch, mhc, oracle_mod):
     assert torch.equal(g["R_out"], ref)
 
 
+@pytest.mark.parametrize("rows", [1, 7, 48])
+def test_fused_decode_sizes_equal_post_then_pre_bits(torch, mhc, oracle_mod, rows):
+    # at decode sizes the fused call is one launch (hc_post on the loaded
+    # columns, then the decode pre on R'); it must give exactly what
+    # mhc_post followed by mhc_pre gives
+    c = Chain(torch, oracle_mod, rows, 400 + rows)
+    g = c.gpu(torch, mhc)
+    d = c.d
+    R2 = mhc.mhc_post(d["R"], d["y"], d["post"], d["comb"])
+    pre = torch.empty((rows, HC), dtype=torch.float32, device="cuda")
+    mix = torch.empty((rows, MIX), dtype=torch.float32, device="cuda")
+    xn, po, co = mhc.mhc_pre(R2, d["fn"], d["scale"], d["base"], d["w"], pre_out=pre, mix_out=mix)
+    torch.cuda.synchronize()
+    ref = {"R_out": R2, "x_norm": xn, "post": po, "comb": co, "pre": pre, "mix": mix}
+    for k, v in ref.items():
+        assert torch.equal(g[k], v), k
+
+
 def test_fused_full_size_sampled_rows(torch, mhc, oracle_mod):
     rows = 16384
     R = synth.residual(4, rows)
