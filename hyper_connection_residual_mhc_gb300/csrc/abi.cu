@@ -119,11 +119,12 @@ int mhc_kernel_status_detail(uint32_t *where64) {
 
 int mhc_kernel_status(uint32_t *status, int reset) {
   if (!status) return MHC_ERR_NULL;
-  unsigned int w = 0, w2 = 0;
+  unsigned int w = 0, w2 = 0, w3 = 0;
   cudaError_t e = mhc::fused_error_word(&w, reset != 0);
   if (e == cudaSuccess) e = mhc::fused_post_pre_error_word(&w2, reset != 0);
+  if (e == cudaSuccess) e = mhc::head_error_word(&w3, reset != 0);
   if (e != cudaSuccess) return cuda_fail(e);
-  *status = w | w2;
+  *status = w | w2 | w3;
   return MHC_OK;
 }
 
@@ -374,10 +375,18 @@ int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const fl
   }
   if (int e = check_device()) return e;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float *pre_ws = static_cast<float *>(workspace);
-  cudaError_t ce = mhc::launch_head_stats(R, fn, scale, base, rows, logical_rows, norm_eps,
-                                          hc_eps, pre_ws, pre_out, mix_out, s);
-  if (ce == cudaSuccess) ce = mhc::launch_head_combine(R, pre_ws, rows, logical_rows, y, s);
+  cudaError_t ce;
+  if (logical_rows <= mhc::kHeadOnePassMaxRows) {
+    // small chunk: one pass over R on the CUDA cores (no workspace used)
+    ce = mhc::launch_head_onepass(R, fn, scale, base, rows, logical_rows, norm_eps, hc_eps, y,
+                                  pre_out, mix_out, s);
+  } else {
+    // tensor-core stats (gates to the workspace), then a streaming combine
+    float *pre_ws = static_cast<float *>(workspace);
+    ce = mhc::launch_head_stats(R, fn, scale, base, rows, logical_rows, norm_eps, hc_eps, pre_ws,
+                                pre_out, mix_out, s);
+    if (ce == cudaSuccess) ce = mhc::launch_head_combine(R, pre_ws, rows, logical_rows, y, s);
+  }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 

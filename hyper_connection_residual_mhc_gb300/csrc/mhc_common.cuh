@@ -181,6 +181,16 @@ cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *s
                               const float *base, int64_t rows, int64_t logical_rows,
                               float norm_eps, float hc_eps, float *pre_ws, float *pre_out,
                               float *mix_out, cudaStream_t s);
+// all of hc_head in one pass over R (head_onepass.cu): 4-CTA clusters, fp32
+// projections on the CUDA cores, the combine from shared memory.  It is
+// latency-bound (a 4-row tile per ~4 us per cluster), so it serves chunks of
+// up to 256 rows, where it takes ~6 us against ~12.5 us for the two launches
+constexpr int64_t kHeadOnePassMaxRows = 256;
+cudaError_t launch_head_onepass(const uint16_t *R, const float *fn, const float *scale,
+                                const float *base, int64_t rows, int64_t logical_rows,
+                                float norm_eps, float hc_eps, uint16_t *y, float *pre_out,
+                                float *mix_out, cudaStream_t s);
+cudaError_t head_error_word(unsigned int *out, bool reset);
 // y = bf16(sum_i pre_i R_i), one block per row (hc_head's combine)
 cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows,
                                 int64_t logical_rows, uint16_t *y, cudaStream_t s);

@@ -281,8 +281,14 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
  *   pre[i] = sigmoid(mix[i] * scale[0] + base[i]) + hc_eps
  *   y[m,h] = bf16( sum_i pre[i] * R[m, i, h] )     (fp32 sum, one rounding)
  *
- * Two launches: mhc_pre's tensor-core stats kernel built for 4 mixes (the
- * gates go to the workspace), then a streaming combine.
+ * Chunks of more than 256 rows (logical_rows): two launches, mhc_pre's
+ * tensor-core stats kernel built for 4 mixes (the gates go to the
+ * workspace), then a streaming combine.  Chunks of up to 256 rows: one
+ * launch of 4-CTA clusters that forms the 4 dots in fp32 on the CUDA cores
+ * and combines each row from shared memory, reading R once (the workspace
+ * is then not used, but must still be passed).  The two paths form the dots
+ * differently and agree to the gate tolerance; every row range of a chunk
+ * gives the whole-chunk bits.
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual after the last layer

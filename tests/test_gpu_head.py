@@ -94,9 +94,9 @@ def test_hc_head_full_size_sampled_rows(torch, mhc, oracle_mod, rows):
     _check(torch, y, pre, mix, R[idx], o, idx)
 
 
-def test_hc_head_row_shards_and_repeat_are_bit_exact(torch, mhc):
-    rows = 2048
-    R = synth.residual(WL[rows].seed, rows)
+@pytest.mark.parametrize("rows", [256, 2048])    # the one-pass and the two-launch path
+def test_hc_head_row_shards_and_repeat_are_bit_exact(torch, mhc, rows):
+    R = synth.residual(WL[rows].seed if rows in WL else 50, rows)
     hw = synth.head_weights(2)
     dR = _dev_bf16(torch, R)
     full = _run(torch, mhc, dR, hw)
@@ -112,8 +112,10 @@ def test_hc_head_row_shards_and_repeat_are_bit_exact(torch, mhc):
 
 def test_hc_head_gates_equal_pre_pass_gates(torch, mhc):
     # with hc_head's parameters set to the layer's first 4 fn rows, scale[0]
-    # and base[0:4] (norm_eps = rms_eps, hc_eps = hc_pre_eps), the 4-mix
-    # kernel must give the same gates as the 24-mix one to fp32 rounding
+    # and base[0:4] (norm_eps = rms_eps, hc_eps = hc_pre_eps), hc_head's pre
+    # gates are the pre pass's pre gates.  The two kernels form the dots
+    # differently (fp32 on the CUDA cores; bf16 hi/lo on the tensor cores),
+    # so they agree to the gate tolerance both meet against the oracle.
     rows = 300
     R = synth.residual(6, rows)
     W = synth.weights(6)
@@ -125,7 +127,7 @@ def test_hc_head_gates_equal_pre_pass_gates(torch, mhc):
     mhc.mhc_pre(dR, _dev_f32(torch, W.fn), _dev_f32(torch, W.scale), _dev_f32(torch, W.base),
                 _dev_bf16(torch, W.norm_w), pre_out=pre_p)
     d = (pre_h - pre_p).abs().max().item()
-    assert d <= 2e-7, d
+    assert d <= 1e-6, d
 
 
 def test_hc_head_validation(torch, mhc):
