@@ -1,5 +1,5 @@
-// pre_decode.cu -- mhc_pre for decode-size chunks (a few to a few hundred
-// rows) in a single launch.
+// pre_decode.cu -- mhc_pre (and mhc_fused_post_pre) for decode-size chunks
+// (up to 48 rows) in a single launch.
 //
 // Definitions: deepseek_v4.py (sglang), DeepseekV4DecoderLayer.hc_pre
 // (hc_pre_torch_impl: rsqrt of mean(x^2) + rms_eps, mixes = (x @ fn^T) *
@@ -32,6 +32,12 @@
 // the co-resident clusters.  The barriers are the hardware cluster barrier;
 // every thread of every CTA arrives at each of them (no early exit), so each
 // completes.
+//
+// Built twice: kPost = false is mhc_pre; kPost = true is mhc_fused_post_pre
+// at these sizes (deepseek_v4.py, the use_fused_mhc_post_pre path): each
+// thread first forms its 4 columns of R' = hc_post(R, y, post, comb) from the
+// four streams and y at those columns, writes them to R_out, and runs the
+// pre on R' -- one launch, and R' is never read back.
 #include <mutex>
 
 #include "mhc_common.cuh"
