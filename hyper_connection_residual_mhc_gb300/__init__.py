@@ -66,6 +66,11 @@ SIGNATURES = {
     "mhc_fused_post_pre_workspace_bytes": (ctypes.c_size_t, [_i64]),
     "mhc_hc_head": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
                                    ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
+    "mhc_prepare_weights": (ctypes.c_int, [_vp, ctypes.POINTER(_vp), _vp]),
+    "mhc_release_weights": (ctypes.c_int, [_vp]),
+    "mhc_pre_prepared": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                        ctypes.POINTER(MhcParams), _vp, ctypes.c_size_t, _vp,
+                                        _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -161,9 +166,16 @@ def mhc_pre(R, fn, scale, base, norm_w, *, logical_rows=None, params=None, works
     Returns ``(x_norm [rows,5120] bf16, post [rows,4] f32, comb [rows,4,4] f32)``.
     """
     import torch
+    _need(fn, "fn", torch.float32, (MIX, K))
+    return _pre_call("mhc_pre", _ptr(fn), R, scale, base, norm_w, logical_rows, params, workspace,
+                     x_norm, post, comb, pre_out, mix_out, stream)
+
+
+def _pre_call(name, fn_arg, R, scale, base, norm_w, logical_rows, params, workspace, x_norm,
+              post, comb, pre_out, mix_out, stream):
+    import torch
     rows = int(R.shape[0])
     _need(R, "R", torch.bfloat16, (rows, HC, H))
-    _need(fn, "fn", torch.float32, (MIX, K))
     _need(scale, "scale", torch.float32, (3,))
     _need(base, "base", torch.float32, (MIX,))
     _need(norm_w, "norm_w", torch.bfloat16, (H,))
@@ -183,13 +195,57 @@ def mhc_pre(R, fn, scale, base, norm_w, *, logical_rows=None, params=None, works
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     p = default_params() if params is None else params
-    code = lib().mhc_pre(
-        _ptr(R), _ptr(fn), _ptr(scale), _ptr(base), _ptr(norm_w), rows,
+    code = getattr(lib(), name)(
+        _ptr(R), fn_arg, _ptr(scale), _ptr(base), _ptr(norm_w), rows,
         rows if logical_rows is None else int(logical_rows), ctypes.byref(p),
         _ptr(workspace), ws_bytes, _ptr(x_norm), _ptr(post), _ptr(comb), _ptr(pre_out),
         _ptr(mix_out), _stream(stream))
-    _check("mhc_pre", code)
+    _check(name, code)
     return x_norm, post, comb
+
+
+class Weights:
+    """A prepared-weights handle (mhc_prepare_weights in include/mhc.h); freed by
+    release() or when the object is collected."""
+
+    def __init__(self, handle):
+        self._h = handle
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("the prepared weights were released")
+        return self._h
+
+    def release(self):
+        if self._h is not None:
+            h, self._h = self._h, None
+            _check("mhc_release_weights", lib().mhc_release_weights(h))
+
+    def __del__(self):
+        try:
+            self.release()
+        except Exception:
+            pass
+
+
+def mhc_prepare_weights(fn, *, stream=None) -> Weights:
+    """fn [24, 20480] f32 -> a handle holding fn's copy and the stats kernel's
+    operand image (see mhc_prepare_weights in include/mhc.h)."""
+    import torch
+    _need(fn, "fn", torch.float32, (MIX, K))
+    h = ctypes.c_void_p()
+    _check("mhc_prepare_weights", lib().mhc_prepare_weights(_ptr(fn), ctypes.byref(h),
+                                                            _stream(stream)))
+    return Weights(h.value)
+
+
+def mhc_pre_prepared(R, weights, scale, base, norm_w, *, logical_rows=None, params=None,
+                     workspace=None, x_norm=None, post=None, comb=None, pre_out=None,
+                     mix_out=None, stream=None):
+    """mhc_pre with fn from a prepared-weights handle (bit-identical to mhc_pre)."""
+    return _pre_call("mhc_pre_prepared", weights.handle, R, scale, base, norm_w, logical_rows,
+                     params, workspace, x_norm, post, comb, pre_out, mix_out, stream)
 
 
 def mhc_pre_noalloc_max_rows() -> int:

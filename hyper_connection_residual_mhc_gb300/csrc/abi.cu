@@ -81,6 +81,7 @@ const char *mhc_strerror(int code) {
     case MHC_ERR_DEVICE: return "the current device is not an sm_103 GPU";
     case MHC_ERR_SCRATCH_LIMIT:
       return "rows exceed mhc_pre_noalloc's fixed scratch (see mhc_pre_noalloc_max_rows)";
+    case MHC_ERR_ALLOC: return "a device allocation failed (mhc_prepare_weights)";
     default: return "unknown libmhc error code";
   }
 }
@@ -128,10 +129,13 @@ int mhc_kernel_status(uint32_t *status, int reset) {
   return MHC_OK;
 }
 
-int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float *base,
-            const uint16_t *norm_w, int64_t rows, int64_t logical_rows, const mhc_params *p_in,
-            void *workspace, size_t workspace_bytes, uint16_t *x_norm, float *post,
-            float *comb, float *pre_out, float *mix_out, void *stream) {
+namespace {
+// mhc_pre and mhc_pre_prepared: fn is the fp32 weight (the caller's, or the
+// handle's copy); fn_img is NULL or the handle's operand image
+int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const float *scale,
+             const float *base, const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+             const mhc_params *p_in, void *workspace, size_t workspace_bytes, uint16_t *x_norm,
+             float *post, float *comb, float *pre_out, float *mix_out, void *stream) {
   mhc_params p;
   if (p_in) p = *p_in; else mhc_default_params(&p);
   if (int e = check_rows(rows, logical_rows)) return e;
@@ -179,14 +183,83 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
                                 comb, pre_out, mix_out, s);
   } else {
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
-    ce = mhc::launch_pre_stats(R, fn, scale, base, rows, logical_rows, p, pre_ws, logit_ws, post,
-                               pre_out, mix_out, s);
+    ce = mhc::launch_pre_stats(R, fn, fn_img, scale, base, rows, logical_rows, p, pre_ws, logit_ws,
+                               post, pre_out, mix_out, s);
     if (ce == cudaSuccess)
       ce = mhc::launch_combine_norm_sinkhorn(R, pre_ws, norm_w, p.norm_eps, logit_ws, comb,
                                              p.hc_sinkhorn_eps, p.sinkhorn_iters, rows,
                                              logical_rows, x_norm, s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+}  // namespace
+
+int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float *base,
+            const uint16_t *norm_w, int64_t rows, int64_t logical_rows, const mhc_params *p,
+            void *workspace, size_t workspace_bytes, uint16_t *x_norm, float *post,
+            float *comb, float *pre_out, float *mix_out, void *stream) {
+  return pre_impl(R, fn, nullptr, scale, base, norm_w, rows, logical_rows, p, workspace,
+                  workspace_bytes, x_norm, post, comb, pre_out, mix_out, stream);
+}
+
+// ---- prepared weights --------------------------------------------------------------
+struct mhc_weights {
+  int device;
+  float *fn32;      // device copy of fn [24, 20480] fp32 (decode path)
+  uint8_t *img;     // the stats kernel's bf16 hi/lo B-tile image of all 16 cluster ranks
+};
+
+int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream) {
+  if (!fn || !out) return MHC_ERR_NULL;
+  *out = nullptr;
+  if (!aligned16(fn)) return MHC_ERR_ALIGN;
+  if (int e = check_device()) return e;
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  const size_t fn_bytes = (size_t)MHC_MIX * MHC_K * sizeof(float);
+  mhc_weights *w = new mhc_weights{dev, nullptr, nullptr};
+  ce = cudaMalloc(reinterpret_cast<void **>(&w->fn32), fn_bytes);
+  if (ce == cudaSuccess) ce = cudaMalloc(reinterpret_cast<void **>(&w->img), mhc::fn_img_bytes());
+  if (ce != cudaSuccess) {
+    cudaFree(w->fn32);
+    cudaFree(w->img);
+    delete w;
+    cuda_fail(ce);
+    return MHC_ERR_ALLOC;
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ce = cudaMemcpyAsync(w->fn32, fn, fn_bytes, cudaMemcpyDeviceToDevice, s);
+  if (ce == cudaSuccess) ce = mhc::launch_fn_img_prep(fn, w->img, s);
+  if (ce != cudaSuccess) {
+    cudaFree(w->fn32);
+    cudaFree(w->img);
+    delete w;
+    return cuda_fail(ce);
+  }
+  *out = w;
+  return MHC_OK;
+}
+
+int mhc_release_weights(mhc_weights *w) {
+  if (!w) return MHC_OK;
+  cudaError_t e1 = cudaFree(w->fn32), e2 = cudaFree(w->img);
+  delete w;
+  if (e1 != cudaSuccess) return cuda_fail(e1);
+  if (e2 != cudaSuccess) return cuda_fail(e2);
+  return MHC_OK;
+}
+
+int mhc_pre_prepared(const uint16_t *R, const mhc_weights *w, const float *scale,
+                     const float *base, const uint16_t *norm_w, int64_t rows,
+                     int64_t logical_rows, const mhc_params *p, void *workspace,
+                     size_t workspace_bytes, uint16_t *x_norm, float *post, float *comb,
+                     float *pre_out, float *mix_out, void *stream) {
+  if (!w) return MHC_ERR_NULL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != w->device) return MHC_ERR_DEVICE;
+  return pre_impl(R, w->fn32, w->img, scale, base, norm_w, rows, logical_rows, p, workspace,
+                  workspace_bytes, x_norm, post, comb, pre_out, mix_out, stream);
 }
 
 int64_t mhc_pre_noalloc_max_rows(void) { return mhc::noalloc_max_rows(); }

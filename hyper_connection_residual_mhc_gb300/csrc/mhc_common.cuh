@@ -164,10 +164,17 @@ cudaError_t launch_post_pre_decode(const uint16_t *R, const uint16_t *y, const f
 // tensor-core stats half of mhc_pre (cluster of 16 CTAs): writes the pre gates
 // to pre_ws [rows, 4] and the comb logits to logit_ws [rows, 16] for the
 // combine launch, and post (+ pre_out, mix_out)
-cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
-                             const float *base, int64_t rows, int64_t logical_rows,
-                             const mhc_params &p, float *pre_ws, float *logit_ws, float *post,
-                             float *pre_out, float *mix_out, cudaStream_t s);
+// (fn_img: NULL, or the prepared-weights image of fn_img_bytes(), which the
+// kernel then bulk-copies instead of converting fn)
+cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const uint8_t *fn_img,
+                             const float *scale, const float *base, int64_t rows,
+                             int64_t logical_rows, const mhc_params &p, float *pre_ws,
+                             float *logit_ws, float *post, float *pre_out, float *mix_out,
+                             cudaStream_t s);
+// prepared weights: fn [24, 20480] fp32 -> the stats kernel's bf16 hi/lo
+// B-tile image of all 16 cluster ranks (fn_img_bytes() bytes)
+size_t fn_img_bytes();
+cudaError_t launch_fn_img_prep(const float *fn, uint8_t *img, cudaStream_t s);
 // combine + RMSNorm with a fifth warp per row block for the Sinkhorn of the
 // comb logits (writes comb [rows, 4, 4])
 cudaError_t launch_combine_norm_sinkhorn(const uint16_t *R, const float *pre,

@@ -151,8 +151,33 @@ struct Cfg {
   static_assert(NM % 4 == 0 && (2 * NM) % 8 == 0, "pushes of 4 mixes; padding starts on an 8-row group");
 };
 
+// fn's 8 consecutive k of mix c -> the bf16 hi and lo halves (hi = bf16(f),
+// lo = bf16(f - hi), both round-to-nearest-even), written as two 16-byte
+// chunks q of B-tile rows c and c + NM (K-major, 128-byte swizzle).  The
+// stats kernel's loaders and the prepared-weights image use this one routine,
+// so both give the same bits.
+template <int NM>
+__device__ __forceinline__ void fn_item_to_tile(const float4 &f0, const float4 &f1, int c, int q,
+                                                uint8_t *tile) {
+  const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * e]);
+    const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * e + 1]);
+    hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
+    lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
+  }
+  const int nh = c, nlo = c + NM;
+  *reinterpret_cast<uint4 *>(tile + (nh >> 3) * 1024 + (nh & 7) * 128 + ((q ^ (nh & 7)) << 4)) =
+      make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4 *>(tile + (nlo >> 3) * 1024 + (nlo & 7) * 128 + ((q ^ (nlo & 7)) << 4)) =
+      make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
 struct StatsArgs {
   const float *fn;
+  const uint8_t *fn_img;   // pre pass only, or NULL: fn already in this kernel's B-tile image
   const float *scale;
   const float *base;
   float *pre_ws;     // [rows, 4] pre gates for the combine launch
@@ -200,7 +225,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     mbar_init(bar(B_GALL), kReadN);
     mbar_init(bar(B_OPULL), kOwnerN);
     mbar_init(bar(B_DRAIN), 1);
-    mbar_init(bar(B_FNREADY), kWarps - 1 - kRowN);
+    mbar_init(bar(B_FNREADY), a.fn_img ? 1 : kWarps - 1 - kRowN);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -215,7 +240,18 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
   // written by the MMA, readout and owner warps while the producer starts
   // streaming R and the row warps wait for it:
   // k-block j covers k = (j%4)*5120 + 320*crank + 64*(j/4) + [0, 64)
-  if (warp != kProducerWarp && !(warp >= kRow0 && warp < kRow0 + kRowN)) {
+  // With prepared weights the same bytes come from the image, in four bulk
+  // copies.
+  if (a.fn_img) {
+    if (warp == kMmaWarp && lane == 0) {
+      constexpr uint32_t kImg = kKb * C::kFnBlkBytes, kPart = kImg / 4;
+      static_assert(kImg % 64 == 0 && kImg < (1u << 20), "bulk copies of 16-byte multiples");
+      mbar_expect_tx(bar(B_FNREADY), kImg);
+      const uint8_t *src = a.fn_img + (size_t)crank * kImg;
+      for (int i = 0; i < 4; ++i)
+        bulk_load(sb + C::kOffFn + i * kPart, src + i * kPart, kPart, bar(B_FNREADY));
+    }
+  } else if (warp != kProducerWarp && !(warp >= kRow0 && warp < kRow0 + kRowN)) {
     // 10 loader warps; loads of 8 items are issued before any is converted
     const int loader = warp == kMmaWarp ? 0 : (warp < kRow0 ? warp - 1 : warp - kRowN - 1);
     const int lt = loader * 32 + lane, nl = (kWarps - 1 - kRowN) * 32;
@@ -246,21 +282,7 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         const int item = base + u * nl;
         if (item >= kItems) continue;
         const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
-        const float f[8] = {f0[u].x, f0[u].y, f0[u].z, f0[u].w, f1[u].x, f1[u].y, f1[u].z, f1[u].w};
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * e]);
-          const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * e + 1]);
-          hw[e] = pack2_rn(__bfloat162float(h0), __bfloat162float(h1));
-          lw[e] = pack2_rn(f[2 * e] - __bfloat162float(h0), f[2 * e + 1] - __bfloat162float(h1));
-        }
-        uint8_t *tile = sm + C::kOffFn + j * C::kFnBlkBytes;
-        const int nh = c, nlo = c + NM;
-        *reinterpret_cast<uint4 *>(tile + (nh >> 3) * 1024 + (nh & 7) * 128 + ((q ^ (nh & 7)) << 4)) =
-            make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4 *>(tile + (nlo >> 3) * 1024 + (nlo & 7) * 128 +
-                                   ((q ^ (nlo & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        fn_item_to_tile<NM>(f0[u], f1[u], c, q, sm + C::kOffFn + j * C::kFnBlkBytes);
       }
     }
     // generic-proxy writes -> visible to the tensor core (async proxy)
@@ -330,6 +352,8 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     if (lane == 0) tc_commit(bar(B_DRAIN));
     __syncwarp();
     drain1(bar(B_DRAIN), 0);
+    // the fn image copies have landed before the CTA may leave
+    if (a.fn_img) drain1(bar(B_FNREADY), 0);
     __syncwarp();
   } else if (warp >= kRow0 && warp < kRow0 + kRowN) {
     // ---- row warps: one thread per tile row; sum x^2 from every stage -------
@@ -613,12 +637,42 @@ cudaError_t launch_stats(const uint16_t *R, const StatsArgs &a, int64_t logical_
 
 }  // namespace
 
-cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const float *scale,
-                             const float *base, int64_t rows, int64_t logical_rows,
-                             const mhc_params &p, float *pre_ws, float *logit_ws, float *post,
-                             float *pre_out, float *mix_out, cudaStream_t s) {
+// ---- prepared weights: fn's B-tile image of every cluster rank ---------------------
+namespace {
+constexpr int kImgRankBytes = kKb * Cfg<kMix>::kFnBlkBytes;      // 122880
+constexpr int kImgItemsPerRank = kMix * kKb * 8;                  // 3840 items of 8 k
+
+__global__ void __launch_bounds__(256) fn_img_prep_kernel(const float *__restrict__ fn,
+                                                          uint8_t *__restrict__ img) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x * 256 + threadIdx.x;
+  if (t >= kCl * kImgItemsPerRank) return;
+  const int rank = t / kImgItemsPerRank, item = t % kImgItemsPerRank;
+  const int q = item & 7, j = (item >> 3) % kKb, c = item / (8 * kKb);
+  const int k0 = (j & 3) * kH + rank * kHs + (j >> 2) * kBk + 8 * q;
+  const float4 f0 = __ldg(reinterpret_cast<const float4 *>(fn + (int64_t)c * kK + k0));
+  const float4 f1 = __ldg(reinterpret_cast<const float4 *>(fn + (int64_t)c * kK + k0 + 4));
+  fn_item_to_tile<kMix>(f0, f1, c, q,
+                        img + (size_t)rank * kImgRankBytes + j * Cfg<kMix>::kFnBlkBytes);
+}
+}  // namespace
+
+size_t fn_img_bytes() { return (size_t)kCl * kImgRankBytes; }
+
+cudaError_t launch_fn_img_prep(const float *fn, uint8_t *img, cudaStream_t s) {
+  constexpr int kItems = kCl * kImgItemsPerRank;
+  return launch_pdl(fn_img_prep_kernel, dim3((kItems + 255) / 256), dim3(256), 0, s, 1, false,
+                    fn, img);
+}
+
+cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const uint8_t *fn_img,
+                             const float *scale, const float *base, int64_t rows,
+                             int64_t logical_rows, const mhc_params &p, float *pre_ws,
+                             float *logit_ws, float *post, float *pre_out, float *mix_out,
+                             cudaStream_t s) {
   StatsArgs a;
-  a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
+  a.fn = fn; a.fn_img = fn_img; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
   a.post = post; a.logit_ws = logit_ws; a.pre_out = pre_out; a.mix_out = mix_out;
   a.rows = rows;
   a.num_tiles = (int)((rows + kTile - 1) / kTile);
@@ -632,7 +686,7 @@ cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *s
                               float norm_eps, float hc_eps, float *pre_ws, float *pre_out,
                               float *mix_out, cudaStream_t s) {
   StatsArgs a;
-  a.fn = fn; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
+  a.fn = fn; a.fn_img = nullptr; a.scale = scale; a.base = base; a.pre_ws = pre_ws;
   a.post = nullptr; a.logit_ws = nullptr; a.pre_out = pre_out; a.mix_out = mix_out;
   a.rows = rows;
   a.num_tiles = (int)((rows + kTile - 1) / kTile);

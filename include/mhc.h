@@ -65,6 +65,7 @@ extern "C" {
 #define MHC_ERR_CUDA (-7)        /* a CUDA call failed (see mhc_last_cuda_error) */
 #define MHC_ERR_DEVICE (-8)      /* current device is not an sm_103 GPU */
 #define MHC_ERR_SCRATCH_LIMIT (-9) /* rows above mhc_pre_noalloc's fixed scratch size */
+#define MHC_ERR_ALLOC (-10)      /* a device allocation failed (mhc_prepare_weights) */
 
 /* Scalars of the split/Sinkhorn and the two RMS normalisations.
  * deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre passes rms_eps =
@@ -227,6 +228,42 @@ int mhc_post(const uint16_t *R, const uint16_t *y, const float *post, const floa
 int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
                      float norm_eps, int64_t rows, int64_t logical_rows, uint16_t *x_norm,
                      void *stream);
+
+/*
+ * Prepared weights -- a layer's fn converted once, at load time, into what the
+ * kernels read, so that mhc_pre does not convert it at every call.
+ *
+ * deepseek_v4.py: DeepseekV4DecoderLayer.refresh_mhc_norm_weight_cache casts
+ * the norm weights once so the fused path does not cast per forward, and
+ * DeepseekV4ForCausalLM._prewarm_mhc_pre_kernels sets mhc_pre up at load
+ * time; the handle does the same for fn.
+ *
+ * mhc_prepare_weights(fn, &w, stream)
+ *   fn [24, 20480] fp32, device, 16-byte aligned (hc_fn of one sublayer).
+ *   Allocates device memory on the current device (about 3.9 MB, the only
+ *   allocation libmhc makes) and enqueues on `stream`: a copy of fn, and
+ *   fn's bf16 hi/lo operand image for every CTA of the tensor-core stats
+ *   kernel (the same bits the kernel would form itself).  The handle may be
+ *   used by calls enqueued after it on `stream`, or on any stream once the
+ *   caller has ordered them after it; fn itself may be freed or changed
+ *   afterwards.  Returns MHC_OK, MHC_ERR_NULL, MHC_ERR_ALIGN, MHC_ERR_DEVICE,
+ *   MHC_ERR_ALLOC (then *out = NULL) or MHC_ERR_CUDA.
+ * mhc_release_weights(w)
+ *   Frees the handle (NULL is a no-op).  No work using it may still be
+ *   pending.
+ * mhc_pre_prepared(R, w, scale, base, norm_w, ...)
+ *   mhc_pre with fn taken from the handle: the same arguments, checks and
+ *   outputs, bit-identical to mhc_pre on the fn the handle was made from.
+ *   MHC_ERR_DEVICE if the current device is not the handle's.
+ */
+typedef struct mhc_weights mhc_weights;
+int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream);
+int mhc_release_weights(mhc_weights *w);
+int mhc_pre_prepared(const uint16_t *R, const mhc_weights *w, const float *scale,
+                     const float *base, const uint16_t *norm_w, int64_t rows,
+                     int64_t logical_rows, const mhc_params *p, void *workspace,
+                     size_t workspace_bytes, uint16_t *x_norm, float *post, float *comb,
+                     float *pre_out, float *mix_out, void *stream);
 
 /*
  * mhc_fused_post_pre -- hc_post of one sublayer and hc_pre of the next on its

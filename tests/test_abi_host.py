@@ -187,3 +187,18 @@ def test_fused_post_pre_validation(lib):
     assert call_fpp(lib, R_out=fake(0)) == ERR_OVERLAP         # in-place residual
     assert call_fpp(lib, xn=fake(8)) == ERR_OVERLAP            # two outputs
     assert call_fpp(lib, ws=fake(1)) == ERR_OVERLAP            # workspace on y
+
+
+def test_prepared_weights_host_checks(lib):
+    import hyper_connection_residual_mhc_gb300 as m
+    h = ctypes.c_void_p(123)
+    assert lib.mhc_prepare_weights(None, ctypes.byref(h), None) == ERR_NULL
+    assert lib.mhc_prepare_weights(fake(1), None, None) == ERR_NULL
+    assert lib.mhc_prepare_weights(fake(1) + 4, ctypes.byref(h), None) == ERR_ALIGN
+    assert h.value is None                      # *out is cleared once fn and out are given
+    assert lib.mhc_release_weights(None) == 0   # like free(NULL)
+    p = m.default_params()
+    assert lib.mhc_pre_prepared(fake(0), None, fake(2), fake(3), fake(4), 4, 4, ctypes.byref(p),
+                                fake(9), lib.mhc_pre_workspace_bytes(4), fake(5), fake(6), fake(7),
+                                None, None, None) == ERR_NULL
+    assert b"allocation" in lib.mhc_strerror(-10)
