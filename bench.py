@@ -3,7 +3,9 @@
 
 One step = mhc_pre then mhc_post over one M=16384-row chunk of the residual
 R[M,4,5120] (the prefill-chunk workload), with synthetic seeded inputs
-already resident in HBM.  Prints one JSON line (rank 0).
+already resident in HBM; fn is prepared once (mhc_prepare_weights), as at
+model load, and the step calls mhc_pre_prepared.  Prints one JSON line
+(rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mhc|reference]
 
@@ -227,10 +229,13 @@ def run_mhc(args):
     R2 = torch.empty_like(R)
     ws = torch.empty((max(1, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # fn prepared once, as at model load (outside every timed region)
+    wh = m.mhc_prepare_weights(fn)
+    torch.cuda.synchronize(dev)
 
     def step():
-        m.mhc_pre(R, fn, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn, post=post,
-                  comb=comb, stream=stream)
+        m.mhc_pre_prepared(R, wh, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
+                           post=post, comb=comb, stream=stream)
         m.mhc_post(R, y, post, comb, logical_rows=M, out=R2, stream=stream)
 
     for _ in range(args.warmup):
@@ -260,8 +265,8 @@ def run_mhc(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_)]
     for i in range(K_):
         ev[i][0].record(stream)
-        m.mhc_pre(R, fn, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn, post=post,
-                  comb=comb, stream=stream)
+        m.mhc_pre_prepared(R, wh, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
+                           post=post, comb=comb, stream=stream)
         ev[i][1].record(stream)
         m.mhc_post(R, y, post, comb, logical_rows=M, out=R2, stream=stream)
         ev[i][2].record(stream)
@@ -278,8 +283,8 @@ def run_mhc(args):
                     "R2": torch.empty_like(R2), "ws": torch.empty_like(ws)}
 
         def step_on(B, st):
-            m.mhc_pre(B["R"], fn, scale, base, w, logical_rows=M, workspace=B["ws"], x_norm=B["xn"],
-                      post=B["post"], comb=B["comb"], stream=st)
+            m.mhc_pre_prepared(B["R"], wh, scale, base, w, logical_rows=M, workspace=B["ws"],
+                               x_norm=B["xn"], post=B["post"], comb=B["comb"], stream=st)
             m.mhc_post(B["R"], B["y"], B["post"], B["comb"], logical_rows=M, out=B["R2"], stream=st)
 
         e2e = run_e2e(m, torch, dist, world, dev, step_on, make_bufs, Rh, yh, bf, M, K_)
@@ -408,6 +413,8 @@ def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, d
             "workload": f"M={M} rows per GPU: R[M,4,5120] bf16, fn[24,20480] f32, y[M,5120] bf16 "
                         f"(seed {SEED}); one step = mhc_pre + mhc_post",
             "rows_per_gpu": M,
+            "weights": "fn prepared once with mhc_prepare_weights before the timed regions (as "
+                       "at model load); the step calls mhc_pre_prepared + mhc_post",
             "l2": f"inputs larger than L2 (R alone is {M * K * 2 / 1e6:.0f} MB per step); no flush",
             "achieved_gbs": gbs,
             "frac_of_hbm": gbs / hbm_peak,
@@ -686,10 +693,11 @@ def run_sweep(args):
         comb = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
         R2 = torch.empty_like(R)
         ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+        wh = m.mhc_prepare_weights(fn)          # as at model load, outside the timing
 
         def pre():
-            m.mhc_pre(R, fn, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn, post=post,
-                      comb=comb, stream=stream)
+            m.mhc_pre_prepared(R, wh, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
+                               post=post, comb=comb, stream=stream)
 
         def post_(yy=y):
             m.mhc_post(R, yy, post, comb, logical_rows=M, out=R2, stream=stream)
@@ -711,7 +719,8 @@ def run_sweep(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"M={M} rows: R[M,4,5120] bf16, fn[24,20480] f32, "
                                    f"y[M,5120] bf16 (seed {seed}); one step = mhc_pre + "
-                                   "mhc_post; median of per-step event times",
+                                   "mhc_post (fn prepared once); median of per-step event "
+                                   "times",
                        "op": "sweep", "rows": M,
                        "l2": "512 MB memset before every timed step (outside the events)",
                        "pre_ms": pre_ms, "post_ms": post_ms,
