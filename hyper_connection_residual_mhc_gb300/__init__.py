@@ -71,6 +71,10 @@ SIGNATURES = {
     "mhc_pre_prepared": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64,
                                         ctypes.POINTER(MhcParams), _vp, ctypes.c_size_t, _vp,
                                         _vp, _vp, _vp, _vp, _vp]),
+    "mhc_fused_post_pre_prepared": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                                   _i64, ctypes.POINTER(MhcParams), _vp,
+                                                   ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                   _vp]),
 }
 
 
@@ -350,12 +354,31 @@ def mhc_fused_post_pre(R, y, post, comb, fn, scale, base, norm_w, *, logical_row
     """hc_post then the next hc_pre on its result (see mhc_fused_post_pre in
     include/mhc.h).  Returns ``(R_out, x_norm, post_out, comb_out)``."""
     import torch
+    _need(fn, "fn", torch.float32, (MIX, K))
+    return _fused_call("mhc_fused_post_pre", _ptr(fn), mhc_fused_post_pre_workspace_bytes, R, y,
+                       post, comb, scale, base, norm_w, logical_rows, params, workspace, R_out,
+                       x_norm, post_out, comb_out, pre_out, mix_out, stream)
+
+
+def mhc_fused_post_pre_prepared(R, y, post, comb, weights, scale, base, norm_w, *,
+                                logical_rows=None, params=None, workspace=None, R_out=None,
+                                x_norm=None, post_out=None, comb_out=None, pre_out=None,
+                                mix_out=None, stream=None):
+    """mhc_fused_post_pre with the next sublayer's fn from a prepared-weights
+    handle (bit-identical; the workspace needs no room for fn's image)."""
+    return _fused_call("mhc_fused_post_pre_prepared", weights.handle, mhc_pre_workspace_bytes, R,
+                       y, post, comb, scale, base, norm_w, logical_rows, params, workspace, R_out,
+                       x_norm, post_out, comb_out, pre_out, mix_out, stream)
+
+
+def _fused_call(name, fn_arg, ws_bytes_of, R, y, post, comb, scale, base, norm_w, logical_rows,
+                params, workspace, R_out, x_norm, post_out, comb_out, pre_out, mix_out, stream):
+    import torch
     rows = int(R.shape[0])
     _need(R, "R", torch.bfloat16, (rows, HC, H))
     _need(y, "y", torch.bfloat16, (rows, H))
     _need(post, "post", torch.float32, (rows, HC))
     _need(comb, "comb", torch.float32, (rows, HC, HC))
-    _need(fn, "fn", torch.float32, (MIX, K))
     _need(scale, "scale", torch.float32, (3,))
     _need(base, "base", torch.float32, (MIX,))
     _need(norm_w, "norm_w", torch.bfloat16, (H,))
@@ -373,15 +396,15 @@ def mhc_fused_post_pre(R, y, post, comb, fn, scale, base, norm_w, *, logical_row
         _need(pre_out, "pre_out", torch.float32, (rows, HC))
     if mix_out is not None:
         _need(mix_out, "mix_out", torch.float32, (rows, MIX))
-    need = mhc_fused_post_pre_workspace_bytes(rows)
+    need = ws_bytes_of(rows)
     if workspace is None and need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     p = default_params() if params is None else params
-    code = lib().mhc_fused_post_pre(
-        _ptr(R), _ptr(y), _ptr(post), _ptr(comb), _ptr(fn), _ptr(scale), _ptr(base),
+    code = getattr(lib(), name)(
+        _ptr(R), _ptr(y), _ptr(post), _ptr(comb), fn_arg, _ptr(scale), _ptr(base),
         _ptr(norm_w), rows, rows if logical_rows is None else int(logical_rows), ctypes.byref(p),
         _ptr(workspace), ws_bytes, _ptr(R_out), _ptr(x_norm), _ptr(post_out), _ptr(comb_out),
         _ptr(pre_out), _ptr(mix_out), _stream(stream))
-    _check("mhc_fused_post_pre", code)
+    _check(name, code)
     return R_out, x_norm, post_out, comb_out

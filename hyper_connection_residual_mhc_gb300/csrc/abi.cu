@@ -205,8 +205,9 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
 // ---- prepared weights --------------------------------------------------------------
 struct mhc_weights {
   int device;
-  float *fn32;      // device copy of fn [24, 20480] fp32 (decode path)
+  float *fn32;      // device copy of fn [24, 20480] fp32 (decode paths)
   uint8_t *img;     // the stats kernel's bf16 hi/lo B-tile image of all 16 cluster ranks
+  uint8_t *img64;   // the fused post -> pre kernel's image (64-byte swizzled 32-k blocks)
 };
 
 int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream) {
@@ -218,23 +219,28 @@ int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream) {
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return cuda_fail(ce);
   const size_t fn_bytes = (size_t)MHC_MIX * MHC_K * sizeof(float);
-  mhc_weights *w = new mhc_weights{dev, nullptr, nullptr};
-  ce = cudaMalloc(reinterpret_cast<void **>(&w->fn32), fn_bytes);
-  if (ce == cudaSuccess) ce = cudaMalloc(reinterpret_cast<void **>(&w->img), mhc::fn_img_bytes());
-  if (ce != cudaSuccess) {
+  mhc_weights *w = new mhc_weights{dev, nullptr, nullptr, nullptr};
+  auto drop = [&]() {
     cudaFree(w->fn32);
     cudaFree(w->img);
+    cudaFree(w->img64);
     delete w;
+  };
+  ce = cudaMalloc(reinterpret_cast<void **>(&w->fn32), fn_bytes);
+  if (ce == cudaSuccess) ce = cudaMalloc(reinterpret_cast<void **>(&w->img), mhc::fn_img_bytes());
+  if (ce == cudaSuccess)
+    ce = cudaMalloc(reinterpret_cast<void **>(&w->img64), mhc::fused_fn_bytes());
+  if (ce != cudaSuccess) {
+    drop();
     cuda_fail(ce);
     return MHC_ERR_ALLOC;
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   ce = cudaMemcpyAsync(w->fn32, fn, fn_bytes, cudaMemcpyDeviceToDevice, s);
   if (ce == cudaSuccess) ce = mhc::launch_fn_img_prep(fn, w->img, s);
+  if (ce == cudaSuccess) ce = mhc::launch_fn_prep_sw64(fn, w->img64, s, false);
   if (ce != cudaSuccess) {
-    cudaFree(w->fn32);
-    cudaFree(w->img);
-    delete w;
+    drop();
     return cuda_fail(ce);
   }
   *out = w;
@@ -243,10 +249,11 @@ int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream) {
 
 int mhc_release_weights(mhc_weights *w) {
   if (!w) return MHC_OK;
-  cudaError_t e1 = cudaFree(w->fn32), e2 = cudaFree(w->img);
+  cudaError_t e1 = cudaFree(w->fn32), e2 = cudaFree(w->img), e3 = cudaFree(w->img64);
   delete w;
   if (e1 != cudaSuccess) return cuda_fail(e1);
   if (e2 != cudaSuccess) return cuda_fail(e2);
+  if (e3 != cudaSuccess) return cuda_fail(e3);
   return MHC_OK;
 }
 
@@ -349,12 +356,16 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 
-int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
-                       const float *comb, const float *fn, const float *scale, const float *base,
-                       const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
-                       const mhc_params *p_in, void *workspace, size_t workspace_bytes,
-                       uint16_t *R_out, uint16_t *x_norm, float *post_out, float *comb_out,
-                       float *pre_out, float *mix_out, void *stream) {
+namespace {
+// mhc_fused_post_pre and its prepared form: fnp_ready is NULL (the call
+// writes fn's image into its workspace) or the handle's image (fn is then the
+// handle's fp32 copy and the workspace needs no room for an image)
+int fused_impl(const uint16_t *R, const uint16_t *y, const float *post, const float *comb,
+               const float *fn, const uint8_t *fnp_ready, const float *scale, const float *base,
+               const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+               const mhc_params *p_in, void *workspace, size_t workspace_bytes,
+               uint16_t *R_out, uint16_t *x_norm, float *post_out, float *comb_out,
+               float *pre_out, float *mix_out, void *stream) {
   mhc_params p;
   if (p_in) p = *p_in; else mhc_default_params(&p);
   if (int e = check_rows(rows, logical_rows)) return e;
@@ -370,7 +381,8 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
   for (const void *q : al)
     if (!aligned16(q)) return MHC_ERR_ALIGN;
   if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
-  const size_t need = mhc_fused_post_pre_workspace_bytes(rows);
+  const size_t need = fnp_ready ? mhc_pre_workspace_bytes(rows)
+                                : mhc_fused_post_pre_workspace_bytes(rows);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return MHC_ERR_WORKSPACE;
   const size_t nr = (size_t)rows;
@@ -405,15 +417,44 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
   } else {
     float *pre_ws = static_cast<float *>(workspace);
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
-    uint8_t *fnp = static_cast<uint8_t *>(workspace) + mhc_pre_workspace_bytes(rows);
-    ce = mhc::launch_post_pre_fused(R, y, post, comb, fn, scale, base, rows, logical_rows, p,
-                                    pre_ws, logit_ws, fnp, R_out, post_out, pre_out, mix_out, s);
+    const uint8_t *fnp =
+        fnp_ready ? fnp_ready : static_cast<uint8_t *>(workspace) + mhc_pre_workspace_bytes(rows);
+    ce = mhc::launch_post_pre_fused(R, y, post, comb, fnp_ready ? nullptr : fn, scale, base, rows,
+                                    logical_rows, p, pre_ws, logit_ws, fnp, R_out, post_out,
+                                    pre_out, mix_out, s);
     if (ce == cudaSuccess)
       ce = mhc::launch_combine_norm_sinkhorn(R_out, pre_ws, norm_w, p.norm_eps, logit_ws, comb_out,
                                              p.hc_sinkhorn_eps, p.sinkhorn_iters, rows,
                                              logical_rows, x_norm, s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+}  // namespace
+
+int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
+                       const float *comb, const float *fn, const float *scale, const float *base,
+                       const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+                       const mhc_params *p, void *workspace, size_t workspace_bytes,
+                       uint16_t *R_out, uint16_t *x_norm, float *post_out, float *comb_out,
+                       float *pre_out, float *mix_out, void *stream) {
+  return fused_impl(R, y, post, comb, fn, nullptr, scale, base, norm_w, rows, logical_rows, p,
+                    workspace, workspace_bytes, R_out, x_norm, post_out, comb_out, pre_out,
+                    mix_out, stream);
+}
+
+int mhc_fused_post_pre_prepared(const uint16_t *R, const uint16_t *y, const float *post,
+                                const float *comb, const mhc_weights *w, const float *scale,
+                                const float *base, const uint16_t *norm_w, int64_t rows,
+                                int64_t logical_rows, const mhc_params *p, void *workspace,
+                                size_t workspace_bytes, uint16_t *R_out, uint16_t *x_norm,
+                                float *post_out, float *comb_out, float *pre_out, float *mix_out,
+                                void *stream) {
+  if (!w) return MHC_ERR_NULL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != w->device) return MHC_ERR_DEVICE;
+  return fused_impl(R, y, post, comb, w->fn32, w->img64, scale, base, norm_w, rows, logical_rows,
+                    p, workspace, workspace_bytes, R_out, x_norm, post_out, comb_out, pre_out,
+                    mix_out, stream);
 }
 
 int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const float *base,

@@ -206,12 +206,14 @@ cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t row
 // [rows, 16] and its post gates (+ pre_out, mix_out)
 // (fnp: fused_fn_bytes() of scratch for fn in the kernel's B-operand image)
 size_t fused_fn_bytes();
+// (fn NULL: fnp already holds the image, written by launch_fn_prep_sw64)
 cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const float *post,
                                   const float *comb, const float *fn, const float *scale,
                                   const float *base, int64_t rows, int64_t logical_rows,
                                   const mhc_params &p, float *pre_ws, float *logit_ws,
-                                  uint8_t *fnp, uint16_t *R_out, float *post_out, float *pre_out,
-                                  float *mix_out, cudaStream_t s);
+                                  const uint8_t *fnp, uint16_t *R_out, float *post_out,
+                                  float *pre_out, float *mix_out, cudaStream_t s);
+cudaError_t launch_fn_prep_sw64(const float *fn, uint8_t *fnp, cudaStream_t s, bool pdl);
 cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset);
 // the stats kernel's error word (nonzero once a bounded wait expired)
 cudaError_t fused_error_word(unsigned int *out, bool reset);

@@ -507,12 +507,18 @@ bool encode_rows(CUtensorMap *map, const uint16_t *base, int64_t cols, int64_t r
 
 size_t fused_fn_bytes() { return (size_t)kFnBlocks * kFnBlkBytes; }
 
+cudaError_t launch_fn_prep_sw64(const float *fn, uint8_t *fnp, cudaStream_t s, bool pdl) {
+  constexpr int kPrepItems = kFnBlocks * kMix * 4;
+  return launch_pdl(fn_prep_sw64_kernel, dim3((kPrepItems + 255) / 256), dim3(256), 0, s, 1, pdl,
+                    fn, fnp);
+}
+
 cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const float *post,
                                   const float *comb, const float *fn, const float *scale,
                                   const float *base, int64_t rows, int64_t logical_rows,
                                   const mhc_params &p, float *pre_ws, float *logit_ws,
-                                  uint8_t *fnp, uint16_t *R_out, float *post_out, float *pre_out,
-                                  float *mix_out, cudaStream_t s) {
+                                  const uint8_t *fnp, uint16_t *R_out, float *post_out,
+                                  float *pre_out, float *mix_out, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -523,10 +529,11 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   CUtensorMap map_r, map_y;
   if (!encode_rows(&map_r, R, kK, rows) || !encode_rows(&map_y, y, kH, rows))
     return cudaErrorInvalidValue;
-  constexpr int kPrepItems = kFnBlocks * kMix * 4;
-  e = launch_pdl(fn_prep_sw64_kernel, dim3((kPrepItems + 255) / 256), dim3(256), 0, s, 1,
-                 use_pdl(logical_rows), fn, fnp);
-  if (e != cudaSuccess) return e;
+  // fn == NULL: fnp already holds the image (prepared weights)
+  if (fn) {
+    e = launch_fn_prep_sw64(fn, const_cast<uint8_t *>(fnp), s, use_pdl(logical_rows));
+    if (e != cudaSuccess) return e;
+  }
   FusedArgs a;
   a.post_in = post;
   a.comb_in = comb;

@@ -240,10 +240,11 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
  *
  * mhc_prepare_weights(fn, &w, stream)
  *   fn [24, 20480] fp32, device, 16-byte aligned (hc_fn of one sublayer).
- *   Allocates device memory on the current device (about 3.9 MB, the only
+ *   Allocates device memory on the current device (about 5.9 MB, the only
  *   allocation libmhc makes) and enqueues on `stream`: a copy of fn, and
- *   fn's bf16 hi/lo operand image for every CTA of the tensor-core stats
- *   kernel (the same bits the kernel would form itself).  The handle may be
+ *   fn's bf16 hi/lo operand images for the tensor-core stats kernel and for
+ *   the fused post -> pre kernel (the same bits those kernels would form
+ *   themselves).  The handle may be
  *   used by calls enqueued after it on `stream`, or on any stream once the
  *   caller has ordered them after it; fn itself may be freed or changed
  *   afterwards.  Returns MHC_OK, MHC_ERR_NULL, MHC_ERR_ALIGN, MHC_ERR_DEVICE,
@@ -255,6 +256,10 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
  *   mhc_pre with fn taken from the handle: the same arguments, checks and
  *   outputs, bit-identical to mhc_pre on the fn the handle was made from.
  *   MHC_ERR_DEVICE if the current device is not the handle's.
+ * mhc_fused_post_pre_prepared(R, y, post, comb, w, scale, base, norm_w, ...)
+ *   mhc_fused_post_pre likewise (w is the next sublayer's weights); its
+ *   workspace needs only mhc_pre_workspace_bytes(rows) bytes, since the call
+ *   no longer converts fn.
  */
 typedef struct mhc_weights mhc_weights;
 int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream);
@@ -264,6 +269,13 @@ int mhc_pre_prepared(const uint16_t *R, const mhc_weights *w, const float *scale
                      int64_t logical_rows, const mhc_params *p, void *workspace,
                      size_t workspace_bytes, uint16_t *x_norm, float *post, float *comb,
                      float *pre_out, float *mix_out, void *stream);
+int mhc_fused_post_pre_prepared(const uint16_t *R, const uint16_t *y, const float *post,
+                                const float *comb, const mhc_weights *w, const float *scale,
+                                const float *base, const uint16_t *norm_w, int64_t rows,
+                                int64_t logical_rows, const mhc_params *p, void *workspace,
+                                size_t workspace_bytes, uint16_t *R_out, uint16_t *x_norm,
+                                float *post_out, float *comb_out, float *pre_out, float *mix_out,
+                                void *stream);
 
 /*
  * mhc_fused_post_pre -- hc_post of one sublayer and hc_pre of the next on its

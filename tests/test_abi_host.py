@@ -202,3 +202,12 @@ def test_prepared_weights_host_checks(lib):
                                 fake(9), lib.mhc_pre_workspace_bytes(4), fake(5), fake(6), fake(7),
                                 None, None, None) == ERR_NULL
     assert b"allocation" in lib.mhc_strerror(-10)
+
+
+def test_fused_prepared_null_handle(lib):
+    import hyper_connection_residual_mhc_gb300 as m
+    p = m.default_params()
+    assert lib.mhc_fused_post_pre_prepared(
+        fake(0), fake(1), fake(2), fake(3), None, fake(5), fake(6), fake(7), 4, 4,
+        ctypes.byref(p), fake(9), lib.mhc_pre_workspace_bytes(4), fake(10), fake(11), fake(12),
+        fake(13), None, None, None) == ERR_NULL

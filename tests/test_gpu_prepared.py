@@ -79,3 +79,28 @@ def test_released_handle_is_refused(torch, mhc):
     with pytest.raises(ValueError):
         mhc.mhc_pre_prepared(R, handle, torch.from_numpy(W.scale).cuda(),
                              torch.from_numpy(W.base).cuda(), _bf(torch, W.norm_w))
+
+
+@pytest.mark.parametrize("rows", [8, 1500])
+def test_fused_prepared_equals_fused_bits(torch, mhc, rows):
+    # the next sublayer's fn through a handle; the prepared call runs with the
+    # smaller workspace (no room for fn's image)
+    W, Wn = synth.weights(12), synth.weights(13)
+    R = _bf(torch, synth.residual(12, rows))
+    y = _bf(torch, synth.sublayer_out(12, rows))
+    _, post, comb = mhc.mhc_pre(R, torch.from_numpy(W.fn).cuda(), torch.from_numpy(W.scale).cuda(),
+                                torch.from_numpy(W.base).cuda(), _bf(torch, W.norm_w))
+    fn = torch.from_numpy(Wn.fn).cuda()
+    scale = torch.from_numpy(Wn.scale).cuda()
+    base = torch.from_numpy(Wn.base).cuda()
+    w = _bf(torch, Wn.norm_w)
+    ref = mhc.mhc_fused_post_pre(R, y, post, comb, fn, scale, base, w)
+    handle = mhc.mhc_prepare_weights(fn)
+    ws = torch.empty((max(256, mhc.mhc_pre_workspace_bytes(rows)),), dtype=torch.uint8,
+                     device="cuda")
+    got = mhc.mhc_fused_post_pre_prepared(R, y, post, comb, handle, scale, base, w, workspace=ws)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("R_out", "x_norm", "post", "comb"), got, ref):
+        assert torch.equal(a, b), name
+    handle.release()
+    assert mhc.mhc_kernel_status() == 0
