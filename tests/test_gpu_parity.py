@@ -158,6 +158,26 @@ def test_full_size_sampled_rows(torch, mhc, oracle_mod, rows):
                  term_mag=P.post_term_magnitude(c.R[idx], c.y[idx], post_g, comb_g))
 
 
+def test_chunk_larger_than_the_headline_sampled_rows(torch, mhc, oracle_mod):
+    # 40001 rows: 313 tiles over the co-resident clusters (many rounds), a
+    # 65-row last tile, and 1.6 GB of R -- sizes past every workload above
+    rows = 40001
+    c = Case(torch, rows, 77)
+    idx = np.unique(np.concatenate([[0, 127, 128, 20000, rows - 65, rows - 1],
+                                    np.random.default_rng(77).integers(0, rows, 24)]))
+    g = c.gpu_pre(torch, mhc)
+    out = mhc.mhc_post(c.dR, c.dy, g["post"], g["comb"])
+    torch.cuda.synchronize()
+    _check_pre(torch, g, c.oracle_pre(oracle_mod, idx), c, idx)
+    post_g = host_f(g["post"])[idx].astype(np.float32)
+    comb_g = host_f(g["comb"])[idx].astype(np.float32)
+    ref = oracle_mod.post(c.R[idx], c.y[idx], post_g, comb_g)
+    P.check_bf16(_bits(torch, out)[idx], ref, "R_out",
+                 term_mag=P.post_term_magnitude(c.R[idx], c.y[idx], post_g, comb_g))
+    assert mhc.mhc_kernel_status() == 0
+    _cases.clear()
+
+
 def test_post_alone_with_second_seed_output(torch, mhc, oracle_mod):
     # M=4096: mhc_post on its own with y drawn from a second stream
     c = Case(torch, 4096, 3, y_tensor=synth.T_Y2)
