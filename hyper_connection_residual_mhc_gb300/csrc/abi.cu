@@ -180,7 +180,7 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const fl
     // decode-size chunk: latency-shaped CUDA-core path (keyed on the chunk's
     // row count, so every shard of the chunk takes it)
     ce = mhc::launch_pre_decode(R, fn, scale, base, norm_w, rows, logical_rows, p, x_norm, post,
-                                comb, pre_out, mix_out, s);
+                                comb, pre_out, mix_out, s, /*fn_stable=*/fn_img != nullptr);
   } else {
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
     ce = mhc::launch_pre_stats(R, fn, fn_img, scale, base, rows, logical_rows, p, pre_ws, logit_ws,
@@ -413,7 +413,7 @@ int fused_impl(const uint16_t *R, const uint16_t *y, const float *post, const fl
     // decode pre on R'
     ce = mhc::launch_post_pre_decode(R, y, post, comb, fn, scale, base, norm_w, rows,
                                      logical_rows, p, R_out, x_norm, post_out, comb_out, pre_out,
-                                     mix_out, s);
+                                     mix_out, s, /*fn_stable=*/fnp_ready != nullptr);
   } else {
     float *pre_ws = static_cast<float *>(workspace);
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));

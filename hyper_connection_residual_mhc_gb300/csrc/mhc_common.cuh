@@ -151,7 +151,7 @@ cudaError_t launch_pre_decode(const uint16_t *R, const float *fn, const float *s
                               const float *base, const uint16_t *norm_w, int64_t rows,
                               int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
                               float *post, float *comb, float *pre_out, float *mix_out,
-                              cudaStream_t s);
+                              cudaStream_t s, bool fn_stable = false);
 // the same launch with hc_post of the previous sublayer first: R_out =
 // hc_post(R, y, post_in, comb_in) (mhc_post's bits), then mhc_pre on R_out
 cudaError_t launch_post_pre_decode(const uint16_t *R, const uint16_t *y, const float *post_in,
@@ -159,7 +159,7 @@ cudaError_t launch_post_pre_decode(const uint16_t *R, const uint16_t *y, const f
                                    const float *base, const uint16_t *norm_w, int64_t rows,
                                    int64_t logical_rows, const mhc_params &p, uint16_t *R_out,
                                    uint16_t *x_norm, float *post, float *comb, float *pre_out,
-                                   float *mix_out, cudaStream_t s);
+                                   float *mix_out, cudaStream_t s, bool fn_stable = false);
 
 // tensor-core stats half of mhc_pre (cluster of 16 CTAs): writes the pre gates
 // to pre_ws [rows, 4] and the comb logits to logit_ws [rows, 16] for the
