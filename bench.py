@@ -577,12 +577,15 @@ def run_op(args):
             for _ in range(args.warmup):
                 launch(side)
             eager_us = timed(lambda: launch(side), args.steps)
+            # the graph holds --chain consecutive steps, so each step after the
+            # first can overlap its predecessor's tail
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=side):
-                launch(side)
+                for _ in range(args.chain):
+                    launch(side)
             for _ in range(args.warmup):
                 g.replay()
-            graph_us = timed(g.replay, args.steps)
+            graph_us = timed(g.replay, args.steps) / args.chain
         nbytes = M * (PRE_BYTES_ROW + POST_BYTES_ROW) + PRE_BYTES_CALL
         line = {
             "metric": (f"mhc_fused_post_pre latency at M={M} rows (one decode sublayer boundary)"
@@ -595,10 +598,10 @@ def run_op(args):
                                    "L2-resident between steps (decode-size, latency-bound)",
                        "op": "latency", "fused": bool(args.fused), "rows": M,
                        "logical_rows": LM, "eager_us": eager_us,
-                       "graph_us": graph_us},
+                       "graph_us": graph_us, "graph_chain": args.chain},
             "roofline": {"bound": "latency", "algorithmic_bytes_per_step": nbytes,
                          "achieved_gbs_graph": nbytes / (graph_us * 1e-6) / 1e9},
-            "gpu_launches": (3 if LM > 48 else (1 if args.fused else 2)) * args.steps,
+            "gpu_launches": (3 if LM > 48 else (1 if args.fused else 2)) * args.steps * args.chain,
         }
         print(json.dumps(line), flush=True)
         return
@@ -752,6 +755,9 @@ def main():
                          "point alone")
     ap.add_argument("--fused", action="store_true",
                     help="--op latency: time mhc_fused_post_pre (one decode sublayer boundary)")
+    ap.add_argument("--chain", type=int, default=1,
+                    help="--op latency: consecutive steps captured in one CUDA graph "
+                         "(the graph figure is per step)")
     ap.add_argument("--logical-rows", type=int, default=0,
                     help="--op latency: the chunk's row count (default: --rows)")
     ap.add_argument("--rows", type=int, default=ROWS,
@@ -760,6 +766,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.chain < 1:
+        ap.error("--chain must be >= 1")
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "sweep":
