@@ -33,6 +33,7 @@ _lib = None
 _D = ctypes.POINTER(ctypes.c_double)
 _F = ctypes.POINTER(ctypes.c_float)
 _U16 = ctypes.POINTER(ctypes.c_uint16)
+_U8 = ctypes.POINTER(ctypes.c_uint8)
 
 
 def build(force: bool = False) -> str:
@@ -67,8 +68,11 @@ def _load():
             lib.oracle_pre.argtypes = [_U16, i64, _F, _F, _F, _U16, dbl, dbl, dbl, dbl, dbl,
                                        c_int, _D, _D, _D, _D, _D, _U16]
             lib.oracle_hc_head.argtypes = [_U16, i64, _F, _F, _F, dbl, dbl, _D, _D, _U16]
+            lib.oracle_mxfp8_quantize.argtypes = [_U16, i64, i64, _U8, _U8]
+            lib.oracle_swizzle_128x4.argtypes = [_U8, i64, i64, _U8]
             for f in ("oracle_stats", "oracle_split_sinkhorn", "oracle_combine_norm",
-                      "oracle_post", "oracle_pre", "oracle_hc_head"):
+                      "oracle_post", "oracle_pre", "oracle_hc_head", "oracle_mxfp8_quantize",
+                      "oracle_swizzle_128x4"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -200,3 +204,31 @@ def fused_post_pre(R, y, post_w, comb, fn, scale, base, w, **pre_kw):
     Returns (R' bf16 bits, the pre dict of R')."""
     R2 = post(R, y, post_w, comb)
     return R2, pre(R2, fn, scale, base, w, **pre_kw)
+
+
+def mxfp8_quantize(x):
+    """MXFP8 of bf16 rows (prefill_sp.py, _mxfp8_quantize: per row, per 32
+    columns, linear scale layout): x [rows, cols] bf16 bits, cols a multiple
+    of 32 -> (q [rows, cols] uint8 E4M3 codes, s [rows, cols/32] uint8 ue8m0
+    scales)."""
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16 or x.ndim != 2 or x.shape[1] % 32:
+        raise ValueError("expected [rows, cols] uint16 bf16 bits with cols % 32 == 0")
+    rows, cols = x.shape
+    q = np.zeros((rows, cols), np.uint8)
+    s = np.zeros((rows, cols // 32), np.uint8)
+    _load().oracle_mxfp8_quantize(_p(x, _U16), rows, cols, _p(q, _U8), _p(s, _U8))
+    return q, s
+
+
+def swizzle_128x4(s):
+    """The 128x4 tiled layout of linear ue8m0 scales (prefill_sp.py,
+    swizzle_128x4): s [rows, groups] uint8, groups a multiple of 4 -> a flat
+    uint8 array of ceil(rows/128)*128*groups bytes (padding rows zero)."""
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    if s.ndim != 2 or s.shape[1] % 4:
+        raise ValueError("expected [rows, groups] with groups % 4 == 0")
+    rows, groups = s.shape
+    out = np.zeros(((rows + 127) // 128 * 128 * groups,), np.uint8)
+    _load().oracle_swizzle_128x4(_p(s, _U8), rows, groups, _p(out, _U8))
+    return out

@@ -45,6 +45,16 @@
  *     every column i by (its sum over j + eps).
  * The combine+RMSNorm keeps y in full precision (fused reading); an option
  * emulates the unfused path, which rounds y to bf16 before the norm.
+ *
+ * MXFP8 output of x_norm (prefill_sp.py, _mxfp8_quantize / mxfp8_gather and
+ * swizzle_128x4): per row, per 32 columns, fp8 codes plus one ue8m0 scale,
+ * scales in a linear [rows, cols/32] layout, and the 128x4 tiled scale layout
+ * the pages build from it.  The pages call a library quantizer and do not
+ * state its scale or rounding rule; the reading used here is the OCP
+ * Microscaling Formats (MX) v1.0 conversion: shared exponent
+ * floor(log2(block amax)) - 8 (8 = the largest exponent of E4M3), clamped to
+ * the scale format's range, elements x / 2^shared rounded to E4M3 nearest-even
+ * and saturated to +-448, the sign kept (so -0 and tiny negatives give 0x80).
  */
 #include <math.h>
 #include <stdint.h>
@@ -289,4 +299,94 @@ void oracle_hc_head(const uint16_t *R, int64_t rows, const float *fn, const floa
         }
     }
     free(x);
+}
+
+/* ---- MXFP8: E4M3 codes with ue8m0 block scales ----------------------------- */
+
+/* E4M3 (OCP 8-bit float: sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, exponent 15 with mantissa 7 is NaN).  A normal code is
+ * (1 + m/8) * 2^(E-7), E = 1..15; a subnormal (m/8) * 2^-6.  The largest
+ * finite value is 448 (0x7E).  Rounds a finite double to nearest, ties to the
+ * even mantissa, and saturates to 448. */
+static uint8_t e4m3_from_double(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0;
+    if (isnan(v))
+        return sign | 0x7F;
+    double a = fabs(v);
+    int q;                        /* quantum exponent of a's binade */
+    if (a >= ldexp(1.0, -6)) {
+        int e;
+        (void)frexp(a, &e);       /* a in [2^(e-1), 2^e) */
+        q = (e - 1) - 3;
+    } else {
+        q = -9;                   /* subnormal quantum */
+    }
+    double t = ldexp(nearbyint(ldexp(a, -q)), q);   /* exact scaling, one rounding */
+    if (t > 448.0)
+        t = 448.0;
+    if (t == 0.0)
+        return sign;
+    if (t < ldexp(1.0, -6))
+        return sign | (uint8_t)(t * 512.0);         /* subnormal mantissa t / 2^-9 */
+    int e;
+    double f = frexp(t, &e);      /* t = (2f) * 2^(e-1), 2f in [1, 2) */
+    int E = (e - 1) + 7;
+    int m = (int)((2.0 * f - 1.0) * 8.0);           /* exact: t has 4 significant bits */
+    return sign | (uint8_t)(E << 3) | (uint8_t)m;
+}
+
+/* x [rows, cols] bf16 bits, cols a multiple of 32 (finite values).  For each
+ * row m and block b of 32 columns:
+ *   amax  = max |x[m, 32b .. 32b+31]|
+ *   e     = floor(log2 amax) - 8, clamped to [-127, 127]; e = -127 when amax = 0
+ *   s[m, b] = e + 127                              (ue8m0 code of 2^e)
+ *   q[m, k] = E4M3( x[m, k] / 2^e )                (nearest-even, saturating)
+ * q is [rows, cols], s is [rows, cols/32] (the linear layout). */
+void oracle_mxfp8_quantize(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q,
+                           uint8_t *s)
+{
+    const int64_t nb = cols / 32;
+    for (int64_t m = 0; m < rows; ++m) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint16_t *blk = x + m * cols + 32 * b;
+            double amax = 0.0;
+            for (int k = 0; k < 32; ++k) {
+                double a = fabs(oracle_bf16_to_double(blk[k]));
+                if (a > amax)
+                    amax = a;
+            }
+            int e = -127;
+            if (amax > 0.0) {
+                int ex;
+                (void)frexp(amax, &ex);             /* amax in [2^(ex-1), 2^ex) */
+                e = (ex - 1) - 8;
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+            }
+            s[m * nb + b] = (uint8_t)(e + 127);
+            for (int k = 0; k < 32; ++k)
+                q[m * cols + 32 * b + k] =
+                    e4m3_from_double(ldexp(oracle_bf16_to_double(blk[k]), -e));
+        }
+    }
+}
+
+/* The 128x4 tiled scale layout (prefill_sp.py, swizzle_128x4): s [rows,
+ * groups] (groups a multiple of 4) -> out of ceil(rows/128)*128*groups bytes.
+ * Rows are padded to a multiple of 128 with zero scales; tile (m/128, g/4) is
+ * the (m/128 * groups/4 + g/4)-th run of 512 bytes, and inside it the byte
+ * of (m, g) sits at [m%32][(m%128)/32][g%4]. */
+void oracle_swizzle_128x4(const uint8_t *s, int64_t rows, int64_t groups, uint8_t *out)
+{
+    const int64_t tm = (rows + 127) / 128, tg = groups / 4;
+    memset(out, 0, (size_t)(tm * 128 * groups));
+    for (int64_t m = 0; m < rows; ++m)
+        for (int64_t g = 0; g < groups; ++g) {
+            int64_t tile = (m / 128) * tg + g / 4;
+            int64_t inner = (m % 32) * 16 + ((m % 128) / 32) * 4 + g % 4;
+            out[tile * 512 + inner] = s[m * groups + g];
+        }
 }
