@@ -529,6 +529,44 @@ def run_op(args):
         workload = (f"M={M} rows: R[M,4,5120], y[M,5120] bf16, next fn[24,20480] f32 "
                     f"(seed {SEED}), prepared once; unfused mhc_post+mhc_pre: {unfused_ms:.4f} "
                     "ms/step")
+    elif args.op == "pre_mxfp8":
+        # mhc_pre with x_norm's MXFP8 codes and scales written beside it, timed
+        # against mhc_pre_prepared alone (the same inputs, the same way)
+        W = synth.weights(SEED)
+        t_ = lambda a: torch.from_numpy(a).to(dev)
+        scale, base, w = t_(W.scale), t_(W.base), bf(W.norm_w)
+        wh = m.mhc_prepare_weights(t_(W.fn))
+        xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        xq = torch.empty((M, H), dtype=torch.uint8, device=dev)
+        xs = torch.empty((M, H // 32), dtype=torch.uint8, device=dev)
+        po = torch.empty((M, HC), dtype=torch.float32, device=dev)
+        co = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
+        ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+
+        def step():
+            m.mhc_pre_mxfp8(R, wh, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
+                            x_q=xq, x_s=xs, post=po, comb=co, stream=stream)
+
+        def plain():
+            m.mhc_pre_prepared(R, wh, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
+                               post=po, comb=co, stream=stream)
+        for _ in range(args.warmup):
+            plain()
+        torch.cuda.synchronize(dev)
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(args.steps):
+            plain()
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        plain_ms = a_.elapsed_time(b_) / args.steps
+        # mhc_pre's bytes plus the codes (1 B per x_norm value) and scales (1 B
+        # per 32 values)
+        nbytes = M * (PRE_BYTES_ROW + H + H // 32) + PRE_BYTES_CALL
+        launches = 2            # stats + combine; at decode sizes decode kernel + quantizer
+        metric = "mhc_pre_mxfp8 rows/s (mhc_pre + MXFP8 x_norm) and achieved HBM GB/s"
+        workload = (f"M={M} rows: R[M,4,5120] bf16, fn[24,20480] f32 (seed {SEED}), prepared "
+                    f"once; mhc_pre_prepared alone: {plain_ms:.4f} ms/step")
     elif args.op == "latency":
         # decode-size rows: one step = mhc_pre + mhc_post; latency per step,
         # launched eagerly and replayed from a CUDA graph
@@ -749,7 +787,8 @@ def main():
     ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["step", "hc_head", "latency", "fused_post_pre", "sweep"],
+    ap.add_argument("--op", choices=["step", "hc_head", "latency", "fused_post_pre", "sweep",
+                                     "pre_mxfp8"],
                     default="step",
                     help="step: mhc_pre + mhc_post (the headline); others time one entry "
                          "point alone")

@@ -75,6 +75,12 @@ SIGNATURES = {
                                                    _i64, ctypes.POINTER(MhcParams), _vp,
                                                    ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp, _vp,
                                                    _vp]),
+    "mhc_pre_mxfp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                     ctypes.POINTER(MhcParams), _vp, ctypes.c_size_t, _vp, _vp,
+                                     _vp, _vp, _vp, _vp]),
+    "mhc_quantize_mxfp8": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "mhc_swizzle_scales_128x4_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "mhc_swizzle_scales_128x4": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
 }
 
 
@@ -250,6 +256,73 @@ def mhc_pre_prepared(R, weights, scale, base, norm_w, *, logical_rows=None, para
     """mhc_pre with fn from a prepared-weights handle (bit-identical to mhc_pre)."""
     return _pre_call("mhc_pre_prepared", weights.handle, R, scale, base, norm_w, logical_rows,
                      params, workspace, x_norm, post, comb, pre_out, mix_out, stream)
+
+
+def mhc_pre_mxfp8(R, weights, scale, base, norm_w, *, logical_rows=None, params=None,
+                  workspace=None, x_norm=None, x_q=None, x_s=None, post=None, comb=None,
+                  stream=None):
+    """mhc_pre_prepared that also writes x_norm's MXFP8 (see mhc_pre_mxfp8 in
+    include/mhc.h). Returns ``(x_norm [rows,5120] bf16, x_q [rows,5120] uint8
+    E4M3 codes, x_s [rows,160] uint8 ue8m0 scales, post, comb)``."""
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(scale, "scale", torch.float32, (3,))
+    _need(base, "base", torch.float32, (MIX,))
+    _need(norm_w, "norm_w", torch.bfloat16, (H,))
+    dev = R.device
+    x_norm = torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if x_norm is None else x_norm
+    x_q = torch.empty((rows, H), dtype=torch.uint8, device=dev) if x_q is None else x_q
+    x_s = torch.empty((rows, H // 32), dtype=torch.uint8, device=dev) if x_s is None else x_s
+    post = torch.empty((rows, HC), dtype=torch.float32, device=dev) if post is None else post
+    comb = torch.empty((rows, HC, HC), dtype=torch.float32, device=dev) if comb is None else comb
+    _need(x_norm, "x_norm", torch.bfloat16, (rows, H))
+    _need(x_q, "x_q", torch.uint8, (rows, H))
+    _need(x_s, "x_s", torch.uint8, (rows, H // 32))
+    _need(post, "post", torch.float32, (rows, HC))
+    _need(comb, "comb", torch.float32, (rows, HC, HC))
+    need = mhc_pre_workspace_bytes(rows)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    p = default_params() if params is None else params
+    code = lib().mhc_pre_mxfp8(
+        _ptr(R), weights.handle, _ptr(scale), _ptr(base), _ptr(norm_w), rows,
+        rows if logical_rows is None else int(logical_rows), ctypes.byref(p), _ptr(workspace),
+        ws_bytes, _ptr(x_norm), _ptr(x_q), _ptr(x_s), _ptr(post), _ptr(comb), _stream(stream))
+    _check("mhc_pre_mxfp8", code)
+    return x_norm, x_q, x_s, post, comb
+
+
+def mhc_quantize_mxfp8(x, *, logical_rows=None, q=None, s=None, stream=None):
+    """MXFP8 of bf16 rows x [rows, cols] (see mhc_quantize_mxfp8 in
+    include/mhc.h). Returns ``(q [rows, cols] uint8, s [rows, cols/32] uint8)``."""
+    import torch
+    rows, cols = int(x.shape[0]), int(x.shape[1])
+    _need(x, "x", torch.bfloat16, (rows, cols))
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device) if q is None else q
+    s = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device) if s is None else s
+    _need(q, "q", torch.uint8, (rows, cols))
+    _need(s, "s", torch.uint8, (rows, cols // 32))
+    code = lib().mhc_quantize_mxfp8(_ptr(x), rows, cols,
+                                    rows if logical_rows is None else int(logical_rows),
+                                    _ptr(q), _ptr(s), _stream(stream))
+    _check("mhc_quantize_mxfp8", code)
+    return q, s
+
+
+def mhc_swizzle_scales_128x4(s, *, out=None, stream=None):
+    """Linear ue8m0 scales s [rows, groups] -> the 128x4 tiled layout, a flat
+    uint8 tensor (see mhc_swizzle_scales_128x4 in include/mhc.h)."""
+    import torch
+    rows, groups = int(s.shape[0]), int(s.shape[1])
+    _need(s, "s", torch.uint8, (rows, groups))
+    n = int(lib().mhc_swizzle_scales_128x4_bytes(rows, groups))
+    out = torch.empty((n,), dtype=torch.uint8, device=s.device) if out is None else out
+    _need(out, "out", torch.uint8, (n,))
+    code = lib().mhc_swizzle_scales_128x4(_ptr(s), rows, groups, _ptr(out), _stream(stream))
+    _check("mhc_swizzle_scales_128x4", code)
+    return out
 
 
 def mhc_pre_noalloc_max_rows() -> int:

@@ -31,6 +31,9 @@ bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 // rows are indexed with 32-bit block counts in places: keep rows * 640 chunks
 // (the largest per-row grid) inside a signed 32-bit grid dimension times 256.
 constexpr int64_t kMaxRows = (int64_t)1 << 24;
+// columns of a row the MXFP8 quantizer takes: a 16M-row by 64k-column call
+// stays below 2^40 values, well inside the kernels' 64-bit chunk indices
+constexpr int64_t kMaxMxCols = (int64_t)1 << 16;
 
 int check_rows(int64_t rows, int64_t logical_rows) {
   if (rows < 0 || logical_rows < rows || rows > kMaxRows) return MHC_ERR_SHAPE;
@@ -130,12 +133,14 @@ int mhc_kernel_status(uint32_t *status, int reset) {
 }
 
 namespace {
-// mhc_pre and mhc_pre_prepared: fn is the fp32 weight (the caller's, or the
-// handle's copy); fn_img is NULL or the handle's operand image
+// mhc_pre, mhc_pre_prepared and mhc_pre_mxfp8: fn is the fp32 weight (the
+// caller's, or the handle's copy); fn_img is NULL or the handle's operand
+// image; mx_q / mx_s are NULL or x_norm's MXFP8 codes and linear scales
 int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const float *scale,
              const float *base, const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
              const mhc_params *p_in, void *workspace, size_t workspace_bytes, uint16_t *x_norm,
-             float *post, float *comb, float *pre_out, float *mix_out, void *stream) {
+             float *post, float *comb, float *pre_out, float *mix_out, void *stream,
+             uint8_t *mx_q = nullptr, uint8_t *mx_s = nullptr) {
   mhc_params p;
   if (p_in) p = *p_in; else mhc_default_params(&p);
   if (int e = check_rows(rows, logical_rows)) return e;
@@ -149,6 +154,8 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const fl
   for (const void *q : al)
     if (!aligned16(q)) return MHC_ERR_ALIGN;
   if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
+  if ((mx_q == nullptr) != (mx_s == nullptr)) return MHC_ERR_NULL;
+  if (mx_q && (!aligned16(mx_q) || !aligned16(mx_s))) return MHC_ERR_ALIGN;
   const size_t need = mhc_pre_workspace_bytes(rows);
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -157,9 +164,13 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const fl
   const size_t nr = (size_t)rows;
   const Span ins[] = {span(R, nr * MHC_K * 2), span(fn, (size_t)MHC_MIX * MHC_K * 4),
                       span(scale, 12), span(base, MHC_MIX * 4), span(norm_w, MHC_HIDDEN * 2)};
-  Span outs[6];
+  Span outs[8];
   int n_out = 0;
   outs[n_out++] = span(x_norm, nr * MHC_HIDDEN * 2);
+  if (mx_q) {
+    outs[n_out++] = span(mx_q, nr * MHC_HIDDEN);
+    outs[n_out++] = span(mx_s, nr * (MHC_HIDDEN / 32));
+  }
   outs[n_out++] = span(post, nr * MHC_HC * 4);
   outs[n_out++] = span(comb, nr * MHC_HC * MHC_HC * 4);
   if (pre_out) outs[n_out++] = span(pre_out, nr * MHC_HC * 4);
@@ -181,6 +192,10 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const fl
     // row count, so every shard of the chunk takes it)
     ce = mhc::launch_pre_decode(R, fn, scale, base, norm_w, rows, logical_rows, p, x_norm, post,
                                 comb, pre_out, mix_out, s, /*fn_stable=*/fn_img != nullptr);
+    // the decode kernel writes bf16 x_norm only; its MXFP8 follows in a
+    // second, streaming launch
+    if (ce == cudaSuccess && mx_q)
+      ce = mhc::launch_mx_quantize(x_norm, rows, MHC_HIDDEN, logical_rows, mx_q, mx_s, s);
   } else {
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
     ce = mhc::launch_pre_stats(R, fn, fn_img, scale, base, rows, logical_rows, p, pre_ws, logit_ws,
@@ -188,7 +203,7 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const fl
     if (ce == cudaSuccess)
       ce = mhc::launch_combine_norm_sinkhorn(R, pre_ws, norm_w, p.norm_eps, logit_ws, comb,
                                              p.hc_sinkhorn_eps, p.sinkhorn_iters, rows,
-                                             logical_rows, x_norm, s);
+                                             logical_rows, x_norm, s, mx_q, mx_s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
@@ -267,6 +282,57 @@ int mhc_pre_prepared(const uint16_t *R, const mhc_weights *w, const float *scale
   if (cudaGetDevice(&dev) == cudaSuccess && dev != w->device) return MHC_ERR_DEVICE;
   return pre_impl(R, w->fn32, w->img, scale, base, norm_w, rows, logical_rows, p, workspace,
                   workspace_bytes, x_norm, post, comb, pre_out, mix_out, stream);
+}
+
+int mhc_pre_mxfp8(const uint16_t *R, const mhc_weights *w, const float *scale, const float *base,
+                  const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+                  const mhc_params *p, void *workspace, size_t workspace_bytes,
+                  uint16_t *x_norm, uint8_t *x_q, uint8_t *x_s, float *post, float *comb,
+                  void *stream) {
+  if (!w) return MHC_ERR_NULL;
+  if (rows > 0 && (!x_q || !x_s)) return MHC_ERR_NULL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != w->device) return MHC_ERR_DEVICE;
+  return pre_impl(R, w->fn32, w->img, scale, base, norm_w, rows, logical_rows, p, workspace,
+                  workspace_bytes, x_norm, post, comb, nullptr, nullptr, stream, x_q, x_s);
+}
+
+int mhc_quantize_mxfp8(const uint16_t *x, int64_t rows, int64_t cols, int64_t logical_rows,
+                       uint8_t *q, uint8_t *s, void *stream) {
+  if (int e = check_rows(rows, logical_rows)) return e;
+  if (cols <= 0 || cols % 32 != 0 || cols > kMaxMxCols) return MHC_ERR_SHAPE;
+  if (rows == 0) return MHC_OK;
+  if (!x || !q || !s) return MHC_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return MHC_ERR_ALIGN;
+  const size_t n = (size_t)rows * (size_t)cols;
+  const Span sp[] = {span(x, n * 2), span(q, n), span(s, n / 32)};
+  for (int a = 0; a < 3; ++a)
+    for (int b = a + 1; b < 3; ++b)
+      if (overlap(sp[a], sp[b])) return MHC_ERR_OVERLAP;
+  if (int e = check_device()) return e;
+  cudaError_t ce = mhc::launch_mx_quantize(x, rows, cols, logical_rows, q, s,
+                                           static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+}
+
+size_t mhc_swizzle_scales_128x4_bytes(int64_t rows, int64_t groups) {
+  if (rows <= 0 || groups <= 0 || rows > kMaxRows || groups > kMaxMxCols / 32) return 0;
+  return (size_t)((rows + 127) / 128 * 128) * (size_t)groups;
+}
+
+int mhc_swizzle_scales_128x4(const uint8_t *s, int64_t rows, int64_t groups, uint8_t *out,
+                             void *stream) {
+  if (rows < 0 || rows > kMaxRows) return MHC_ERR_SHAPE;
+  if (groups <= 0 || groups % 4 != 0 || groups > kMaxMxCols / 32) return MHC_ERR_SHAPE;
+  if (rows == 0) return MHC_OK;
+  if (!s || !out) return MHC_ERR_NULL;
+  if (!aligned16(s) || !aligned16(out)) return MHC_ERR_ALIGN;
+  if (overlap(span(s, (size_t)rows * (size_t)groups),
+              span(out, mhc_swizzle_scales_128x4_bytes(rows, groups))))
+    return MHC_ERR_OVERLAP;
+  if (int e = check_device()) return e;
+  cudaError_t ce = mhc::launch_mx_swizzle(s, rows, groups, out, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 
 int64_t mhc_pre_noalloc_max_rows(void) { return mhc::noalloc_max_rows(); }

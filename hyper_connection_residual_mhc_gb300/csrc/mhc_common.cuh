@@ -69,6 +69,43 @@ __device__ __forceinline__ void post_chunk(const uint4 (&rv)[kHC], const uint4 &
   }
 }
 
+// ---- MXFP8: E4M3 codes with a ue8m0 scale per 32 values ---------------------
+// (prefill_sp.py, _mxfp8_quantize: per row, per 32 columns.)  The scale rule
+// is the OCP Microscaling (MX) v1.0 conversion for E4M3, whose largest
+// exponent is 8: e = floor(log2 amax) - 8, clamped below at -127 (a zero or
+// tiny block), scale code e + 127; each value becomes E4M3(v / 2^e), rounded
+// to nearest-even and saturated to +-448, the sign kept.
+constexpr int kMxBlock = 32;
+// One block is held by 4 consecutive lanes (lane & ~3 .. | 3), 8 values each
+// in column order; v holds the values exactly (bf16 widened).  Every lane of
+// the warp must call this together.  Returns the 8 codes (first value in the
+// lowest byte) and sets the block's scale code.
+__device__ __forceinline__ uint2 mx_block8(const float (&v)[8], uint32_t &scale_code) {
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  // amax >= 0, so its bits are the biased exponent and the mantissa; a zero
+  // or subnormal amax (biased exponent 0) takes the clamp
+  const int biased = (int)(__float_as_uint(amax) >> 23);
+  const int e = max(biased - 127 - 8, -127);
+  scale_code = (uint32_t)(e + 127);
+  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, exact, normal
+  uint32_t w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint16_t p01, p23;
+    // cvt ... d, a, b packs a into the high byte and b into the low byte
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+        : "=h"(p01) : "f"(v[4 * h + 1] * inv), "f"(v[4 * h] * inv));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+        : "=h"(p23) : "f"(v[4 * h + 3] * inv), "f"(v[4 * h + 2] * inv));
+    w[h] = (uint32_t)p01 | ((uint32_t)p23 << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
 // Streaming (evict-first) 16-byte global accesses for data touched once.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
@@ -177,11 +214,23 @@ size_t fn_img_bytes();
 cudaError_t launch_fn_img_prep(const float *fn, uint8_t *img, cudaStream_t s);
 // combine + RMSNorm with a fifth warp per row block for the Sinkhorn of the
 // comb logits (writes comb [rows, 4, 4])
+// mx_q / mx_s non-NULL: the same launch also writes x_norm's MXFP8 codes
+// [rows, 5120] and linear ue8m0 scales [rows, 160] (mx_block8 of the bf16
+// x_norm values)
 cudaError_t launch_combine_norm_sinkhorn(const uint16_t *R, const float *pre,
                                          const uint16_t *norm_w, float norm_eps,
                                          const float *logit, float *comb, float sink_eps,
                                          int iters, int64_t rows, int64_t logical_rows,
-                                         uint16_t *x_norm, cudaStream_t s);
+                                         uint16_t *x_norm, cudaStream_t s,
+                                         uint8_t *mx_q = nullptr, uint8_t *mx_s = nullptr);
+// MXFP8 of bf16 rows x [rows, cols] (cols a multiple of 32): codes q [rows,
+// cols], linear scales s [rows, cols/32]
+cudaError_t launch_mx_quantize(const uint16_t *x, int64_t rows, int64_t cols,
+                               int64_t logical_rows, uint8_t *q, uint8_t *s, cudaStream_t st);
+// linear scales s [rows, groups] -> the 128x4 tiled layout, ceil(rows/128)*128
+// *groups bytes, padding rows zero (groups a multiple of 4)
+cudaError_t launch_mx_swizzle(const uint8_t *s, int64_t rows, int64_t groups, uint8_t *out,
+                              cudaStream_t st);
 // the same stats kernel built for hc_head's 4 mixes: writes the gates to
 // pre_ws [rows, 4] (+ pre_out, mix_out [rows, 4])
 cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *scale,

@@ -148,10 +148,15 @@ static_assert(kChunksPerStream % kCnThreads == 0, "");
 
 // One row by one 128-thread block: y = sum_i pv_i R_i in fp32, then x_norm
 // (kNorm) or y itself, cast once to bf16.
-template <bool kNorm>
+// kMx: the block also writes x_norm's MXFP8 codes (mxq, 8 per chunk) and
+// linear block scales (mxs): a 32-column block is 4 consecutive chunks, held
+// by 4 consecutive lanes.
+template <bool kNorm, bool kMx = false>
 __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const float (&pv)[kHC],
                                             const uint4 *__restrict__ w, float norm_eps,
-                                            uint4 *__restrict__ out, int64_t row) {
+                                            uint4 *__restrict__ out, int64_t row,
+                                            uint2 *__restrict__ mxq = nullptr,
+                                            uint8_t *__restrict__ mxs = nullptr) {
   const int tid = threadIdx.x;
   const uint4 *r = R + row * (kHC * kChunksPerStream);
 
@@ -198,7 +203,16 @@ __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const f
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = (y[q][e] * rn) * wf[e];
-      st_stream(o + c, pack8_rn(v));
+      const uint4 xb = pack8_rn(v);
+      st_stream(o + c, xb);
+      if constexpr (kMx) {
+        float vb[8];
+        unpack8(xb, vb);                 // the bf16 values, as stored
+        uint32_t sc;
+        const uint2 codes = mx_block8(vb, sc);
+        __stcs(mxq + row * kChunksPerStream + c, codes);
+        if ((tid & 3) == 0) mxs[row * (kH / kMxBlock) + (c >> 2)] = (uint8_t)sc;
+      }
     }
   }
 }
@@ -226,12 +240,12 @@ __device__ __forceinline__ void sinkhorn_row(const float *__restrict__ logit,
 
 // kSink: a fifth warp runs the row's Sinkhorn while the four combine warps
 // stream R (the stats launch leaves the comb logits in the workspace).
-template <bool kNorm, bool kSink>
+template <bool kNorm, bool kSink, bool kMx = false>
 __global__ void __launch_bounds__(kCnThreads + 32)
 combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
                     const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out,
                     const float *__restrict__ logit, float *__restrict__ comb, float sink_eps,
-                    int iters) {
+                    int iters, uint2 *__restrict__ mxq, uint8_t *__restrict__ mxs) {
   pdl_wait();
   pdl_trigger();
   // last rows first: after mhc_pre's stats launch the most recently read rows
@@ -243,7 +257,7 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
   }
   const float4 pq = __ldg(pre + row);
   const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
-  combine_row<kNorm>(R, pv, w, norm_eps, out, row);
+  combine_row<kNorm, kMx>(R, pv, w, norm_eps, out, row, mxq, mxs);
 }
 
 }  // namespace
@@ -261,25 +275,36 @@ cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint1
   return launch_pdl(combine_norm_kernel<true, false>, dim3((unsigned)rows), dim3(kCnThreads), 0, s,
                     1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
                     reinterpret_cast<const uint4 *>(norm_w), norm_eps,
-                    reinterpret_cast<uint4 *>(x_norm), nullptr, nullptr, 0.f, 0);
+                    reinterpret_cast<uint4 *>(x_norm), nullptr, nullptr, 0.f, 0,
+                    (uint2 *)nullptr, (uint8_t *)nullptr);
 }
 
 cudaError_t launch_combine_norm_sinkhorn(const uint16_t *R, const float *pre,
                                          const uint16_t *norm_w, float norm_eps,
                                          const float *logit, float *comb, float sink_eps,
                                          int iters, int64_t rows, int64_t logical_rows,
-                                         uint16_t *x_norm, cudaStream_t s) {
+                                         uint16_t *x_norm, cudaStream_t s, uint8_t *mx_q,
+                                         uint8_t *mx_s) {
+  if (mx_q)
+    return launch_pdl(combine_norm_kernel<true, true, true>, dim3((unsigned)rows),
+                      dim3(kCnThreads + 32), 0, s, 1, use_pdl(logical_rows),
+                      reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
+                      reinterpret_cast<const uint4 *>(norm_w), norm_eps,
+                      reinterpret_cast<uint4 *>(x_norm), logit, comb, sink_eps, iters,
+                      reinterpret_cast<uint2 *>(mx_q), mx_s);
   return launch_pdl(combine_norm_kernel<true, true>, dim3((unsigned)rows), dim3(kCnThreads + 32),
                     0, s, 1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R),
                     reinterpret_cast<const float4 *>(pre), reinterpret_cast<const uint4 *>(norm_w),
-                    norm_eps, reinterpret_cast<uint4 *>(x_norm), logit, comb, sink_eps, iters);
+                    norm_eps, reinterpret_cast<uint4 *>(x_norm), logit, comb, sink_eps, iters,
+                    (uint2 *)nullptr, (uint8_t *)nullptr);
 }
 
 cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows,
                                 int64_t logical_rows, uint16_t *y, cudaStream_t s) {
   return launch_pdl(combine_norm_kernel<false, false>, dim3((unsigned)rows), dim3(kCnThreads), 0, s,
                     1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
-                    nullptr, 0.f, reinterpret_cast<uint4 *>(y), nullptr, nullptr, 0.f, 0);
+                    nullptr, 0.f, reinterpret_cast<uint4 *>(y), nullptr, nullptr, 0.f, 0,
+                    (uint2 *)nullptr, (uint8_t *)nullptr);
 }
 
 cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *scale,

@@ -359,6 +359,58 @@ int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const fl
                 void *workspace, size_t workspace_bytes, uint16_t *y, float *pre_out,
                 float *mix_out, void *stream);
 
+/*
+ * MXFP8 output of x_norm -- the attention input as fp8 codes with one
+ * power-of-two scale per 32 values.
+ *
+ * prefill_sp.py, _mxfp8_quantize and mxfp8_gather: each rank quantizes its
+ * bf16 rows per row and per 32 columns (linear scale layout), and
+ * swizzle_128x4 tiles the chunk's scales for the GEMM that reads them.  The
+ * pages call a library quantizer and do not state its rule; libmhc takes the
+ * OCP Microscaling Formats (MX) v1.0 conversion to E4M3:
+ *   amax = max |x| over the block (x as bf16, i.e. x_norm's stored values)
+ *   e    = floor(log2 amax) - 8, at least -127 (e = -127 for amax = 0)
+ *   s    = e + 127                     ue8m0 code of the scale 2^e
+ *   q_k  = E4M3(x_k / 2^e)             round to nearest-even, saturate to
+ *                                      +-448, sign kept (-0 gives 0x80)
+ * Values must be finite.
+ *
+ * mhc_pre_mxfp8(R, w, scale, base, norm_w, rows, logical_rows, p, workspace,
+ *               workspace_bytes, x_norm, x_q, x_s, post, comb, stream)
+ *   mhc_pre_prepared (same arguments, checks and bits) that also writes
+ *   x_q [rows, 5120] uint8 E4M3 codes and x_s [rows, 160] uint8 scales of
+ *   x_norm, both device, 16-byte aligned, overlapping nothing else.  Chunks
+ *   of more than 48 rows: the combine + RMSNorm launch writes them beside
+ *   x_norm; decode-size chunks: one more launch after the decode kernel.
+ *   MHC_ERR_NULL if x_q or x_s is NULL.
+ * mhc_quantize_mxfp8(x, rows, cols, logical_rows, q, s, stream)
+ *   The same quantization of any bf16 rows: x [rows, cols] bf16 (cols a
+ *   multiple of 32, at most 65536), q [rows, cols] uint8, s [rows, cols/32]
+ *   uint8 (linear layout), all device, 16-byte aligned, no overlap.
+ *   logical_rows as for mhc_pre (launch shape only).  MHC_ERR_SHAPE for a
+ *   bad rows/cols; rows = 0 launches nothing.
+ * mhc_swizzle_scales_128x4(s, rows, groups, out, stream)
+ *   s [rows, groups] uint8 linear scales (groups a multiple of 4, at most
+ *   2048) -> out, mhc_swizzle_scales_128x4_bytes(rows, groups) =
+ *   ceil(rows/128)*128*groups bytes: rows padded with zero scales to a
+ *   multiple of 128; tile (m/128, g/4) is the (m/128 * groups/4 + g/4)-th
+ *   run of 512 bytes, inside which (m, g) sits at byte
+ *   (m%32)*16 + ((m%128)/32)*4 + g%4.  Device buffers, 16-byte aligned, not
+ *   overlapping.  Run it on the whole chunk's scales (a shard's rows do not
+ *   in general fill whole 128-row tiles).
+ * All enqueue on `stream` and return MHC_OK or an MHC_ERR_* code, as mhc_pre.
+ */
+int mhc_pre_mxfp8(const uint16_t *R, const mhc_weights *w, const float *scale, const float *base,
+                  const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
+                  const mhc_params *p, void *workspace, size_t workspace_bytes,
+                  uint16_t *x_norm, uint8_t *x_q, uint8_t *x_s, float *post, float *comb,
+                  void *stream);
+int mhc_quantize_mxfp8(const uint16_t *x, int64_t rows, int64_t cols, int64_t logical_rows,
+                       uint8_t *q, uint8_t *s, void *stream);
+size_t mhc_swizzle_scales_128x4_bytes(int64_t rows, int64_t groups);
+int mhc_swizzle_scales_128x4(const uint8_t *s, int64_t rows, int64_t groups, uint8_t *out,
+                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -211,3 +211,32 @@ def test_fused_prepared_null_handle(lib):
         fake(0), fake(1), fake(2), fake(3), None, fake(5), fake(6), fake(7), 4, 4,
         ctypes.byref(p), fake(9), lib.mhc_pre_workspace_bytes(4), fake(10), fake(11), fake(12),
         fake(13), None, None, None) == ERR_NULL
+
+
+def test_mxfp8_host_checks(lib):
+    import hyper_connection_residual_mhc_gb300 as m
+    p = m.default_params()
+    # pre: a NULL handle, then (through the shared checks) NULL codes
+    assert lib.mhc_pre_mxfp8(fake(0), None, fake(2), fake(3), fake(4), 4, 4, ctypes.byref(p),
+                             fake(9), lib.mhc_pre_workspace_bytes(4), fake(5), fake(10),
+                             fake(11), fake(6), fake(7), None) == ERR_NULL
+    q = lib.mhc_quantize_mxfp8
+    assert q(fake(0), 4, 48, 4, fake(1), fake(2), None) == ERR_SHAPE          # cols % 32
+    assert q(fake(0), 4, 0, 4, fake(1), fake(2), None) == ERR_SHAPE
+    assert q(fake(0), 4, 1 << 17, 4, fake(1), fake(2), None) == ERR_SHAPE     # too wide
+    assert q(fake(0), 4, 64, 2, fake(1), fake(2), None) == ERR_SHAPE          # logical < rows
+    assert q(fake(0), 0, 64, 0, None, None, None) == 0                        # empty: no launch
+    assert q(None, 4, 64, 4, fake(1), fake(2), None) == ERR_NULL
+    assert q(fake(0), 4, 64, 4, fake(1) + 8, fake(2), None) == ERR_ALIGN
+    assert q(fake(0), 4, 64, 4, fake(0) + 256, fake(2), None) == ERR_OVERLAP  # codes on x
+    assert q(fake(0), 4, 64, 4, fake(1), fake(1) + 128, None) == ERR_OVERLAP  # scales on codes
+    sw = lib.mhc_swizzle_scales_128x4
+    assert lib.mhc_swizzle_scales_128x4_bytes(1, 160) == 128 * 160
+    assert lib.mhc_swizzle_scales_128x4_bytes(129, 8) == 256 * 8
+    assert lib.mhc_swizzle_scales_128x4_bytes(0, 8) == 0
+    assert sw(fake(0), 4, 6, fake(1), None) == ERR_SHAPE                      # groups % 4
+    assert sw(fake(0), -1, 8, fake(1), None) == ERR_SHAPE
+    assert sw(fake(0), 0, 8, None, None) == 0
+    assert sw(None, 4, 8, fake(1), None) == ERR_NULL
+    assert sw(fake(0) + 4, 4, 8, fake(1), None) == ERR_ALIGN
+    assert sw(fake(0), 4, 8, fake(0) + 16, None) == ERR_OVERLAP
