@@ -1,5 +1,6 @@
 // abi.cu -- the extern "C" entry points of libmhc: host-side validation, then
 // the internal launchers.  Nothing here allocates device memory.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -46,14 +47,16 @@ int check_device() {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  static int ok_mask = 0;  // bit d set: device d verified
-  if (dev >= 0 && dev < 31 && (ok_mask >> dev) & 1) return MHC_OK;
+  // bit d set: device d verified (callers may come from several host threads)
+  static std::atomic<unsigned> ok_mask{0u};
+  if (dev >= 0 && dev < 32 && (ok_mask.load(std::memory_order_relaxed) >> dev) & 1u)
+    return MHC_OK;
   int major = 0, minor = 0;
   e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (major != 10 || minor != 3) return MHC_ERR_DEVICE;
-  if (dev >= 0 && dev < 31) ok_mask |= 1 << dev;
+  if (dev >= 0 && dev < 32) ok_mask.fetch_or(1u << dev, std::memory_order_relaxed);
   return MHC_OK;
 }
 
@@ -75,7 +78,9 @@ const char *mhc_strerror(int code) {
   switch (code) {
     case MHC_OK: return "ok";
     case MHC_ERR_NULL: return "a required pointer is NULL";
-    case MHC_ERR_SHAPE: return "bad row count (rows < 0, logical_rows < rows, or too many rows)";
+    case MHC_ERR_SHAPE:
+      return "bad shape (rows < 0, logical_rows < rows, too many rows, or a bad column or "
+             "group count)";
     case MHC_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
     case MHC_ERR_PARAM: return "bad scalar parameter (eps < 0 or not finite, iterations < 1)";
     case MHC_ERR_OVERLAP: return "an output buffer overlaps an input buffer";

@@ -57,7 +57,7 @@ extern "C" {
 /* return codes */
 #define MHC_OK 0
 #define MHC_ERR_NULL (-1)        /* a required pointer is NULL */
-#define MHC_ERR_SHAPE (-2)       /* rows < 0, logical_rows < rows, or rows too large */
+#define MHC_ERR_SHAPE (-2)       /* rows < 0, logical_rows < rows, rows too large, or a bad column / group count */
 #define MHC_ERR_ALIGN (-3)       /* a tensor pointer is not 16-byte aligned */
 #define MHC_ERR_PARAM (-4)       /* eps < 0 or not finite, iters < 1, ... */
 #define MHC_ERR_OVERLAP (-5)     /* an output buffer overlaps an input buffer */
