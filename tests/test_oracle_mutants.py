@@ -57,6 +57,22 @@ MUTANTS = [
     ("combine: streams interleaved",
      "acc += pre[m * O_HC + i] * oracle_bf16_to_double(row[i * O_H + h]);",
      "acc += pre[m * O_HC + i] * oracle_bf16_to_double(row[h * O_HC + i]);", MAIN_PINS),
+    ("combine: every row gated by row 0",
+     "acc += pre[m * O_HC + i] * oracle_bf16_to_double(row[i * O_H + h]);",
+     "acc += pre[i] * oracle_bf16_to_double(row[i * O_H + h]);", MAIN_PINS),
+    ("sinkhorn: one iteration short", "for (int t = 0; t < iters; ++t)",
+     "for (int t = 0; t < iters - 1; ++t)", MAIN_PINS),
+    ("split: logit without base",
+     "l[c] = mix[m * O_MIX + c] * (double)scale[g] + (double)base[c];",
+     "l[c] = mix[m * O_MIX + c] * (double)scale[g];", MAIN_PINS),
+    ("stats: mix divided by rsqrt", "mix[m * O_MIX + c] = dot * r;",
+     "mix[m * O_MIX + c] = dot / r;", MAIN_PINS),
+    ("bf16: subnormals flushed", "    if (q < -133)\n        q = -133;",
+     "    if (q < -126)\n        q = -126;", MAIN_PINS),
+    ("hc_head: streams interleaved", "acc += p[i] * x[i * O_H + h];",
+     "acc += p[i] * x[h * O_HC + i];", MAIN_PINS),
+    ("post: every row gated by row 0", "double p = (double)post[m * O_HC + i];",
+     "double p = (double)post[i];", MAIN_PINS),
     ("post: comb transposed", "acc += (double)comb[m * 16 + j * 4 + i] *",
      "acc += (double)comb[m * 16 + i * 4 + j] *", MAIN_PINS),
     ("post: sublayer output dropped", "double acc = p * oracle_bf16_to_double(yr[h]);",

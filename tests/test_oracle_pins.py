@@ -271,6 +271,25 @@ def test_combine_norm_one_hot_pre_constant_stream(oracle_mod):
         assert np.all(xn == want), (i, xn[0, :4], want)
 
 
+def test_combine_norm_gates_are_per_row(oracle_mod):
+    # four rows with the same constant streams c_i, row m gated by e_(3-m):
+    # row m's x_norm is the closed form of stream 3-m, so each row must read
+    # its own gates
+    cs = [0.5, -2.0, 0.125, 3.0]
+    R = np.zeros((HC, HC, H), np.uint16)
+    for i, c in enumerate(cs):
+        R[:, i, :] = bf(c)
+    pre = np.zeros((HC, HC))
+    for m in range(HC):
+        pre[m, HC - 1 - m] = 1.0
+    eps = 0.75
+    xn = oracle_mod.combine_norm(R, pre, bf(np.ones(H)), eps)
+    for m in range(HC):
+        c = cs[HC - 1 - m]
+        want = oracle_mod.to_bf16(np.array([c / math.sqrt(c * c + eps)]))[0]
+        assert np.all(xn[m] == want), (m, xn[m, :4], want)
+
+
 def test_combine_norm_weighted_sum_and_per_column_weight(oracle_mod):
     # pre = (a, b, 0, 0) on constant streams: y = a c0 + b c1 everywhere; the
     # weight multiplies column h.  Exact: y/|y| = sign(y) when eps = 0.
