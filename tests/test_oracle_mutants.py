@@ -83,6 +83,27 @@ MUTANTS = [
      "p[c] = sigmoid(mx * (double)scale[0] + (double)base[c] + hc_eps);", MAIN_PINS),
     ("hc_head: rsqrt without eps", "double r = 1.0 / sqrt(ss / (double)O_K + norm_eps);",
      "double r = 1.0 / sqrt(ss / (double)O_K);", MAIN_PINS),
+    ("stats: every row's mix in row 0", "mix[m * O_MIX + c] = dot * r;", "mix[c] = dot * r;",
+     MAIN_PINS),
+    ("split: every row's pre in row 0", "pre[m * O_HC + i] = sigmoid(l[i]) + pre_eps;",
+     "pre[i] = sigmoid(l[i]) + pre_eps;", MAIN_PINS),
+    ("stats: fn row stride dropped",
+     "const float *f = fn + (int64_t)c * O_K;\n            double dot = 0.0;\n            "
+     "for (int k = 0; k < O_K; ++k)\n                dot += x[k] * (double)f[k];\n            "
+     "mix[m * O_MIX + c]",
+     "const float *f = fn + (int64_t)c;\n            double dot = 0.0;\n            "
+     "for (int k = 0; k < O_K; ++k)\n                dot += x[k] * (double)f[k];\n            "
+     "mix[m * O_MIX + c]", MAIN_PINS),
+    ("sinkhorn: row step sums a column",
+     "for (int i = 0; i < O_HC; ++i)\n                    s += C[j][i];",
+     "for (int i = 0; i < O_HC; ++i)\n                    s += C[i][j];", MAIN_PINS),
+    ("post: output streams interleaved",
+     "R_out[m * (int64_t)O_K + i * O_H + h] = oracle_double_to_bf16(acc);",
+     "R_out[m * (int64_t)O_K + i + h * O_HC] = oracle_double_to_bf16(acc);", MAIN_PINS),
+    ("split: comb written transposed", "comb[m * 16 + j * 4 + i] = C[j][i];",
+     "comb[m * 16 + j * 4 + i] = C[i][j];", MAIN_PINS),
+    ("combine: eps outside the sqrt", "double rn = 1.0 / sqrt(ss / (double)O_H + norm_eps);",
+     "double rn = 1.0 / (sqrt(ss / (double)O_H) + norm_eps);", MAIN_PINS),
     ("mxfp8: scale exponent off by one", "e = (ex - 1) - 8;", "e = ex - 8;", MX_PINS),
     ("mxfp8: ties away from zero", "double t = ldexp(nearbyint(ldexp(a, -q)), q);",
      "double t = ldexp(round(ldexp(a, -q)), q);", MX_PINS),
