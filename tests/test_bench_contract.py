@@ -37,3 +37,22 @@ def test_warmup_below_three_is_refused():
                           "--steps", "1", "--warmup", "2"], cwd=ROOT, capture_output=True,
                          text=True, timeout=120)
     assert out.returncode != 0
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    # launched as for N > 1: rank 0 alone runs and prints, the other rank
+    # exits 0 without output
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                          "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
