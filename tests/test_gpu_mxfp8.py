@@ -37,8 +37,8 @@ def _bf(torch, bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def _bits(t):
-    return t.cpu().view(dtype=__import__("torch").int16).numpy().view(np.uint16)
+def _bits(torch, t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
 def special_rows(rows, cols, seed):
@@ -94,7 +94,7 @@ def test_pre_mxfp8(torch, mhc, rows):
     xn, q, s, post, comb = mhc.mhc_pre_mxfp8(R, h, scale, base, w)
     torch.cuda.synchronize()
     assert torch.equal(xn, xn_ref) and torch.equal(post, post_ref) and torch.equal(comb, comb_ref)
-    q_ref, s_ref = oracle.mxfp8_quantize(_bits(xn))
+    q_ref, s_ref = oracle.mxfp8_quantize(_bits(torch, xn))
     assert np.array_equal(s.cpu().numpy(), s_ref)
     assert np.array_equal(q.cpu().numpy(), q_ref)
     # the whole chunk's scales, tiled: the oracle's tiling of the same bytes
