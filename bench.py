@@ -639,7 +639,10 @@ def run_op(args):
                        "graph_us": graph_us, "graph_chain": args.chain},
             "roofline": {"bound": "latency", "algorithmic_bytes_per_step": nbytes,
                          "achieved_gbs_graph": nbytes / (graph_us * 1e-6) / 1e9},
-            "gpu_launches": (3 if LM > 48 else (1 if args.fused else 2)) * args.steps * args.chain,
+            # per step: prefill sizes 3 (stats, combine, post) or, fused with fn
+            # prepared, 2 (fused kernel, combine); decode sizes 2, or 1 fused
+            "gpu_launches": ((2 if args.fused else 3) if LM > 48 else (1 if args.fused else 2))
+                            * args.steps * args.chain,
         }
         print(json.dumps(line), flush=True)
         return
