@@ -55,26 +55,32 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 
-    def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src) + f".{os.getpid()}.o")
+    srcs = _sources()
+    objs = [os.path.join(OUT_DIR, os.path.basename(src) + f".{os.getpid()}.o") for src in srcs]
+
+    def compile_one(src_obj):
+        src, obj = src_obj
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
         if verbose_ptxas:
             sys.stderr.write(r.stderr)
-        return obj
 
-    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(compile_one, _sources()))
     tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    for o in objs:
-        os.remove(o)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    try:
+        with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+            list(ex.map(compile_one, zip(srcs, objs)))
+        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True,
+                           text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, LIB)
+    finally:
+        # no objects or partial libraries are left behind, whatever failed
+        for f in objs + [tmp]:
+            if os.path.exists(f):
+                os.remove(f)
     return LIB
 
 
