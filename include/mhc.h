@@ -8,7 +8,11 @@
  *   pre : stats -> split/Sinkhorn -> combine + RMSNorm  (feeds the sublayer)
  *   post: new residual from the sublayer output          (after the sublayer)
  * as defined in deepseek_v4.py (sglang), DeepseekV4DecoderLayer.hc_pre and
- * DeepseekV4DecoderLayer.hc_post.
+ * DeepseekV4DecoderLayer.hc_post.  Beside mhc_pre and mhc_post: the two fused
+ * across a sublayer boundary (mhc_fused_post_pre), the model's final stream
+ * collapse (mhc_hc_head), prepared weights (mhc_prepare_weights and the
+ * *_prepared calls) and MXFP8 output of the normalised input (mhc_pre_mxfp8,
+ * mhc_quantize_mxfp8, mhc_swizzle_scales_128x4).
  *
  * Conventions for every entry point below
  *  - All tensor arguments are DEVICE pointers, owned by the caller, row-major
@@ -35,9 +39,10 @@
  *  - Arguments are validated on the host before any launch; on an error the
  *    call returns a negative code, launches nothing and writes nothing.
  *  - Output buffers must not overlap any input buffer.
- *  - No call allocates device memory.  Scratch space, where an entry point
- *    needs it, is passed in by the caller (`workspace`), except for
- *    mhc_pre_noalloc, which uses a fixed array inside the library.
+ *  - No call allocates device memory except mhc_prepare_weights (its
+ *    handle's 5.9 MB, freed by mhc_release_weights).  Scratch space, where an
+ *    entry point needs it, is passed in by the caller (`workspace`), except
+ *    for mhc_pre_noalloc, which uses a fixed array inside the library.
  */
 #ifndef MHC_H
 #define MHC_H
