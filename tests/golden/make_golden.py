@@ -36,6 +36,7 @@ def main():
     post32 = o["post"].astype("float32")
     comb32 = o["comb"].astype("float32")
     r_out = oracle.post(R, y, post32, comb32)
+    q, sc = oracle.mxfp8_quantize(o["x_norm"])
     fixture = {
         "what": "oracle outputs on rows 0..7 of the M=128 seed-0 workload (regression only)",
         "inputs": {"seed": 0, "rows": ROWS, "rms_eps": 1e-6, "hc_pre_eps": 1e-6,
@@ -49,6 +50,10 @@ def main():
         "x_norm_row0_first8": [int(v) for v in o["x_norm"][0, :8]],
         "r_out_sha256": digest(r_out),
         "r_out_row0_stream1_first8": [int(v) for v in r_out[0, 1, :8]],
+        "x_norm_mxfp8_codes_sha256": digest(q),
+        "x_norm_mxfp8_scales_sha256": digest(sc),
+        "x_norm_mxfp8_scales_row0": [int(v) for v in sc[0]],
+        "x_norm_mxfp8_scales_128x4_sha256": digest(oracle.swizzle_128x4(sc)),
     }
     with open(os.path.join(HERE, "oracle_m128_seed0_rows0-7.json"), "w") as f:
         json.dump(fixture, f, indent=1)

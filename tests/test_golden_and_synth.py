@@ -32,6 +32,11 @@ def test_oracle_matches_stored_regression_fixture(oracle_mod):
     assert _digest(o["x_norm"]) == g["x_norm_sha256"]
     r_out = oracle_mod.post(R, y, o["post"].astype(np.float32), o["comb"].astype(np.float32))
     assert _digest(r_out) == g["r_out_sha256"]
+    q, sc = oracle_mod.mxfp8_quantize(o["x_norm"])
+    assert [int(v) for v in sc[0]] == g["x_norm_mxfp8_scales_row0"]
+    assert _digest(sc) == g["x_norm_mxfp8_scales_sha256"]
+    assert _digest(q) == g["x_norm_mxfp8_codes_sha256"]
+    assert _digest(oracle_mod.swizzle_128x4(sc)) == g["x_norm_mxfp8_scales_128x4_sha256"]
 
 
 def test_generator_is_counter_based_and_sliceable():
