@@ -128,20 +128,22 @@ int mhc_kernel_status_detail(uint32_t *where64) {
 
 int mhc_kernel_status(uint32_t *status, int reset) {
   if (!status) return MHC_ERR_NULL;
-  unsigned int w = 0, w2 = 0, w3 = 0;
+  unsigned int w = 0, w2 = 0, w3 = 0, w4 = 0;
   cudaError_t e = mhc::fused_error_word(&w, reset != 0);
   if (e == cudaSuccess) e = mhc::fused_post_pre_error_word(&w2, reset != 0);
   if (e == cudaSuccess) e = mhc::head_error_word(&w3, reset != 0);
+  if (e == cudaSuccess) e = mhc::onepass_error_word(&w4, reset != 0);
   if (e != cudaSuccess) return cuda_fail(e);
-  *status = w | w2 | w3;
+  *status = w | w2 | w3 | w4;
   return MHC_OK;
 }
 
 namespace {
 // mhc_pre, mhc_pre_prepared and mhc_pre_mxfp8: fn is the fp32 weight (the
-// caller's, or the handle's copy); fn_img is NULL or the handle's operand
-// image; mx_q / mx_s are NULL or x_norm's MXFP8 codes and linear scales
-int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const float *scale,
+// caller's, or the handle's copy); fn_b_img is NULL or the handle's image of
+// fn's operand tiles; mx_q / mx_s are NULL or x_norm's MXFP8 codes and linear
+// scales
+int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_b_img, const float *scale,
              const float *base, const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
              const mhc_params *p_in, void *workspace, size_t workspace_bytes, uint16_t *x_norm,
              float *post, float *comb, float *pre_out, float *mix_out, void *stream,
@@ -190,25 +192,21 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_img, const fl
 
   if (int e = check_device()) return e;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float *pre_ws = static_cast<float *>(workspace);
   cudaError_t ce;
   if (logical_rows <= mhc::kDecodeMaxRows) {
     // decode-size chunk: latency-shaped CUDA-core path (keyed on the chunk's
     // row count, so every shard of the chunk takes it)
     ce = mhc::launch_pre_decode(R, fn, scale, base, norm_w, rows, logical_rows, p, x_norm, post,
-                                comb, pre_out, mix_out, s, /*fn_stable=*/fn_img != nullptr);
+                                comb, pre_out, mix_out, s, /*fn_stable=*/fn_b_img != nullptr);
     // the decode kernel writes bf16 x_norm only; its MXFP8 follows in a
     // second, streaming launch
     if (ce == cudaSuccess && mx_q)
       ce = mhc::launch_mx_quantize(x_norm, rows, MHC_HIDDEN, logical_rows, mx_q, mx_s, s);
   } else {
-    float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
-    ce = mhc::launch_pre_stats(R, fn, fn_img, scale, base, rows, logical_rows, p, pre_ws, logit_ws,
-                               post, pre_out, mix_out, s);
-    if (ce == cudaSuccess)
-      ce = mhc::launch_combine_norm_sinkhorn(R, pre_ws, norm_w, p.norm_eps, logit_ws, comb,
-                                             p.hc_sinkhorn_eps, p.sinkhorn_iters, rows,
-                                             logical_rows, x_norm, s, mx_q, mx_s);
+    // one launch that reads R from HBM once (fn's operand tiles from the
+    // handle's image when prepared)
+    ce = mhc::launch_pre_onepass(R, fn, fn_b_img, scale, base, norm_w, rows, logical_rows, p,
+                                 x_norm, post, comb, pre_out, mix_out, s, mx_q, mx_s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
@@ -226,7 +224,7 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
 struct mhc_weights {
   int device;
   float *fn32;      // device copy of fn [24, 20480] fp32 (decode paths)
-  uint8_t *img;     // the stats kernel's bf16 hi/lo B-tile image of all 16 cluster ranks
+  uint8_t *img;     // the one-pass pre kernel's bf16 hi/lo operand tiles of fn, all 16 ranks
   uint8_t *img64;   // the fused post -> pre kernel's image (64-byte swizzled 32-k blocks)
 };
 
@@ -247,7 +245,8 @@ int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream) {
     delete w;
   };
   ce = cudaMalloc(reinterpret_cast<void **>(&w->fn32), fn_bytes);
-  if (ce == cudaSuccess) ce = cudaMalloc(reinterpret_cast<void **>(&w->img), mhc::fn_img_bytes());
+  if (ce == cudaSuccess)
+    ce = cudaMalloc(reinterpret_cast<void **>(&w->img), mhc::fn_b_img_bytes());
   if (ce == cudaSuccess)
     ce = cudaMalloc(reinterpret_cast<void **>(&w->img64), mhc::fused_fn_bytes());
   if (ce != cudaSuccess) {
@@ -257,7 +256,7 @@ int mhc_prepare_weights(const float *fn, mhc_weights **out, void *stream) {
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   ce = cudaMemcpyAsync(w->fn32, fn, fn_bytes, cudaMemcpyDeviceToDevice, s);
-  if (ce == cudaSuccess) ce = mhc::launch_fn_img_prep(fn, w->img, s);
+  if (ce == cudaSuccess) ce = mhc::launch_fn_b_img(fn, w->img, s);
   if (ce == cudaSuccess) ce = mhc::launch_fn_prep_sw64(fn, w->img64, s, false);
   if (ce != cudaSuccess) {
     drop();

@@ -268,6 +268,25 @@ cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset);
 cudaError_t fused_error_word(unsigned int *out, bool reset);
 cudaError_t fused_error_where(unsigned int *out32);
 
+// all of mhc_pre in one launch of 16-CTA clusters that reads R from HBM once
+// (pre_onepass.cu): 32-row tiles, the four streams of a 64-column block as
+// one MMA operand against fn's hi/lo for all four streams, one cluster
+// exchange per tile, the combine re-reading its tile from L2.  fn_img: NULL,
+// or the prepared-weights image of fn_b_img_bytes() (then fn is not read).
+// mx_q / mx_s non-NULL: x_norm's MXFP8 codes [rows, 5120] and linear ue8m0
+// scales [rows, 160] as well.
+cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t *fn_img,
+                               const float *scale, const float *base, const uint16_t *norm_w,
+                               int64_t rows, int64_t logical_rows, const mhc_params &p,
+                               uint16_t *x_norm, float *post, float *comb, float *pre_out,
+                               float *mix_out, cudaStream_t s, uint8_t *mx_q = nullptr,
+                               uint8_t *mx_s = nullptr);
+// prepared weights: fn [24, 20480] fp32 -> the one-pass kernel's B tiles of
+// all 16 cluster ranks (fn_b_img_bytes() bytes)
+size_t fn_b_img_bytes();
+cudaError_t launch_fn_b_img(const float *fn, uint8_t *img, cudaStream_t s);
+cudaError_t onepass_error_word(unsigned int *out, bool reset);
+
 // allocation-free variant of the CUDA-core pre path (scratch in a static
 // device array of noalloc_max_rows() rows)
 int64_t noalloc_max_rows();
