@@ -68,6 +68,8 @@ def bf16_ulp(x):
 
 
 def _report(name, bad, diff, extra=""):
+    """Raise on any element flagged bad.  Callers flag with ~(d <= tol) so that
+    a NaN difference (a NaN output) counts as out of tolerance."""
     n = int(bad.sum())
     if n:
         idx = np.argwhere(bad)[:5]
@@ -81,7 +83,7 @@ def check_mix(gpu, ref, name="mix"):
     rms = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
     tol = 1e-4 * np.maximum(np.abs(ref), rms)
     d = np.abs(gpu - ref)
-    _report(name, d > tol, d)
+    _report(name, ~(d <= tol), d)
 
 
 def check_gates(gpu_pre, gpu_post, o, scale, R_bits, fn, post_mult=2.0, rms_eps=1e-6):
@@ -105,12 +107,12 @@ def check_gates(gpu_pre, gpu_post, o, scale, R_bits, fn, post_mult=2.0, rms_eps=
         sg = 1.0 / (1.0 + np.exp(-l))
         dl = abs(sc) * dmix[:, lo:lo + 4] + 8 * 2.0 ** -24 * term
         d = np.abs(np.asarray(gpu, np.float64) - np.asarray(ref, np.float64))
-        _report(name, d > np.maximum(1e-6, mult * sg * (1 - sg) * dl), d)
+        _report(name, ~(d <= np.maximum(1e-6, mult * sg * (1 - sg) * dl)), d)
 
 
 def check_abs(gpu, ref, tol, name):
     d = np.abs(np.asarray(gpu, np.float64) - np.asarray(ref, np.float64))
-    _report(name, d > tol, d)
+    _report(name, ~(d <= tol), d)
 
 
 def scaled_column_mask(shape_tail):

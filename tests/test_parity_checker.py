@@ -88,3 +88,25 @@ def test_post_mistakes_are_caught(case, oracle_mod):
     streams[:, [0, 3]] = streams[:, [3, 0]]
     with pytest.raises(AssertionError):
         P.check_bf16(streams, R2, "R_out", term_mag=tm)
+
+
+def test_a_nan_output_is_caught_by_every_check(case):
+    # a NaN compares false against any tolerance: every check must still fail
+    o, W, R = case["o"], case["W"], case["R"]
+    mix = o["mix"].copy()
+    mix[1, 5] = np.nan
+    with pytest.raises(AssertionError):
+        P.check_mix(mix, o["mix"])
+    for key in ("pre", "post"):
+        g = {"pre": o["pre"].copy(), "post": o["post"].copy()}
+        g[key][2, 3] = np.nan
+        with pytest.raises(AssertionError):
+            P.check_gates(g["pre"], g["post"], o, W.scale, R, W.fn)
+    comb = o["comb"].copy()
+    comb[0, 1, 2] = np.nan
+    with pytest.raises(AssertionError):
+        P.check_abs(comb, o["comb"], 1e-6, "comb")
+    xn = o["x_norm"].copy()
+    xn[3, 7] = 0x7FC0   # a bf16 quiet NaN
+    with pytest.raises(AssertionError):
+        P.check_bf16(xn, o["x_norm"], "x_norm")
