@@ -44,27 +44,6 @@
 
 namespace mhc {
 
-#ifdef MHC_TRACE
-// diagnostic builds only: per-CTA timestamps of the phases (slots 0..15)
-__device__ unsigned long long *g_dtrace;
-#define MHC_DTRACE(ev) MHC_DTRACE_BY(0, ev)
-#define MHC_DTRACE_BY(t, ev)                                                        \
-  do {                                                                              \
-    if (g_dtrace && threadIdx.x == (t)) {                                           \
-      unsigned long long t_;                                                        \
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                        \
-      g_dtrace[(size_t)blockIdx.x * 512 + (ev)] = t_;                               \
-    }                                                                               \
-  } while (0)
-#else
-#define MHC_DTRACE(ev) \
-  do {                 \
-  } while (0)
-#define MHC_DTRACE_BY(t, ev) \
-  do {                       \
-  } while (0)
-#endif
-
 namespace {
 
 constexpr int kDCl = 16;                      // CTAs per cluster
@@ -197,7 +176,6 @@ pre_decode_kernel(const DecArgs a) {
   if (a.fn_stable) load_fn();
   pdl_wait();
   if (!a.fn_stable) load_fn();
-  MHC_DTRACE(0);
   float wf[4] = {0.f, 0.f, 0.f, 0.f};
   if (tid < kDQ) {
     const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(a.norm_w + h0));
@@ -219,7 +197,6 @@ pre_decode_kernel(const DecArgs a) {
         xr[r] = r < nr ? __ldg(reinterpret_cast<const uint2 *>(a.R + (row0 + r) * kK + k0))
                        : make_uint2(0u, 0u);
     }
-    MHC_DTRACE(1);
 
     // ---- 1. partials (row loops unrolled with a uniform guard, so the
     // per-row arrays stay in registers) --------------------------------------
@@ -246,7 +223,6 @@ pre_decode_kernel(const DecArgs a) {
       xs[r][si][q] = xr[r];
     }
     __syncthreads();
-    MHC_DTRACE(2);
     for (int t = tid; t < nr * kDPart; t += kDThreads) {
       const int r = t / kDPart, c = t % kDPart;
       float s = red[0][r][c];
@@ -255,7 +231,6 @@ pre_decode_kernel(const DecArgs a) {
       d_st_remote(d_mapa(d_smem_addr(&recv[rank][r][c]), (uint32_t)r), s);
     }
     d_cluster_sync();
-    MHC_DTRACE(3);
 
     // ---- 2. owner of group row `rank` (warp 9, which has no combine work):
     // the gates go to every CTA first; the Sinkhorn then runs while the other
@@ -289,7 +264,6 @@ pre_decode_kernel(const DecArgs a) {
           d_st_remote(d_mapa(d_smem_addr(&pre_all[r][t & 3]), (uint32_t)(t >> 2)), gv);
         }
       }
-      MHC_DTRACE_BY(kOwnerWarp * 32, 4);
       d_cluster_arrive();        // barrier 2: the gates are out
       d_cluster_wait();
       d_cluster_arrive();        // barrier 3: this warp sends no partial sums
@@ -314,12 +288,10 @@ pre_decode_kernel(const DecArgs a) {
           }
         }
       }
-      MHC_DTRACE_BY(kOwnerWarp * 32, 9);
       d_cluster_wait();
       continue;                  // nothing of steps 3 and 4 is this warp's
     }
     d_cluster_sync();            // barrier 2
-    MHC_DTRACE(5);
 
     // ---- 3. y on this CTA's columns; partial sums of y^2 to every CTA --------
     float y[kDRows][4];
@@ -378,9 +350,7 @@ pre_decode_kernel(const DecArgs a) {
       const float s = (red[0][r][0] + red[1][r][0]) + red[2][r][0];
       d_st_remote(d_mapa(d_smem_addr(&sq[rank][r]), (uint32_t)dst), s);
     }
-    MHC_DTRACE(6);
     d_cluster_sync();
-    MHC_DTRACE(7);
 
     // ---- 4. x_norm on this CTA's columns ---------------------------------------
     if (tid < kDQ) {
@@ -400,7 +370,6 @@ pre_decode_kernel(const DecArgs a) {
         *reinterpret_cast<uint2 *>(a.x_norm + (row0 + r) * kH + h0) = o;
       }
     }
-    MHC_DTRACE(8);
   }
   // the next launch may start scheduling once every CTA got here
   pdl_trigger();
@@ -490,11 +459,5 @@ cudaError_t launch_post_pre_decode(const uint16_t *R, const uint16_t *y, const f
   a.p = p;
   return launch_decode<true>(a, logical_rows, s);
 }
-
-#ifdef MHC_TRACE
-extern "C" int mhc_dtrace_set(void *buf) {
-  return (int)cudaMemcpyToSymbol(g_dtrace, &buf, sizeof buf);
-}
-#endif
 
 }  // namespace mhc

@@ -59,21 +59,6 @@ __device__ unsigned int g_fused_error;
 __device__ unsigned int g_fused_where[32];
 __device__ unsigned int g_fused_where_aborted[32];
 
-#ifdef MHC_TRACE
-// Diagnostic builds only: per-CTA timestamps of pipeline events.
-constexpr int kTraceTiles = 32, kTraceEv = 16, kTraceSlots = kTraceTiles * kTraceEv;
-__device__ unsigned long long *g_trace;
-#define MHC_TRACE_AT(tile, ev)                                                         \
-  do {                                                                                 \
-    if (g_trace && (tile) < kTraceTiles)                                               \
-      g_trace[(size_t)blockIdx.x * kTraceSlots + (tile) * kTraceEv + (ev)] = now_ns(); \
-  } while (0)
-#else
-#define MHC_TRACE_AT(tile, ev) \
-  do {                         \
-  } while (0)
-#endif
-
 namespace {
 using namespace ptx;
 
@@ -302,7 +287,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
       const int y = (cid + it * ncl) * kTile;
-      if (lane == 0) MHC_TRACE_AT(it, 0);
       for (int j = 0; j < kKb; ++j) {
         if (!waitw(bar(B_EMPTY + stage), phase ^ 1, false, ab, 1, it)) { ok = false; break; }
         if (lane == 0) {
@@ -314,7 +298,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         last[stage] = (int)phase;
         if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
-      if (lane == 0) MHC_TRACE_AT(it, 1);
     }
     // every copy issued must have landed before the CTA may exit
     for (int s = 0; s < kStages; ++s)
@@ -372,7 +355,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
       for (int q = 0; q < 8; ++q) ssq[q] = 0.f;
       for (int j = 0; j < kKb; ++j) {
         if (!waitw(bar(B_FULL + stage), phase, false, ab, 4, it)) { ok = false; break; }
-        if (j == 0 && warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 2);
         const uint8_t *st = sm + C::kOffStage + stage * kStageBytes + row * 128;
         uint4 cq[8];
 #pragma unroll
@@ -396,7 +378,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      if (warp == kRow0 && lane == 0) MHC_TRACE_AT(it, 3);
       // hand the row's sum x^2 to the readout warps (slot free once tile it-2
       // was read out)
       const int buf = it & 1;
@@ -464,7 +445,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         // all readout warps pushed tile t: tell all 16 owners
         if (!waitw(bar(B_GALL), (uint32_t)(t & 1), false, ab, 7, t)) break;
         if (lane == 0) arrive_all_ctas(bar(B_PREADY), kCl);
-        if (lane == 0) MHC_TRACE_AT(t, 4);
         __syncwarp();
       }
     }
@@ -486,7 +466,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
     for (int it = 0; it < T; ++it) {
       const int64_t grow = (int64_t)(cid + it * ncl) * kTile + row_t;
       if (!waitw(bar(B_PREADY), (uint32_t)(it & 1), true, ab, 8, it)) break;
-      if (warp == kOwnerLead && lane == 0) MHC_TRACE_AT(it, 5);
       // this row's 25 partials from the 16 CTAs, summed in CTA order
       float acc0 = 0.f, acc1 = 0.f;
       if (e <= NM) {
@@ -541,7 +520,6 @@ pre_stats_kernel(const __grid_constant__ CUtensorMap tmap, const StatsArgs a) {
         }
         (void)full;
       }
-      if (warp == kOwnerLead && lane == 0) MHC_TRACE_AT(it, 6);
       (void)gb;
       __syncwarp();
     }
@@ -693,12 +671,6 @@ cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *s
   a.rms_eps = norm_eps; a.pre_eps = hc_eps; a.sink_eps = 0.f; a.post_mult = 0.f; a.iters = 0;
   return launch_stats<kHeadMix>(R, a, logical_rows, s);
 }
-
-#ifdef MHC_TRACE
-extern "C" int mhc_trace_set(void *buf) {
-  return (int)cudaMemcpyToSymbol(g_trace, &buf, sizeof buf);
-}
-#endif
 
 cudaError_t fused_error_word(unsigned int *out, bool reset) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_fused_error, sizeof(unsigned int));

@@ -33,7 +33,7 @@
  *     y = sum_i pre_i * x_i, cast once to the residual's dtype.
  *
  * The body of hc_split_sinkhorn is not on the pages.  The reading used here
- * (each choice is also listed in the design notes):
+ * (each choice is one reading of an open step, not a fact of the pages):
  *   - the 24 mixes split in order [0,4) pre, [4,8) post, [8,24) comb, the
  *     comb block row-major as comb[j][i] = mix[8 + 4*j + i];
  *   - logit_c = mix_c * scale[g] + base_c with g = 0, 1, 2 for pre, post,
