@@ -332,9 +332,8 @@ def mhc_pre_noalloc_max_rows() -> int:
 def mhc_pre_noalloc(R, fn, scale, base, norm_w, x_norm, post, comb, *, logical_rows=None,
                     params=None, pre_out=None, mix_out=None, stream=None):
     """mhc_pre for callers that cannot provide device scratch (see mhc_pre_noalloc
-    in include/mhc.h).  Allocates nothing: every output is passed in.  The first
-    call on a device sets up the scratch address there; make it before any
-    stream capture.  Calls overlapping on the GPU race on the shared scratch."""
+    in include/mhc.h).  Allocates nothing: every output is passed in, and the
+    kernels take no scratch.  The same launches and bits as mhc_pre."""
     import torch
     rows = int(R.shape[0])
     _need(R, "R", torch.bfloat16, (rows, HC, H))

@@ -88,7 +88,7 @@ const char *mhc_strerror(int code) {
     case MHC_ERR_CUDA: return "a CUDA call failed";
     case MHC_ERR_DEVICE: return "the current device is not an sm_103 GPU";
     case MHC_ERR_SCRATCH_LIMIT:
-      return "rows exceed mhc_pre_noalloc's fixed scratch (see mhc_pre_noalloc_max_rows)";
+      return "rows exceed a fixed scratch size (not returned by this build)";
     case MHC_ERR_ALLOC: return "a device allocation failed (mhc_prepare_weights)";
     default: return "unknown libmhc error code";
   }
@@ -147,7 +147,7 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_b_img, const 
              const float *base, const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
              const mhc_params *p_in, void *workspace, size_t workspace_bytes, uint16_t *x_norm,
              float *post, float *comb, float *pre_out, float *mix_out, void *stream,
-             uint8_t *mx_q = nullptr, uint8_t *mx_s = nullptr) {
+             uint8_t *mx_q = nullptr, uint8_t *mx_s = nullptr, bool ws_required = true) {
   mhc_params p;
   if (p_in) p = *p_in; else mhc_default_params(&p);
   if (int e = check_rows(rows, logical_rows)) return e;
@@ -163,7 +163,7 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_b_img, const 
   if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
   if ((mx_q == nullptr) != (mx_s == nullptr)) return MHC_ERR_NULL;
   if (mx_q && (!aligned16(mx_q) || !aligned16(mx_s))) return MHC_ERR_ALIGN;
-  const size_t need = mhc_pre_workspace_bytes(rows);
+  const size_t need = ws_required ? mhc_pre_workspace_bytes(rows) : 0;
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return MHC_ERR_WORKSPACE;
@@ -339,49 +339,17 @@ int mhc_swizzle_scales_128x4(const uint8_t *s, int64_t rows, int64_t groups, uin
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
 
-int64_t mhc_pre_noalloc_max_rows(void) { return mhc::noalloc_max_rows(); }
+int64_t mhc_pre_noalloc_max_rows(void) { return kMaxRows; }
 
-// Allocation-free mhc_pre: same checks as mhc_pre without the workspace, plus
-// the fixed scratch limit; the scratch is libmhc's static device array.
+// Allocation-free mhc_pre: mhc_pre's kernels (the decode-size launch and the
+// one-pass launch) take no scratch, so this is mhc_pre without the workspace
+// argument: the same launches, the same bits.
 int mhc_pre_noalloc(const uint16_t *R, const float *fn, const float *scale, const float *base,
                     const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
-                    const mhc_params *p_in, uint16_t *x_norm, float *post, float *comb,
+                    const mhc_params *p, uint16_t *x_norm, float *post, float *comb,
                     float *pre_out, float *mix_out, void *stream) {
-  mhc_params p;
-  if (p_in) p = *p_in; else mhc_default_params(&p);
-  if (int e = check_rows(rows, logical_rows)) return e;
-  if (rows > mhc::noalloc_max_rows()) return MHC_ERR_SCRATCH_LIMIT;
-  if (!finite_nonneg(p.rms_eps) || !finite_nonneg(p.hc_pre_eps) ||
-      !finite_nonneg(p.hc_sinkhorn_eps) || !finite_nonneg(p.norm_eps) ||
-      !std::isfinite(p.post_mult) || p.sinkhorn_iters < 1 || p.sinkhorn_iters > 100000)
-    return MHC_ERR_PARAM;
-  if (rows == 0) return MHC_OK;
-  if (!R || !fn || !scale || !base || !norm_w || !x_norm || !post || !comb) return MHC_ERR_NULL;
-  const void *al[] = {R, fn, scale, base, norm_w, x_norm, post, comb};
-  for (const void *q : al)
-    if (!aligned16(q)) return MHC_ERR_ALIGN;
-  if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
-  const size_t nr = (size_t)rows;
-  const Span ins[] = {span(R, nr * MHC_K * 2), span(fn, (size_t)MHC_MIX * MHC_K * 4),
-                      span(scale, 12), span(base, MHC_MIX * 4), span(norm_w, MHC_HIDDEN * 2)};
-  Span outs[5];
-  int n_out = 0;
-  outs[n_out++] = span(x_norm, nr * MHC_HIDDEN * 2);
-  outs[n_out++] = span(post, nr * MHC_HC * 4);
-  outs[n_out++] = span(comb, nr * MHC_HC * MHC_HC * 4);
-  if (pre_out) outs[n_out++] = span(pre_out, nr * MHC_HC * 4);
-  if (mix_out) outs[n_out++] = span(mix_out, nr * MHC_MIX * 4);
-  for (int a = 0; a < n_out; ++a) {
-    for (const Span &b : ins)
-      if (overlap(outs[a], b)) return MHC_ERR_OVERLAP;
-    for (int b = a + 1; b < n_out; ++b)
-      if (overlap(outs[a], outs[b])) return MHC_ERR_OVERLAP;
-  }
-  if (int e = check_device()) return e;
-  cudaError_t ce = mhc::launch_pre_noalloc(R, fn, scale, base, norm_w, rows, logical_rows, p,
-                                           x_norm, post, comb, pre_out, mix_out,
-                                           static_cast<cudaStream_t>(stream));
-  return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
+  return pre_impl(R, fn, nullptr, scale, base, norm_w, rows, logical_rows, p, nullptr, 0, x_norm,
+                  post, comb, pre_out, mix_out, stream, nullptr, nullptr, /*ws_required=*/false);
 }
 
 int mhc_post(const uint16_t *R, const uint16_t *y, const float *post, const float *comb,

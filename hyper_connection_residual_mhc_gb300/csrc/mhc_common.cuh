@@ -173,13 +173,6 @@ cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint1
                                 float norm_eps, int64_t rows, int64_t logical_rows,
                                 uint16_t *x_norm, cudaStream_t s);
 
-size_t pre_simt_workspace_bytes(int64_t rows);
-cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *scale,
-                            const float *base, const uint16_t *norm_w, int64_t rows,
-                            int64_t logical_rows, const mhc_params &p, void *workspace,
-                            uint16_t *x_norm, float *post, float *comb, float *pre_out,
-                            float *mix_out, cudaStream_t s);
-
 // decode-size chunks (logical_rows <= kDecodeMaxRows): all of mhc_pre in one
 // launch of 16-CTA clusters, up to 8 rows per cluster pass, no scratch
 // (pre_decode.cu)
@@ -286,14 +279,5 @@ cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t
 size_t fn_b_img_bytes();
 cudaError_t launch_fn_b_img(const float *fn, uint8_t *img, cudaStream_t s);
 cudaError_t onepass_error_word(unsigned int *out, bool reset);
-
-// allocation-free variant of the CUDA-core pre path (scratch in a static
-// device array of noalloc_max_rows() rows)
-int64_t noalloc_max_rows();
-cudaError_t launch_pre_noalloc(const uint16_t *R, const float *fn, const float *scale,
-                               const float *base, const uint16_t *norm_w, int64_t rows,
-                               int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,
-                               float *post, float *comb, float *pre_out, float *mix_out,
-                               cudaStream_t s);
 
 }  // namespace mhc

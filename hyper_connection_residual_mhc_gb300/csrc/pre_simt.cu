@@ -1,143 +1,18 @@
-// pre_simt.cu -- CUDA-core path of mhc_pre, in three launches:
-//   1. stats_partial: partial sums of x.x and x.fn_c over 16 fixed K slices
-//   2. finalize     : rsqrt, mix, logits, gates, Sinkhorn (one thread per row)
-//   3. combine_norm : y = sum_i pre_i R_i, RMSNorm, bf16 x_norm
-// (deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre: hc_pre_torch_impl, then
-// hc_split_sinkhorn and the combine; RMSNorm fused as in prefill_sp.py,
-// hc_combine_norm_rows).
+// pre_simt.cu -- the streaming combine (+ RMSNorm) launches: one 128-thread
+// block per row computes y = sum_i pre_i R_i in fp32, then x_norm or y itself,
+// rounded once to bf16 (deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre: the
+// combine; RMSNorm fused as in prefill_sp.py, hc_combine_norm_rows; hc_head_torch
+// for the un-normalised form).  Used by mhc_combine_norm, by mhc_hc_head above
+// its one-pass size, and by mhc_fused_post_pre after its tensor-core launch,
+// which also hands a fifth warp per row the comb logits for the Sinkhorn.
 //
 // Every row is reduced in one fixed order that depends on nothing but the
-// row's own data: slice boundaries, per-thread strides and the tree of the
-// block reductions are compile-time constants.  Row ranges therefore give the
-// whole-chunk bits.
+// row's own data: per-thread strides and the tree of the block reductions are
+// compile-time constants.  Row ranges therefore give the whole-chunk bits.
 #include "mhc_common.cuh"
 
 namespace mhc {
 namespace {
-
-constexpr int kSlices = 16;                  // K slices of the stats
-constexpr int kSliceK = kK / kSlices;        // 1280
-constexpr int kStatsThreads = 256;
-constexpr int kStatsRows = 4;                // rows per stats block
-constexpr int kPerThreadK = kSliceK / kStatsThreads;   // 5
-constexpr int kPartial = kMix + 1;           // 24 dots + sum of squares
-
-static_assert(kSliceK % kStatsThreads == 0, "slice must split evenly");
-
-// partials layout: [slice][row][kPartial] fp32
-__global__ void __launch_bounds__(kStatsThreads)
-stats_partial_kernel(const uint16_t *__restrict__ R, const float *__restrict__ fn,
-                     float *__restrict__ partials, int64_t rows) {
-  const int slice = blockIdx.y;
-  const int64_t row0 = (int64_t)blockIdx.x * kStatsRows;
-  const int tid = threadIdx.x;
-
-  float acc[kStatsRows][kPartial];
-#pragma unroll
-  for (int r = 0; r < kStatsRows; ++r)
-#pragma unroll
-    for (int c = 0; c < kPartial; ++c) acc[r][c] = 0.f;
-
-#pragma unroll 1
-  for (int s = 0; s < kPerThreadK; ++s) {
-    const int k = slice * kSliceK + s * kStatsThreads + tid;
-    float x[kStatsRows];
-#pragma unroll
-    for (int r = 0; r < kStatsRows; ++r) {
-      const int64_t m = row0 + r;
-      x[r] = m < rows ? __uint_as_float((uint32_t)__ldg(R + m * kK + k) << 16) : 0.f;
-      acc[r][kMix] = fmaf(x[r], x[r], acc[r][kMix]);
-    }
-#pragma unroll
-    for (int c = 0; c < kMix; ++c) {
-      const float f = __ldg(fn + (int64_t)c * kK + k);
-#pragma unroll
-      for (int r = 0; r < kStatsRows; ++r) acc[r][c] = fmaf(x[r], f, acc[r][c]);
-    }
-  }
-
-  // block reduction: warp butterfly, then warps 0..7 in order
-  __shared__ float red[kStatsThreads / 32][kStatsRows * kPartial];
-  const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-  for (int r = 0; r < kStatsRows; ++r)
-#pragma unroll
-    for (int c = 0; c < kPartial; ++c) {
-      float v = acc[r][c];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) red[warp][r * kPartial + c] = v;
-    }
-  __syncthreads();
-  if (tid < kStatsRows * kPartial) {
-    float v = red[0][tid];
-#pragma unroll
-    for (int w = 1; w < kStatsThreads / 32; ++w) v += red[w][tid];
-    const int r = tid / kPartial, c = tid % kPartial;
-    const int64_t m = row0 + r;
-    if (m < rows) partials[((int64_t)slice * rows + m) * kPartial + c] = v;
-  }
-}
-
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
-
-__global__ void __launch_bounds__(128)
-finalize_kernel(const float *__restrict__ partials, const float *__restrict__ scale,
-                const float *__restrict__ base, mhc_params p, int64_t rows,
-                float *__restrict__ pre_ws, float *__restrict__ post, float *__restrict__ comb,
-                float *__restrict__ pre_out, float *__restrict__ mix_out) {
-  const int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (m >= rows) return;
-  float dot[kPartial];
-#pragma unroll
-  for (int c = 0; c < kPartial; ++c) dot[c] = 0.f;
-  for (int s = 0; s < kSlices; ++s) {
-    const float *q = partials + ((int64_t)s * rows + m) * kPartial;
-#pragma unroll
-    for (int c = 0; c < kPartial; ++c) dot[c] += q[c];
-  }
-  const float rsq = 1.0f / sqrtf(dot[kMix] / (float)kK + p.rms_eps);
-  float l[kMix];
-#pragma unroll
-  for (int c = 0; c < kMix; ++c) {
-    const float mix = dot[c] * rsq;
-    if (mix_out) mix_out[m * kMix + c] = mix;
-    const int g = c < 4 ? 0 : (c < 8 ? 1 : 2);
-    l[c] = fmaf(mix, __ldg(scale + g), __ldg(base + c));
-  }
-  float pr[kHC];
-#pragma unroll
-  for (int i = 0; i < kHC; ++i) {
-    pr[i] = sigmoidf_(l[i]) + p.hc_pre_eps;
-    post[m * kHC + i] = p.post_mult * sigmoidf_(l[4 + i]);
-  }
-  *reinterpret_cast<float4 *>(pre_ws + m * kHC) = make_float4(pr[0], pr[1], pr[2], pr[3]);
-  if (pre_out) *reinterpret_cast<float4 *>(pre_out + m * kHC) = make_float4(pr[0], pr[1], pr[2], pr[3]);
-
-  float C[kHC][kHC];
-#pragma unroll
-  for (int j = 0; j < kHC; ++j)
-#pragma unroll
-    for (int i = 0; i < kHC; ++i) C[j][i] = expf(l[8 + 4 * j + i]);
-  const float eps = p.hc_sinkhorn_eps;
-  for (int t = 0; t < p.sinkhorn_iters; ++t) {
-#pragma unroll
-    for (int j = 0; j < kHC; ++j) {
-      const float d = ((C[j][0] + C[j][1]) + C[j][2]) + C[j][3] + eps;
-#pragma unroll
-      for (int i = 0; i < kHC; ++i) C[j][i] = C[j][i] / d;
-    }
-#pragma unroll
-    for (int i = 0; i < kHC; ++i) {
-      const float d = ((C[0][i] + C[1][i]) + C[2][i]) + C[3][i] + eps;
-#pragma unroll
-      for (int j = 0; j < kHC; ++j) C[j][i] = C[j][i] / d;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kHC; ++j)
-    *reinterpret_cast<float4 *>(comb + m * 16 + j * 4) = make_float4(C[j][0], C[j][1], C[j][2], C[j][3]);
-}
 
 // ---- combine (+ RMSNorm): one 128-thread block per row -----------------------
 // kNorm: x_norm = bf16(y * rsqrt(mean y^2 + eps) * w) (the pre pass);
@@ -262,13 +137,6 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
 
 }  // namespace
 
-size_t pre_simt_workspace_bytes(int64_t rows) {
-  // partials [16][rows][25] fp32, then pre [rows][4] fp32 (256-byte aligned)
-  size_t part = (size_t)kSlices * (size_t)rows * kPartial * sizeof(float);
-  part = (part + 255) & ~(size_t)255;
-  return part + (size_t)rows * kHC * sizeof(float);
-}
-
 cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
                                 float norm_eps, int64_t rows, int64_t logical_rows,
                                 uint16_t *x_norm, cudaStream_t s) {
@@ -305,27 +173,6 @@ cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t row
                     1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
                     nullptr, 0.f, reinterpret_cast<uint4 *>(y), nullptr, nullptr, 0.f, 0,
                     (uint2 *)nullptr, (uint8_t *)nullptr);
-}
-
-cudaError_t launch_pre_simt(const uint16_t *R, const float *fn, const float *scale,
-                            const float *base, const uint16_t *norm_w, int64_t rows,
-                            int64_t logical_rows, const mhc_params &p, void *workspace,
-                            uint16_t *x_norm, float *post, float *comb, float *pre_out,
-                            float *mix_out, cudaStream_t s) {
-  float *partials = static_cast<float *>(workspace);
-  size_t part = (size_t)kSlices * (size_t)rows * kPartial * sizeof(float);
-  part = (part + 255) & ~(size_t)255;
-  float *pre_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + part);
-
-  dim3 g1((unsigned)((rows + kStatsRows - 1) / kStatsRows), kSlices);
-  stats_partial_kernel<<<g1, kStatsThreads, 0, s>>>(R, fn, partials, rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  finalize_kernel<<<(unsigned)((rows + 127) / 128), 128, 0, s>>>(
-      partials, scale, base, p, rows, pre_ws, post, comb, pre_out, mix_out);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_combine_norm(R, pre_ws, norm_w, p.norm_eps, rows, logical_rows, x_norm, s);
 }
 
 }  // namespace mhc

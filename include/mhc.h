@@ -42,7 +42,7 @@
  *  - No call allocates device memory except mhc_prepare_weights (its
  *    handle's 5.9 MB, freed by mhc_release_weights).  Scratch space, where an
  *    entry point needs it, is passed in by the caller (`workspace`), except
- *    for mhc_pre_noalloc, which uses a fixed array inside the library.
+ *    for mhc_pre_noalloc, whose kernels need none.
  */
 #ifndef MHC_H
 #define MHC_H
@@ -69,7 +69,7 @@ extern "C" {
 #define MHC_ERR_WORKSPACE (-6)   /* workspace NULL or smaller than required */
 #define MHC_ERR_CUDA (-7)        /* a CUDA call failed (see mhc_last_cuda_error) */
 #define MHC_ERR_DEVICE (-8)      /* current device is not an sm_103 GPU */
-#define MHC_ERR_SCRATCH_LIMIT (-9) /* rows above mhc_pre_noalloc's fixed scratch size */
+#define MHC_ERR_SCRATCH_LIMIT (-9) /* reserved: no entry point of this build returns it */
 #define MHC_ERR_ALLOC (-10)      /* a device allocation failed (mhc_prepare_weights) */
 
 /* Scalars of the split/Sinkhorn and the two RMS normalisations.
@@ -97,15 +97,16 @@ const char *mhc_strerror(int code);
 /* Text of the last CUDA error seen by this thread inside libmhc ("" if none). */
 const char *mhc_last_cuda_error(void);
 
-/* Bytes of device scratch mhc_pre needs for a call on `rows` rows: what its
- * stats launch hands to its combine launch, the pre gates [rows, 4] fp32 and
- * the comb logits [rows, 16] fp32, each rounded up to 256 bytes (0 for
- * rows <= 0).  mhc_hc_head takes the same amount and uses the first part. */
+/* Bytes of device scratch mhc_pre, mhc_hc_head and mhc_fused_post_pre take
+ * for a call on `rows` rows: the pre gates [rows, 4] fp32 and the comb logits
+ * [rows, 16] fp32 that a two-launch path hands from its tensor-core launch to
+ * its streaming combine, each rounded up to 256 bytes (0 for rows <= 0).
+ * mhc_hc_head uses the first part; mhc_pre's own kernels use none of it. */
 size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
- * or nonzero once a tensor-core kernel (the stats of mhc_pre or mhc_hc_head,
- * or mhc_fused_post_pre) gave up a bounded wait (it then returned early and
+ * or nonzero once a tensor-core kernel (of mhc_pre, mhc_hc_head or
+ * mhc_fused_post_pre) gave up a bounded wait (it then returned early and
  * its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
  * the device's pending work.  Returns MHC_OK or MHC_ERR_NULL/MHC_ERR_CUDA. */
 int mhc_kernel_status(uint32_t *status, int reset);
@@ -137,16 +138,16 @@ int mhc_kernel_status_detail(uint32_t *where64);
  * (RMSNorm fused without rounding y first, as the fused combine+norm gate of
  * prefill_sp.py, _combine_norm_fused, requires.)
  *
- * Chunks of more than 48 rows (logical_rows > 48) take two launches:
- * (1) stats (pre_stats.cu): a cluster of 16 CTAs splits each 128-row tile by
- * hidden columns, streams R once with TMA, runs the 24 projections on the
- * tensor cores against fn split into bf16 hi + lo, and finalises the gates
- * and the comb logits per row; (2) combine + RMSNorm (pre_simt.cu,
- * combine_norm_kernel), streaming R again with the gates, while a fifth warp
- * per row runs the Sinkhorn.  Decode-size
- * chunks (logical_rows <= 48) take one latency-shaped launch (pre_decode.cu):
- * 16-CTA clusters of CUDA-core work, up to 8 rows per cluster pass, that
- * leave the workspace untouched.
+ * Chunks of more than 48 rows (logical_rows > 48) take one launch that reads
+ * R from HBM once (pre_onepass.cu): a cluster of 16 CTAs splits each 32-row
+ * tile by hidden columns, streams R with TMA, runs the 24 projections and each
+ * row's 4x4 stream Gram matrix on the tensor cores (fn split into bf16 hi +
+ * lo), exchanges the partial sums between the CTAs of the cluster, finalises
+ * gates, Sinkhorn and 1/rms(y) = 1/sqrt(p^T G p / 5120 + norm_eps), and
+ * combines the tile's columns again from L2.  Decode-size chunks
+ * (logical_rows <= 48) take one latency-shaped launch (pre_decode.cu): 16-CTA
+ * clusters of CUDA-core work, up to 8 rows per cluster pass.  Neither path
+ * touches the workspace.
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual rows
@@ -158,7 +159,9 @@ int mhc_kernel_status_detail(uint32_t *where64);
  *   workspace, workspace_bytes  device scratch of at least
  *            mhc_pre_workspace_bytes(rows) bytes, 256-byte aligned; its
  *            contents on entry do not matter; the call owns it until the
- *            stream reaches the end of the call.
+ *            stream reaches the end of the call.  It is validated (and may be
+ *            used by a later build); this build's kernels leave it untouched,
+ *            and mhc_pre_noalloc is the same call without it.
  * Outputs (fp32 unless stated)
  *   x_norm   [rows, 5120] bf16         normalised combine (sublayer input)
  *   post     [rows, 4]                 post gate
@@ -181,28 +184,20 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
  * cudaMalloc/cudaFree (they may synchronise the device), or a C/FFI caller
  * with no device allocator.
  *
- * Same arguments, outputs and validation as mhc_pre, minus the workspace;
- * results agree with mhc_pre's within the parity tolerances.  It runs
- * libmhc's CUDA-core pre kernels with their scratch in a fixed
- * 256-byte-aligned device array inside libmhc, sized for
- * mhc_pre_noalloc_max_rows() = 16384 rows (about 25.3 MiB, held on every GPU
- * that loads the library until the process exits).  rows above that limit
- * return MHC_ERR_SCRATCH_LIMIT.  It allocates nothing (no cudaMalloc, no
- * cudaFree, no allocating library call).
- *
- * The first call on a device looks up the array's device address there (with
- * that device current) and caches it; make that first call before any stream
- * capture.  All calls share the one array, which keeps the last call's
- * contents (nothing in it needs to start at zero): calls whose execution
- * overlaps on the GPU (other streams, other host threads) race on it, so
- * order them, e.g. on one stream.
+ * Same arguments, outputs and validation as mhc_pre, minus the workspace.
+ * mhc_pre's kernels take no scratch, so this runs exactly mhc_pre's launches
+ * (the decode-size launch up to 48 logical rows, the one-pass launch above)
+ * and gives mhc_pre's bits.  It allocates nothing (no cudaMalloc, no cudaFree,
+ * no allocating library call) and holds no state between calls, so calls on
+ * any streams or host threads may overlap.  mhc_pre_noalloc_max_rows()
+ * returns the library-wide row limit (2^24).
  */
 int mhc_pre_noalloc(const uint16_t *R, const float *fn, const float *scale, const float *base,
                     const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
                     const mhc_params *p, uint16_t *x_norm, float *post, float *comb,
                     float *pre_out, float *mix_out, void *stream);
 
-/* Largest `rows` mhc_pre_noalloc accepts (16384). */
+/* Largest `rows` mhc_pre_noalloc accepts (2^24, as every entry point). */
 int64_t mhc_pre_noalloc_max_rows(void);
 
 /*

@@ -126,6 +126,35 @@ def test_pre_validation(lib):
     assert call_pre(lib, post=fake(7)) == ERR_OVERLAP                       # post on comb
 
 
+def call_noalloc(lib, rows=4, logical=4, params=None, **over):
+    import hyper_connection_residual_mhc_gb300 as m
+    a = dict(R=fake(0), fn=fake(1), scale=fake(2), base=fake(3), w=fake(4), xn=fake(5),
+             post=fake(6), comb=fake(7), pre=None, mix=None)
+    a.update(over)
+    p = m.default_params() if params is None else params
+    return lib.mhc_pre_noalloc(a["R"], a["fn"], a["scale"], a["base"], a["w"], rows, logical,
+                               ctypes.byref(p), a["xn"], a["post"], a["comb"], a["pre"],
+                               a["mix"], None)
+
+
+def test_noalloc_validation_matches_mhc_pre(lib):
+    # the same checks as mhc_pre, minus the workspace; the row limit is the
+    # library-wide one
+    import hyper_connection_residual_mhc_gb300 as m
+    assert lib.mhc_pre_noalloc_max_rows() == 1 << 24
+    big = (1 << 24) + 1
+    assert call_noalloc(lib, rows=big, logical=big) == ERR_SHAPE
+    assert call_pre(lib, rows=big, logical=big) == ERR_SHAPE
+    assert call_noalloc(lib, rows=-3) == ERR_SHAPE
+    assert call_noalloc(lib, rows=5, logical=4) == ERR_SHAPE
+    assert call_noalloc(lib, params=m.default_params(sinkhorn_iters=0)) == ERR_PARAM
+    assert call_noalloc(lib, fn=None) == ERR_NULL
+    assert call_noalloc(lib, comb=fake(7) + 4) == ERR_ALIGN
+    assert call_noalloc(lib, xn=fake(0)) == ERR_OVERLAP
+    assert call_noalloc(lib, post=fake(7)) == ERR_OVERLAP
+    assert call_noalloc(lib, rows=0, logical=0, R=None) == 0
+
+
 def test_combine_norm_validation(lib):
     f = lib.mhc_combine_norm
     assert f(fake(0), fake(1), fake(2), ctypes.c_float(-1.0), 4, 4, fake(3), None) == ERR_PARAM

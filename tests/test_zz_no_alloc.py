@@ -3,12 +3,16 @@
 Callers that cannot hand libmhc device scratch -- a framework whose caching
 allocator owns the device memory, an operator/plugin enqueue that must not
 allocate, a serving loop that cannot afford cudaMalloc/cudaFree, a C/FFI
-caller without a device allocator -- use mhc_pre_noalloc, whose scratch is a
-fixed device array inside the library.  This checks, through the C ABI, that it
-gives what mhc_pre gives (within the parity tolerances of the other tests) on
-two calls in a row with different inputs and sizes, so that nothing left in
-the shared scratch by the first call leaks into the second, and that it
-rejects a row count above its fixed limit.
+caller without a device allocator -- call mhc_pre_noalloc.  mhc_pre's kernels
+take no scratch, so it is mhc_pre without the workspace argument.  Checked
+here through the C ABI:
+  * against the fp64 oracle element by element, on two calls in a row with
+    different sizes and inputs (one-pass launch), and at 8 rows (decode-size
+    launch);
+  * bit-equal to mhc_pre on the same inputs;
+  * 4 row shards of a 2048-row chunk (logical_rows = 2048) give the full
+    call's bits;
+  * the host-side row limit (also covered without a GPU in test_abi_host).
 
 This file is collected last on purpose: run alone in a fresh process or after
 every other test, it sets up its own inputs.
@@ -44,7 +48,7 @@ def _inputs(torch, rows, seed):
 
     R = synth.residual(seed, rows)
     W = synth.weights(seed)
-    return R, W, bf(R), f32(W.fn), f32(W.scale), f32(W.base), bf(W.norm_w)
+    return R, W, (bf(R), f32(W.fn), f32(W.scale), f32(W.base), bf(W.norm_w))
 
 
 def _outputs(torch, rows):
@@ -59,39 +63,69 @@ def _bits(torch, t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def test_noalloc_matches_mhc_pre_on_two_calls_in_a_row(env):
+def _noalloc(m, args, outs, logical_rows=None):
+    xn, post, comb, pre, mix = outs
+    m.mhc_pre_noalloc(*args, xn, post, comb, logical_rows=logical_rows, pre_out=pre, mix_out=mix)
+
+
+def _check_oracle(torch, oracle_mod, R, W, outs):
+    xn, post, comb, pre, mix = outs
+    o = P.oracle_rows_parallel(oracle_mod.pre, R, rows=R.shape[0], fn=W.fn, scale=W.scale,
+                               base=W.base, w=W.norm_w)
+    P.check_mix(mix.cpu().numpy(), o["mix"])
+    P.check_gates(pre.cpu().numpy(), post.cpu().numpy(), o, W.scale, R, W.fn)
+    P.check_abs(comb.cpu().numpy(), o["comb"], 1e-6, "comb")
+    P.check_bf16(_bits(torch, xn), o["x_norm"], "x_norm",
+                 term_mag=P.combine_term_magnitude(R, o["pre"], W.norm_w, 1e-6))
+
+
+def _assert_same_bits(torch, a, b, what):
+    for name, x, y in zip(("x_norm", "post", "comb", "pre", "mix"), a, b):
+        assert np.array_equal(x.contiguous().view(torch.int32 if x.dtype == torch.float32
+                                                  else torch.int16).cpu().numpy(),
+                              y.contiguous().view(torch.int32 if y.dtype == torch.float32
+                                                  else torch.int16).cpu().numpy()), \
+            f"{what}: {name} bits differ"
+
+
+@pytest.mark.parametrize("sizes", [((1500, 41), (701, 42)), ((8, 43), (3, 44))],
+                         ids=["one-pass", "decode"])
+def test_noalloc_against_the_oracle_two_calls_in_a_row(env, oracle_mod, sizes):
     torch, m = env
-    assert m.mhc_pre_noalloc_max_rows() == 16384
-    # two mhc_pre_noalloc calls back to back, larger first, so the second runs
-    # on scratch the first one left full of its own values; then the
-    # workspace-taking mhc_pre on the same inputs as the reference.
     cases = []
-    for rows, seed in ((1500, 41), (701, 42)):
-        R, W, dR, dfn, dscale, dbase, dw = _inputs(torch, rows, seed)
-        cases.append((rows, R, W, (dR, dfn, dscale, dbase, dw), _outputs(torch, rows)))
-    for rows, R, W, args, (xn, post, comb, pre, mix) in cases:
-        m.mhc_pre_noalloc(*args, xn, post, comb, pre_out=pre, mix_out=mix)
-    for rows, R, W, args, got in cases:
-        rxn, rpost, rcomb, rpre, rmix = _outputs(torch, rows)
-        m.mhc_pre(*args, x_norm=rxn, post=rpost, comb=rcomb, pre_out=rpre, mix_out=rmix)
+    for rows, seed in sizes:
+        R, W, args = _inputs(torch, rows, seed)
+        cases.append((R, W, args, _outputs(torch, rows)))
+    for R, W, args, outs in cases:          # back to back, larger first
+        _noalloc(m, args, outs)
+    torch.cuda.synchronize()
+    for R, W, args, outs in cases:
+        _check_oracle(torch, oracle_mod, R, W, outs)
+        ref = _outputs(torch, R.shape[0])
+        xn, post, comb, pre, mix = ref
+        m.mhc_pre(*args, x_norm=xn, post=post, comb=comb, pre_out=pre, mix_out=mix)
         torch.cuda.synchronize()
-        xn, post, comb, pre, mix = got
-        ref_pre = rpre.cpu().numpy()
-        P.check_mix(mix.cpu().numpy(), rmix.cpu().numpy())
-        P.check_abs(pre.cpu().numpy(), ref_pre, 1e-6, "pre")
-        P.check_abs(post.cpu().numpy(), rpost.cpu().numpy(), 1e-6, "post")
-        P.check_abs(comb.cpu().numpy(), rcomb.cpu().numpy(), 1e-6, "comb")
-        P.check_bf16(_bits(torch, xn), _bits(torch, rxn), "x_norm",
-                     term_mag=P.combine_term_magnitude(R, ref_pre, W.norm_w, 1e-6))
+        _assert_same_bits(torch, outs, ref, f"noalloc vs mhc_pre at {R.shape[0]} rows")
 
 
-def test_noalloc_rejects_rows_above_its_scratch(env):
+def test_noalloc_row_shards_give_the_whole_chunk_bits(env):
     torch, m = env
-    rows = m.mhc_pre_noalloc_max_rows() + 1
-    # only shapes matter: the check fires on the host before anything runs
-    R = torch.empty((rows, HC, H), dtype=torch.bfloat16, device="cuda")
-    _, _, dR, dfn, dscale, dbase, dw = _inputs(torch, 1, 43)
-    xn, post, comb, _, _ = _outputs(torch, rows)
-    with pytest.raises(m.MhcError) as e:
-        m.mhc_pre_noalloc(R, dfn, dscale, dbase, dw, xn, post, comb)
-    assert e.value.code == -9
+    rows = 2048
+    R, W, args = _inputs(torch, rows, 45)
+    whole = _outputs(torch, rows)
+    _noalloc(m, args, whole)
+    parts = []
+    for lo in range(0, rows, rows // 4):
+        hi = lo + rows // 4
+        sub = (args[0][lo:hi],) + args[1:]
+        outs = _outputs(torch, hi - lo)
+        _noalloc(m, sub, outs, logical_rows=rows)
+        parts.append(outs)
+    torch.cuda.synchronize()
+    joined = tuple(torch.cat([p[i] for p in parts]) for i in range(5))
+    _assert_same_bits(torch, joined, whole, "4 shards of 2048 rows")
+
+
+def test_noalloc_row_limit(env):
+    torch, m = env
+    assert m.mhc_pre_noalloc_max_rows() == 1 << 24
