@@ -44,9 +44,10 @@ SEED = 4
 PRE_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4          # 51,280
 POST_BYTES_ROW = K * 2 + H * 2 + HC * 4 + HC * HC * 4 + K * 2  # 92,240
 PRE_BYTES_CALL = MIX * K * 4 + H * 2 + 3 * 4 + MIX * 4         # fn, norm_w, scale, base
-PRE_LAUNCHES, POST_LAUNCHES = 2, 1                             # kernels per call
-KERNEL_SRC = {"mhc_post": ["post.cu"], "mhc_pre_stats": ["pre_stats.cu"],
-              "mhc_pre_combine": ["pre_simt.cu"]}
+PRE_LAUNCHES, POST_LAUNCHES = 1, 1                             # kernels per call
+KERNEL_SRC = {"mhc_post": ["post.cu", "mhc_common.cuh"],
+              "mhc_pre": ["pre_onepass.cu", "tc_ptx.cuh", "mhc_common.cuh"]}
+KERNEL_NAME = {"mhc_post": "post_kernel", "mhc_pre": "pre_onepass_kernel<false>"}
 
 
 def peaks():
@@ -74,13 +75,12 @@ def traffic_for(kernel):
             t = json.load(f)[kernel]
     except Exception:
         return None
-    if t.get("src_sha256_16") != src_hash(KERNEL_SRC[kernel]):
+    try:
+        if t.get("src_sha256_16") != src_hash(KERNEL_SRC[kernel]):
+            return None
+    except (KeyError, OSError):
         return None
     return t.get("dram_bytes_per_launch_full_size")
-
-
-def _sum_or_none(*xs):
-    return None if any(x is None for x in xs) else sum(xs)
 
 
 class ClockSampler:
@@ -289,6 +289,20 @@ def run_mhc(args):
 
         e2e = run_e2e(m, torch, dist, world, dev, step_on, make_bufs, Rh, yh, bf, M, K_)
 
+    # ---- the other prefill sizes, each with L2 evicted before every step
+    # (rank 0, N=1; outside the timed region) ---------------------------------
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+        per_config = {}
+        for seed_c, M_c in SWEEP:
+            if M_c == M:
+                continue
+            line_c = measure_config(m, torch, dev, stream, flush, seed_c, M_c, 20, 3, local)
+            per_config[f"M={M_c}"] = config_summary(line_c)
+        del flush
+        torch.cuda.empty_cache()
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) --------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -305,7 +319,8 @@ def run_mhc(args):
                          f"({wall:.1f} s wall on {threads} threads); single-threaded on "
                          f"the first {min(M, 1024)} rows: {one:.0f} rows/s",
                "single_thread_value": one}
-    return finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, dist)
+    return finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, dist,
+                  per_config)
 
 
 def run_e2e(m, torch, dist, world, dev, step_on, make_bufs, Rh, yh, bf, M, K_, lanes=1):
@@ -381,7 +396,8 @@ def run_e2e(m, torch, dist, world, dev, step_on, make_bufs, Rh, yh, bf, M, K_, l
             "pipelined": f"2 buffer sets; compute stream; {lanes} H2D and {lanes} D2H streams"}
 
 
-def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, dist):
+def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, dist,
+           per_config=None):
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -393,9 +409,17 @@ def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, d
     gbs = step_bytes * K_ / (ms / 1e3) / 1e9
     pre_gbs = (M * PRE_BYTES_ROW + PRE_BYTES_CALL) / (pre_ms / 1e3) / 1e9
     post_gbs = M * POST_BYTES_ROW / (post_ms / 1e3) / 1e9
-    # dominant single kernel: post_kernel (the largest share of the launch
-    # list); mhc_pre is two launches and is reported beside it as a call
-    dom, dgbs, dbytes = "mhc_post", post_gbs, M * POST_BYTES_ROW
+    # the dominant kernel is the call with the larger share of the step (each
+    # call is one launch at this size); the other is reported beside it
+    calls = {"mhc_pre": (pre_ms, pre_gbs, M * PRE_BYTES_ROW + PRE_BYTES_CALL),
+             "mhc_post": (post_ms, post_gbs, M * POST_BYTES_ROW)}
+    dom = max(calls, key=lambda k: calls[k][0])
+
+    def kernel_roofline(name):
+        t, g, nb = calls[name]
+        return {"kernel": name, "kernel_name": KERNEL_NAME[name], "launches": 1, "ms": t,
+                "achieved": g, "frac": g / hbm_peak, "algorithmic_bytes_per_launch": nb,
+                "traffic": traffic_for(name)}
     line = {
         "metric": METRIC,
         "value": rows_per_s,
@@ -423,23 +447,23 @@ def finish(args, m, world, rank, M, K_, ms, pre_ms, post_ms, clocks, e2e, cpu, d
             "pre_gbs": pre_gbs,
             "post_gbs": post_gbs,
             "algorithmic_bytes_per_step": step_bytes,
+            "per_config": per_config,
         },
         "roofline": {
             "bound": "hbm",
             "kernel": dom,
-            "achieved": dgbs,
+            "kernel_name": KERNEL_NAME[dom],
+            "achieved": calls[dom][1],
             "peak": hbm_peak,
             "peak_source": f"{peak_src} (hbm_gbs)",
             "unit": "GB/s",
-            "frac": dgbs / hbm_peak,
+            "frac": calls[dom][1] / hbm_peak,
             "traffic": traffic_for(dom),
-            "algorithmic_bytes_per_launch": dbytes,
-            "kernel_name": "post_kernel",
-            "pre_call": {"launches": PRE_LAUNCHES, "ms": pre_ms, "achieved": pre_gbs,
-                         "frac": pre_gbs / hbm_peak,
-                         "algorithmic_bytes": M * PRE_BYTES_ROW + PRE_BYTES_CALL,
-                         "traffic": _sum_or_none(traffic_for("mhc_pre_stats"),
-                                                 traffic_for("mhc_pre_combine"))},
+            "algorithmic_bytes_per_launch": calls[dom][2],
+            "timing": "CUDA events on the launching stream around each call, mean over the "
+                      "steps of a second loop",
+            "pre_call": kernel_roofline("mhc_pre"),
+            "post_call": kernel_roofline("mhc_post"),
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -687,31 +711,21 @@ SWEEP = [(0, 128), (1, 1500), (2, 2048), (3, 4096), (4, 16384)]   # (seed, M)
 FLUSH_BYTES = 512 << 20                                           # > 129 MB of L2
 
 
-def run_sweep(args):
-    """mhc_pre + mhc_post at every prefill size (M = 128, 1500, 2048, 4096,
-    16384; seeds 0..4), one JSON line per size.  Before each timed step a
-    512 MB memset evicts L2, so R never starts L2-resident (fn and norm_w are
-    re-read from L2 or HBM as they fall); events bracket each step alone and
-    the line reports the median over the steps.  At M=4096 mhc_post is also
-    timed alone on a second-seed y."""
-    import torch
-    import hyper_connection_residual_mhc_gb300 as m
-    from hyper_connection_residual_mhc_gb300 import build as b
-    b.build()
-    m.lib()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev)
+def measure_config(m, torch, dev, stream, flush, seed, M, steps, warmup, clock_index=0):
+    """mhc_pre + mhc_post on the M-row workload of `seed` (fn prepared once).
+    Before each timed step a 512 MB memset evicts L2, so R never starts
+    L2-resident (fn and norm_w are re-read from L2 or HBM as they fall);
+    events bracket each step alone and the figures are medians over the
+    steps.  At M=4096 mhc_post is also timed alone on a second-seed y.
+    Returns one JSON-ready line."""
     hbm_peak, peak_src = peaks()
-    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
-    steps = max(20, args.steps)
 
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
     def per_step(fns):
         """Median ms of each of fns (run back to back) and of their sum."""
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             for f in fns:
                 f()
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
@@ -729,59 +743,94 @@ def run_sweep(args):
         total = statistics.median(e[0].elapsed_time(e[-1]) for e in ev)
         return total, parts
 
+    W = synth.weights(seed)
+    R = bf(synth.residual(seed, M))
+    y = bf(synth.sublayer_out(seed, M))
+    t_ = lambda a: torch.from_numpy(a).to(dev)
+    fn, scale, base, w = t_(W.fn), t_(W.scale), t_(W.base), bf(W.norm_w)
+    xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    post = torch.empty((M, HC), dtype=torch.float32, device=dev)
+    comb = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
+    R2 = torch.empty_like(R)
+    ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
+    wh = m.mhc_prepare_weights(fn)          # as at model load, outside the timing
+
+    def pre():
+        m.mhc_pre_prepared(R, wh, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
+                           post=post, comb=comb, stream=stream)
+
+    def post_(yy=y):
+        m.mhc_post(R, yy, post, comb, logical_rows=M, out=R2, stream=stream)
+
+    with ClockSampler(clock_index) as clk:
+        ms, (pre_ms, post_ms) = per_step([pre, post_])
+        extra = {}
+        if M == 4096:
+            y2 = bf(synth.sublayer_out(seed + 1, M))
+            alone, _ = per_step([lambda: post_(y2)])
+            a_gbs = M * POST_BYTES_ROW / (alone / 1e3) / 1e9
+            extra = {"post_alone_ms": alone, "post_alone_gbs": a_gbs,
+                     "post_alone_frac": a_gbs / hbm_peak}
+    torch.cuda.synchronize(dev)
+    wh.release()
+    nbytes = M * (PRE_BYTES_ROW + POST_BYTES_ROW) + PRE_BYTES_CALL
+    gbs = nbytes / (ms / 1e3) / 1e9
+    pre_gbs = (M * PRE_BYTES_ROW + PRE_BYTES_CALL) / (pre_ms / 1e3) / 1e9
+    post_gbs = M * POST_BYTES_ROW / (post_ms / 1e3) / 1e9
+    return {
+        "metric": f"mHC pre+post rows/s and achieved HBM GB/s at M={M}",
+        "value": M / (ms / 1e3), "unit": "rows/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"M={M} rows: R[M,4,5120] bf16, fn[24,20480] f32, "
+                               f"y[M,5120] bf16 (seed {seed}); one step = mhc_pre + "
+                               "mhc_post (fn prepared once); median of per-step event "
+                               "times",
+                   "op": "sweep", "rows": M,
+                   "l2": "512 MB memset before every timed step (outside the events)",
+                   "pre_ms": pre_ms, "post_ms": post_ms,
+                   "pre_gbs": pre_gbs, "post_gbs": post_gbs,
+                   "pre_frac": pre_gbs / hbm_peak, "post_frac": post_gbs / hbm_peak, **extra},
+        "roofline": {"bound": "hbm", "kernel": "mhc_pre+mhc_post", "achieved": gbs,
+                     "peak": hbm_peak, "peak_source": f"{peak_src} (hbm_gbs)",
+                     "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": (PRE_LAUNCHES if M > 48 else 1) * steps + POST_LAUNCHES * steps,
+        "clocks": clk.summary(),
+    }
+
+
+def config_summary(line):
+    """The figures of one measure_config line that the headline line carries."""
+    c = line["config"]
+    out = {"seed_rows": c["workload"].split(";")[0], "rows_per_s": line["value"],
+           "ms_per_step": line["ms_per_step"], "achieved_gbs": line["roofline"]["achieved"],
+           "frac_of_hbm": line["roofline"]["frac"], "pre_ms": c["pre_ms"],
+           "pre_frac": c["pre_frac"], "post_ms": c["post_ms"], "post_frac": c["post_frac"],
+           "steps": line["steps"], "sm_mhz": line["clocks"]["sm_mhz"],
+           "throttle_reasons": line["clocks"]["reasons"]}
+    for k in ("post_alone_ms", "post_alone_gbs", "post_alone_frac"):
+        if k in c:
+            out[k] = c[k]
+    return out
+
+
+def run_sweep(args):
+    """mhc_pre + mhc_post at every prefill size (M = 128, 1500, 2048, 4096,
+    16384; seeds 0..4), one JSON line per size (see measure_config)."""
+    import torch
+    import hyper_connection_residual_mhc_gb300 as m
+    from hyper_connection_residual_mhc_gb300 import build as b
+    b.build()
+    m.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
     for seed, M in SWEEP:
-        W = synth.weights(seed)
-        R = bf(synth.residual(seed, M))
-        y = bf(synth.sublayer_out(seed, M))
-        t_ = lambda a: torch.from_numpy(a).to(dev)
-        fn, scale, base, w = t_(W.fn), t_(W.scale), t_(W.base), bf(W.norm_w)
-        xn = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
-        post = torch.empty((M, HC), dtype=torch.float32, device=dev)
-        comb = torch.empty((M, HC, HC), dtype=torch.float32, device=dev)
-        R2 = torch.empty_like(R)
-        ws = torch.empty((max(256, m.mhc_pre_workspace_bytes(M)),), dtype=torch.uint8, device=dev)
-        wh = m.mhc_prepare_weights(fn)          # as at model load, outside the timing
-
-        def pre():
-            m.mhc_pre_prepared(R, wh, scale, base, w, logical_rows=M, workspace=ws, x_norm=xn,
-                               post=post, comb=comb, stream=stream)
-
-        def post_(yy=y):
-            m.mhc_post(R, yy, post, comb, logical_rows=M, out=R2, stream=stream)
-
-        with ClockSampler(0) as clk:
-            ms, (pre_ms, post_ms) = per_step([pre, post_])
-            extra = {}
-            if M == 4096:
-                y2 = bf(synth.sublayer_out(seed + 1, M))
-                alone, _ = per_step([lambda: post_(y2)])
-                extra = {"post_alone_ms": alone,
-                         "post_alone_gbs": M * POST_BYTES_ROW / (alone / 1e3) / 1e9}
-        nbytes = M * (PRE_BYTES_ROW + POST_BYTES_ROW) + PRE_BYTES_CALL
-        gbs = nbytes / (ms / 1e3) / 1e9
-        line = {
-            "metric": f"mHC pre+post rows/s and achieved HBM GB/s at M={M}",
-            "value": M / (ms / 1e3), "unit": "rows/s", "n_gpus": 1, "steps": steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"M={M} rows: R[M,4,5120] bf16, fn[24,20480] f32, "
-                                   f"y[M,5120] bf16 (seed {seed}); one step = mhc_pre + "
-                                   "mhc_post (fn prepared once); median of per-step event "
-                                   "times",
-                       "op": "sweep", "rows": M,
-                       "l2": "512 MB memset before every timed step (outside the events)",
-                       "pre_ms": pre_ms, "post_ms": post_ms,
-                       "pre_gbs": (M * PRE_BYTES_ROW + PRE_BYTES_CALL) / (pre_ms / 1e3) / 1e9,
-                       "post_gbs": M * POST_BYTES_ROW / (post_ms / 1e3) / 1e9, **extra},
-            "roofline": {"bound": "hbm", "kernel": "mhc_pre+mhc_post", "achieved": gbs,
-                         "peak": hbm_peak, "peak_source": f"{peak_src} (hbm_gbs)",
-                         "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None,
-                         "algorithmic_bytes_per_launch": nbytes},
-            "gpu_launches": (PRE_LAUNCHES if M > 48 else 1) * steps + POST_LAUNCHES * steps,
-            "clocks": clk.summary(),
-        }
+        line = measure_config(m, torch, dev, stream, flush, seed, M, max(20, args.steps),
+                              args.warmup)
         print(json.dumps(line), flush=True)
-        del R, y, R2, xn
 
 
 def main():
@@ -792,6 +841,9 @@ def main():
     ap.add_argument("--impl", choices=["mhc", "reference"], default="mhc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-config figures (M = 128, 1500, 2048, 4096) of the "
+                         "headline line")
     ap.add_argument("--op", choices=["step", "hc_head", "latency", "fused_post_pre", "sweep",
                                      "pre_mxfp8"],
                     default="step",

@@ -44,9 +44,10 @@ def test_clock_summary_without_samples():
 def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
     src = tmp_path / "hyper_connection_residual_mhc_gb300" / "csrc"
     src.mkdir(parents=True)
-    (src / "post.cu").write_text("// the kernel as captured\n")
+    for f in bench.KERNEL_SRC["mhc_post"]:
+        (src / f).write_text(f"// {f} as captured\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    h = bench.src_hash(["post.cu"])
+    h = bench.src_hash(bench.KERNEL_SRC["mhc_post"])
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
         {"mhc_post": {"src_sha256_16": h, "dram_bytes_per_launch_full_size": 1234}}))
