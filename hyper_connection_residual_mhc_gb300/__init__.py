@@ -78,6 +78,10 @@ SIGNATURES = {
     "mhc_pre_mxfp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64,
                                      ctypes.POINTER(MhcParams), _vp, ctypes.c_size_t, _vp, _vp,
                                      _vp, _vp, _vp, _vp]),
+    "mhc_fused_post_pre_mxfp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                                _i64, ctypes.POINTER(MhcParams), _vp,
+                                                ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                _vp]),
     "mhc_quantize_mxfp8": (ctypes.c_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "mhc_swizzle_scales_128x4_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "mhc_swizzle_scales_128x4": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp]),
@@ -480,3 +484,48 @@ def _fused_call(name, fn_arg, ws_bytes_of, R, y, post, comb, scale, base, norm_w
         _ptr(pre_out), _ptr(mix_out), _stream(stream))
     _check(name, code)
     return R_out, x_norm, post_out, comb_out
+
+
+def mhc_fused_post_pre_mxfp8(R, y, post, comb, weights, scale, base, norm_w, *,
+                             logical_rows=None, params=None, workspace=None, R_out=None,
+                             x_norm=None, x_q=None, x_s=None, post_out=None, comb_out=None,
+                             stream=None):
+    """mhc_fused_post_pre_prepared that also writes the next x_norm's MXFP8 (see
+    mhc_fused_post_pre_mxfp8 in include/mhc.h).  Returns ``(R_out, x_norm, x_q
+    [rows,5120] uint8 E4M3 codes, x_s [rows,160] uint8 ue8m0 scales, post_out,
+    comb_out)``."""
+    import torch
+    rows = int(R.shape[0])
+    _need(R, "R", torch.bfloat16, (rows, HC, H))
+    _need(y, "y", torch.bfloat16, (rows, H))
+    _need(post, "post", torch.float32, (rows, HC))
+    _need(comb, "comb", torch.float32, (rows, HC, HC))
+    _need(scale, "scale", torch.float32, (3,))
+    _need(base, "base", torch.float32, (MIX,))
+    _need(norm_w, "norm_w", torch.bfloat16, (H,))
+    dev = R.device
+    R_out = torch.empty_like(R) if R_out is None else R_out
+    x_norm = torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if x_norm is None else x_norm
+    x_q = torch.empty((rows, H), dtype=torch.uint8, device=dev) if x_q is None else x_q
+    x_s = torch.empty((rows, H // 32), dtype=torch.uint8, device=dev) if x_s is None else x_s
+    post_out = torch.empty((rows, HC), dtype=torch.float32, device=dev) if post_out is None else post_out
+    comb_out = (torch.empty((rows, HC, HC), dtype=torch.float32, device=dev)
+                if comb_out is None else comb_out)
+    _need(R_out, "R_out", torch.bfloat16, (rows, HC, H))
+    _need(x_norm, "x_norm", torch.bfloat16, (rows, H))
+    _need(x_q, "x_q", torch.uint8, (rows, H))
+    _need(x_s, "x_s", torch.uint8, (rows, H // 32))
+    _need(post_out, "post_out", torch.float32, (rows, HC))
+    _need(comb_out, "comb_out", torch.float32, (rows, HC, HC))
+    need = mhc_pre_workspace_bytes(rows)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    p = default_params() if params is None else params
+    code = lib().mhc_fused_post_pre_mxfp8(
+        _ptr(R), _ptr(y), _ptr(post), _ptr(comb), weights.handle, _ptr(scale), _ptr(base),
+        _ptr(norm_w), rows, rows if logical_rows is None else int(logical_rows), ctypes.byref(p),
+        _ptr(workspace), ws_bytes, _ptr(R_out), _ptr(x_norm), _ptr(x_q), _ptr(x_s),
+        _ptr(post_out), _ptr(comb_out), _stream(stream))
+    _check("mhc_fused_post_pre_mxfp8", code)
+    return R_out, x_norm, x_q, x_s, post_out, comb_out

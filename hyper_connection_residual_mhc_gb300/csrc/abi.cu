@@ -403,7 +403,8 @@ int fused_impl(const uint16_t *R, const uint16_t *y, const float *post, const fl
                const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
                const mhc_params *p_in, void *workspace, size_t workspace_bytes,
                uint16_t *R_out, uint16_t *x_norm, float *post_out, float *comb_out,
-               float *pre_out, float *mix_out, void *stream) {
+               float *pre_out, float *mix_out, void *stream,
+               uint8_t *mx_q = nullptr, uint8_t *mx_s = nullptr) {
   mhc_params p;
   if (p_in) p = *p_in; else mhc_default_params(&p);
   if (int e = check_rows(rows, logical_rows)) return e;
@@ -419,6 +420,8 @@ int fused_impl(const uint16_t *R, const uint16_t *y, const float *post, const fl
   for (const void *q : al)
     if (!aligned16(q)) return MHC_ERR_ALIGN;
   if ((pre_out && !aligned16(pre_out)) || (mix_out && !aligned16(mix_out))) return MHC_ERR_ALIGN;
+  if ((mx_q == nullptr) != (mx_s == nullptr)) return MHC_ERR_NULL;
+  if (mx_q && (!aligned16(mx_q) || !aligned16(mx_s))) return MHC_ERR_ALIGN;
   const size_t need = fnp_ready ? mhc_pre_workspace_bytes(rows)
                                 : mhc_fused_post_pre_workspace_bytes(rows);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -428,10 +431,14 @@ int fused_impl(const uint16_t *R, const uint16_t *y, const float *post, const fl
                       span(post, nr * MHC_HC * 4), span(comb, nr * MHC_HC * MHC_HC * 4),
                       span(fn, (size_t)MHC_MIX * MHC_K * 4), span(scale, 12),
                       span(base, MHC_MIX * 4), span(norm_w, MHC_HIDDEN * 2)};
-  Span outs[7];
+  Span outs[9];
   int n_out = 0;
   outs[n_out++] = span(R_out, nr * MHC_K * 2);
   outs[n_out++] = span(x_norm, nr * MHC_HIDDEN * 2);
+  if (mx_q) {
+    outs[n_out++] = span(mx_q, nr * MHC_HIDDEN);
+    outs[n_out++] = span(mx_s, nr * (MHC_HIDDEN / 32));
+  }
   outs[n_out++] = span(post_out, nr * MHC_HC * 4);
   outs[n_out++] = span(comb_out, nr * MHC_HC * MHC_HC * 4);
   outs[n_out++] = span(workspace, need);
@@ -452,6 +459,10 @@ int fused_impl(const uint16_t *R, const uint16_t *y, const float *post, const fl
     ce = mhc::launch_post_pre_decode(R, y, post, comb, fn, scale, base, norm_w, rows,
                                      logical_rows, p, R_out, x_norm, post_out, comb_out, pre_out,
                                      mix_out, s, /*fn_stable=*/fnp_ready != nullptr);
+    // the decode kernel writes bf16 x_norm only; its MXFP8 follows in a
+    // second, streaming launch
+    if (ce == cudaSuccess && mx_q)
+      ce = mhc::launch_mx_quantize(x_norm, rows, MHC_HIDDEN, logical_rows, mx_q, mx_s, s);
   } else {
     float *pre_ws = static_cast<float *>(workspace);
     float *logit_ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + gate_bytes(rows));
@@ -463,7 +474,7 @@ int fused_impl(const uint16_t *R, const uint16_t *y, const float *post, const fl
     if (ce == cudaSuccess)
       ce = mhc::launch_combine_norm_sinkhorn(R_out, pre_ws, norm_w, p.norm_eps, logit_ws, comb_out,
                                              p.hc_sinkhorn_eps, p.sinkhorn_iters, rows,
-                                             logical_rows, x_norm, s);
+                                             logical_rows, x_norm, s, mx_q, mx_s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }
@@ -493,6 +504,22 @@ int mhc_fused_post_pre_prepared(const uint16_t *R, const uint16_t *y, const floa
   return fused_impl(R, y, post, comb, w->fn32, w->img64, scale, base, norm_w, rows, logical_rows,
                     p, workspace, workspace_bytes, R_out, x_norm, post_out, comb_out, pre_out,
                     mix_out, stream);
+}
+
+int mhc_fused_post_pre_mxfp8(const uint16_t *R, const uint16_t *y, const float *post,
+                             const float *comb, const mhc_weights *w, const float *scale,
+                             const float *base, const uint16_t *norm_w, int64_t rows,
+                             int64_t logical_rows, const mhc_params *p, void *workspace,
+                             size_t workspace_bytes, uint16_t *R_out, uint16_t *x_norm,
+                             uint8_t *x_q, uint8_t *x_s, float *post_out, float *comb_out,
+                             void *stream) {
+  if (!w) return MHC_ERR_NULL;
+  if (rows > 0 && (!x_q || !x_s)) return MHC_ERR_NULL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != w->device) return MHC_ERR_DEVICE;
+  return fused_impl(R, y, post, comb, w->fn32, w->img64, scale, base, norm_w, rows, logical_rows,
+                    p, workspace, workspace_bytes, R_out, x_norm, post_out, comb_out, nullptr,
+                    nullptr, stream, x_q, x_s);
 }
 
 int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const float *base,

@@ -380,9 +380,18 @@ int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const fl
  *   mhc_pre_prepared (same arguments, checks and bits) that also writes
  *   x_q [rows, 5120] uint8 E4M3 codes and x_s [rows, 160] uint8 scales of
  *   x_norm, both device, 16-byte aligned, overlapping nothing else.  Chunks
- *   of more than 48 rows: the combine + RMSNorm launch writes them beside
+ *   of more than 48 rows: the one-pass kernel's combine writes them beside
  *   x_norm; decode-size chunks: one more launch after the decode kernel.
  *   MHC_ERR_NULL if x_q or x_s is NULL.
+ * mhc_fused_post_pre_mxfp8(R, y, post, comb, w, scale, base, norm_w, rows,
+ *               logical_rows, p, workspace, workspace_bytes, R_out, x_norm,
+ *               x_q, x_s, post_out, comb_out, stream)
+ *   mhc_fused_post_pre_prepared (same arguments, checks and bits, without
+ *   pre_out/mix_out) that also writes x_q [rows, 5120] and x_s [rows, 160]
+ *   of the next sublayer's x_norm, as mhc_pre_mxfp8 does: above 48 rows the
+ *   combine launch writes them beside x_norm, at decode sizes one more
+ *   launch follows the fused decode kernel.  MHC_ERR_NULL if x_q or x_s is
+ *   NULL.
  * mhc_quantize_mxfp8(x, rows, cols, logical_rows, q, s, stream)
  *   The same quantization of any bf16 rows: x [rows, cols] bf16 (cols a
  *   multiple of 32, at most 65536), q [rows, cols] uint8, s [rows, cols/32]
@@ -405,6 +414,13 @@ int mhc_pre_mxfp8(const uint16_t *R, const mhc_weights *w, const float *scale, c
                   const mhc_params *p, void *workspace, size_t workspace_bytes,
                   uint16_t *x_norm, uint8_t *x_q, uint8_t *x_s, float *post, float *comb,
                   void *stream);
+int mhc_fused_post_pre_mxfp8(const uint16_t *R, const uint16_t *y, const float *post,
+                             const float *comb, const mhc_weights *w, const float *scale,
+                             const float *base, const uint16_t *norm_w, int64_t rows,
+                             int64_t logical_rows, const mhc_params *p, void *workspace,
+                             size_t workspace_bytes, uint16_t *R_out, uint16_t *x_norm,
+                             uint8_t *x_q, uint8_t *x_s, float *post_out, float *comb_out,
+                             void *stream);
 int mhc_quantize_mxfp8(const uint16_t *x, int64_t rows, int64_t cols, int64_t logical_rows,
                        uint8_t *q, uint8_t *s, void *stream);
 size_t mhc_swizzle_scales_128x4_bytes(int64_t rows, int64_t groups);

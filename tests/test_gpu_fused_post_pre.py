@@ -164,3 +164,53 @@ def test_fused_shards_and_repeat_are_bit_exact(torch, mhc, oracle_mod):
         part = c.gpu(torch, mhc, r * s, (r + 1) * s, logical_rows=rows)
         for k in full:
             assert torch.equal(part[k], full[k][r * s:(r + 1) * s]), (k, r)
+
+
+@pytest.mark.parametrize("rows", [7, 48, 49, 1500])
+def test_fused_mxfp8_against_the_oracle(torch, mhc, oracle_mod, rows):
+    # the fused boundary with the next x_norm as MXFP8 (prefill_sp.py,
+    # _mxfp8_quantize on the attention input): R_out, x_norm, post and comb
+    # are the bits of mhc_fused_post_pre_prepared, which the tests above
+    # check against the oracle; the codes and scales equal the oracle's
+    # quantization of that x_norm bit for bit
+    c = Chain(torch, oracle_mod, rows, 600 + rows)
+    d = c.d
+    h = mhc.mhc_prepare_weights(d["fn"])
+    R2, xn, q, s, po, co = mhc.mhc_fused_post_pre_mxfp8(d["R"], d["y"], d["post"], d["comb"], h,
+                                                         d["scale"], d["base"], d["w"])
+    ref = mhc.mhc_fused_post_pre_prepared(d["R"], d["y"], d["post"], d["comb"], h, d["scale"],
+                                          d["base"], d["w"])
+    torch.cuda.synchronize()
+    for name, a, b in zip(("R_out", "x_norm", "post", "comb"), (R2, xn, po, co), ref):
+        assert torch.equal(a, b), name
+    q_ref, s_ref = oracle_mod.mxfp8_quantize(_bits(torch, xn))
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    # and the whole chain against the oracle's post then pre
+    g = {"R_out": R2, "x_norm": xn, "post": po, "comb": co}
+    o_R2 = oracle_mod.post(c.R, c.y, c.post, c.comb)
+    P.check_bf16(_bits(torch, R2), o_R2, "R_out",
+                 term_mag=P.post_term_magnitude(c.R, c.y, c.post, c.comb))
+    o = P.oracle_rows_parallel(oracle_mod.pre, _bits(torch, R2), rows=rows, fn=c.Wn.fn,
+                               scale=c.Wn.scale, base=c.Wn.base, w=c.Wn.norm_w)
+    P.check_abs(co.cpu().numpy(), o["comb"], 1e-6, "comb")
+    P.check_bf16(_bits(torch, g["x_norm"]), o["x_norm"], "x_norm",
+                 term_mag=P.combine_term_magnitude(_bits(torch, R2), o["pre"], c.Wn.norm_w, 1e-6))
+    h.release()
+    assert mhc.mhc_kernel_status() == 0
+
+
+def test_fused_mxfp8_row_shards(torch, mhc, oracle_mod):
+    rows = 1500
+    c = Chain(torch, oracle_mod, rows, 700)
+    d = c.d
+    h = mhc.mhc_prepare_weights(d["fn"])
+    args = lambda lo, hi: (d["R"][lo:hi], d["y"][lo:hi], d["post"][lo:hi], d["comb"][lo:hi], h,
+                           d["scale"], d["base"], d["w"])
+    full = mhc.mhc_fused_post_pre_mxfp8(*args(0, rows))
+    parts = [mhc.mhc_fused_post_pre_mxfp8(*args(r0, r0 + 375), logical_rows=rows)
+             for r0 in range(0, rows, 375)]
+    torch.cuda.synchronize()
+    for k in range(6):
+        assert torch.equal(full[k], torch.cat([p[k] for p in parts])), k
+    h.release()
