@@ -507,8 +507,8 @@ def run_op(args):
 
         def step():
             m.mhc_hc_head(R, fn, scale, base, logical_rows=M, workspace=ws, out=y, stream=stream)
-        # up to 256 rows one launch (the one-pass kernel), else stats + combine
-        nbytes, launches = M * HEAD_BYTES_ROW + HEAD_BYTES_CALL, 1 if M <= 256 else 2
+        # one launch at every size (above 256 rows the tiled kernel)
+        nbytes, launches = M * HEAD_BYTES_ROW + HEAD_BYTES_CALL, 1
         metric = "mhc_hc_head rows/s (final stream collapse) and achieved HBM GB/s"
         workload = f"M={M} rows: R[M,4,5120] bf16, hc_head fn[4,20480] f32 (seed {SEED})"
     elif args.op == "fused_post_pre":

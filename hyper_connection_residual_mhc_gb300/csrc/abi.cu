@@ -122,14 +122,14 @@ size_t mhc_fused_post_pre_workspace_bytes(int64_t rows) {
 
 int mhc_kernel_status_detail(uint32_t *where64) {
   if (!where64) return MHC_ERR_NULL;
-  cudaError_t e = mhc::fused_error_where(where64);
+  cudaError_t e = mhc::onepass_error_where(where64);
   return e == cudaSuccess ? MHC_OK : cuda_fail(e);
 }
 
 int mhc_kernel_status(uint32_t *status, int reset) {
   if (!status) return MHC_ERR_NULL;
   unsigned int w = 0, w2 = 0, w3 = 0, w4 = 0;
-  cudaError_t e = mhc::fused_error_word(&w, reset != 0);
+  cudaError_t e = mhc::head_tile_error_word(&w, reset != 0);
   if (e == cudaSuccess) e = mhc::fused_post_pre_error_word(&w2, reset != 0);
   if (e == cudaSuccess) e = mhc::head_error_word(&w3, reset != 0);
   if (e == cudaSuccess) e = mhc::onepass_error_word(&w4, reset != 0);
@@ -560,11 +560,10 @@ int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const fl
     ce = mhc::launch_head_onepass(R, fn, scale, base, rows, logical_rows, norm_eps, hc_eps, y,
                                   pre_out, mix_out, s);
   } else {
-    // tensor-core stats (gates to the workspace), then a streaming combine
-    float *pre_ws = static_cast<float *>(workspace);
-    ce = mhc::launch_head_stats(R, fn, scale, base, rows, logical_rows, norm_eps, hc_eps, pre_ws,
-                                pre_out, mix_out, s);
-    if (ce == cudaSuccess) ce = mhc::launch_head_combine(R, pre_ws, rows, logical_rows, y, s);
+    // one launch: tensor-core stats, the tile kept in shared memory for the
+    // combine (no workspace used)
+    ce = mhc::launch_head_tile(R, fn, scale, base, rows, logical_rows, norm_eps, hc_eps, y,
+                               pre_out, mix_out, s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }

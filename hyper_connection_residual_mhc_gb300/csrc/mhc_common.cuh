@@ -191,20 +191,6 @@ cudaError_t launch_post_pre_decode(const uint16_t *R, const uint16_t *y, const f
                                    uint16_t *x_norm, float *post, float *comb, float *pre_out,
                                    float *mix_out, cudaStream_t s, bool fn_stable = false);
 
-// tensor-core stats half of mhc_pre (cluster of 16 CTAs): writes the pre gates
-// to pre_ws [rows, 4] and the comb logits to logit_ws [rows, 16] for the
-// combine launch, and post (+ pre_out, mix_out)
-// (fn_img: NULL, or the prepared-weights image of fn_img_bytes(), which the
-// kernel then bulk-copies instead of converting fn)
-cudaError_t launch_pre_stats(const uint16_t *R, const float *fn, const uint8_t *fn_img,
-                             const float *scale, const float *base, int64_t rows,
-                             int64_t logical_rows, const mhc_params &p, float *pre_ws,
-                             float *logit_ws, float *post, float *pre_out, float *mix_out,
-                             cudaStream_t s);
-// prepared weights: fn [24, 20480] fp32 -> the stats kernel's bf16 hi/lo
-// B-tile image of all 16 cluster ranks (fn_img_bytes() bytes)
-size_t fn_img_bytes();
-cudaError_t launch_fn_img_prep(const float *fn, uint8_t *img, cudaStream_t s);
 // combine + RMSNorm with a fifth warp per row block for the Sinkhorn of the
 // comb logits (writes comb [rows, 4, 4])
 // mx_q / mx_s non-NULL: the same launch also writes x_norm's MXFP8 codes
@@ -224,25 +210,23 @@ cudaError_t launch_mx_quantize(const uint16_t *x, int64_t rows, int64_t cols,
 // *groups bytes, padding rows zero (groups a multiple of 4)
 cudaError_t launch_mx_swizzle(const uint8_t *s, int64_t rows, int64_t groups, uint8_t *out,
                               cudaStream_t st);
-// the same stats kernel built for hc_head's 4 mixes: writes the gates to
-// pre_ws [rows, 4] (+ pre_out, mix_out [rows, 4])
-cudaError_t launch_head_stats(const uint16_t *R, const float *fn, const float *scale,
-                              const float *base, int64_t rows, int64_t logical_rows,
-                              float norm_eps, float hc_eps, float *pre_ws, float *pre_out,
-                              float *mix_out, cudaStream_t s);
 // all of hc_head in one pass over R (head_onepass.cu): 4-CTA clusters, fp32
 // projections on the CUDA cores, the combine from shared memory.  It is
 // latency-bound (a 4-row tile per ~4 us per cluster), so it serves chunks of
-// up to 256 rows, where it takes ~6 us against ~12.5 us for the two launches
+// up to 256 rows
 constexpr int64_t kHeadOnePassMaxRows = 256;
 cudaError_t launch_head_onepass(const uint16_t *R, const float *fn, const float *scale,
                                 const float *base, int64_t rows, int64_t logical_rows,
                                 float norm_eps, float hc_eps, uint16_t *y, float *pre_out,
                                 float *mix_out, cudaStream_t s);
 cudaError_t head_error_word(unsigned int *out, bool reset);
-// y = bf16(sum_i pre_i R_i), one block per row (hc_head's combine)
-cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows,
-                                int64_t logical_rows, uint16_t *y, cudaStream_t s);
+// above that: one launch of 16-CTA clusters whose tiles stay in shared
+// memory for the combine (head_tile.cu)
+cudaError_t launch_head_tile(const uint16_t *R, const float *fn, const float *scale,
+                             const float *base, int64_t rows, int64_t logical_rows,
+                             float norm_eps, float hc_eps, uint16_t *y, float *pre_out,
+                             float *mix_out, cudaStream_t s);
+cudaError_t head_tile_error_word(unsigned int *out, bool reset);
 // hc_post fused with the next pre's stats (post_pre_fused.cu): writes R_out,
 // the next pre's gates to pre_ws [rows, 4], its comb logits to logit_ws
 // [rows, 16] and its post gates (+ pre_out, mix_out)
@@ -257,9 +241,6 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
                                   float *pre_out, float *mix_out, cudaStream_t s);
 cudaError_t launch_fn_prep_sw64(const float *fn, uint8_t *fnp, cudaStream_t s, bool pdl);
 cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset);
-// the stats kernel's error word (nonzero once a bounded wait expired)
-cudaError_t fused_error_word(unsigned int *out, bool reset);
-cudaError_t fused_error_where(unsigned int *out32);
 
 // all of mhc_pre in one launch of 16-CTA clusters that reads R from HBM once
 // (pre_onepass.cu): 32-row tiles, the four streams of a 64-column block as
@@ -279,5 +260,7 @@ cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t
 size_t fn_b_img_bytes();
 cudaError_t launch_fn_b_img(const float *fn, uint8_t *img, cudaStream_t s);
 cudaError_t onepass_error_word(unsigned int *out, bool reset);
+// where the one-pass kernel's expired (0..31) and abandoned (32..63) waits ended
+cudaError_t onepass_error_where(unsigned int *out64);
 
 }  // namespace mhc

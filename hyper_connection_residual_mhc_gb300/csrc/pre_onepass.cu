@@ -838,6 +838,13 @@ cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t
   return launch<false>(a, logical_rows, s);
 }
 
+cudaError_t onepass_error_where(unsigned int *out64) {
+  cudaError_t e = cudaMemcpyFromSymbol(out64, g_onepass_where, 32 * sizeof(unsigned int));
+  if (e == cudaSuccess)
+    e = cudaMemcpyFromSymbol(out64 + 32, g_onepass_where_aborted, 32 * sizeof(unsigned int));
+  return e;
+}
+
 cudaError_t onepass_error_word(unsigned int *out, bool reset) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_onepass_error, sizeof(unsigned int));
   if (e == cudaSuccess && reset) {

@@ -1,9 +1,8 @@
-// pre_simt.cu -- the streaming combine (+ RMSNorm) launches: one 128-thread
-// block per row computes y = sum_i pre_i R_i in fp32, then x_norm or y itself,
-// rounded once to bf16 (deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre: the
-// combine; RMSNorm fused as in prefill_sp.py, hc_combine_norm_rows; hc_head_torch
-// for the un-normalised form).  Used by mhc_combine_norm, by mhc_hc_head above
-// its one-pass size, and by mhc_fused_post_pre after its tensor-core launch,
+// pre_simt.cu -- the streaming combine + RMSNorm launches: one 128-thread
+// block per row computes y = sum_i pre_i R_i in fp32, then x_norm, rounded
+// once to bf16 (deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre: the combine;
+// RMSNorm fused as in prefill_sp.py, hc_combine_norm_rows).  Used by
+// mhc_combine_norm, and by mhc_fused_post_pre after its tensor-core launch,
 // which also hands a fifth warp per row the comb logits for the Sinkhorn.
 //
 // Every row is reduced in one fixed order that depends on nothing but the
@@ -14,19 +13,18 @@
 namespace mhc {
 namespace {
 
-// ---- combine (+ RMSNorm): one 128-thread block per row -----------------------
-// kNorm: x_norm = bf16(y * rsqrt(mean y^2 + eps) * w) (the pre pass);
-// otherwise y itself, cast once (hc_head: deepseek_v4.py, hc_head_torch).
+// ---- combine + RMSNorm: one 128-thread block per row --------------------------
+// x_norm = bf16(y * rsqrt(mean y^2 + eps) * w)
 constexpr int kCnThreads = 128;
 constexpr int kCnChunks = kChunksPerStream / kCnThreads;   // 5
 static_assert(kChunksPerStream % kCnThreads == 0, "");
 
-// One row by one 128-thread block: y = sum_i pv_i R_i in fp32, then x_norm
-// (kNorm) or y itself, cast once to bf16.
+// One row by one 128-thread block: y = sum_i pv_i R_i in fp32, then x_norm,
+// cast once to bf16.
 // kMx: the block also writes x_norm's MXFP8 codes (mxq, 8 per chunk) and
 // linear block scales (mxs): a 32-column block is 4 consecutive chunks, held
 // by 4 consecutive lanes.
-template <bool kNorm, bool kMx = false>
+template <bool kMx = false>
 __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const float (&pv)[kHC],
                                             const uint4 *__restrict__ w, float norm_eps,
                                             uint4 *__restrict__ out, int64_t row,
@@ -56,11 +54,7 @@ __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const f
     }
   }
   uint4 *o = out + row * kChunksPerStream;
-  if constexpr (!kNorm) {
-#pragma unroll
-    for (int q = 0; q < kCnChunks; ++q) st_stream(o + q * kCnThreads + tid, pack8_rn(y[q]));
-    (void)w; (void)norm_eps; (void)ss;
-  } else {
+  {
     __shared__ float red[kCnThreads / 32];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -115,7 +109,7 @@ __device__ __forceinline__ void sinkhorn_row(const float *__restrict__ logit,
 
 // kSink: a fifth warp runs the row's Sinkhorn while the four combine warps
 // stream R (the stats launch leaves the comb logits in the workspace).
-template <bool kNorm, bool kSink, bool kMx = false>
+template <bool kSink, bool kMx = false>
 __global__ void __launch_bounds__(kCnThreads + 32)
 combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
                     const uint4 *__restrict__ w, float norm_eps, uint4 *__restrict__ out,
@@ -132,7 +126,7 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
   }
   const float4 pq = __ldg(pre + row);
   const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
-  combine_row<kNorm, kMx>(R, pv, w, norm_eps, out, row, mxq, mxs);
+  combine_row<kMx>(R, pv, w, norm_eps, out, row, mxq, mxs);
 }
 
 }  // namespace
@@ -140,7 +134,7 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
 cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w,
                                 float norm_eps, int64_t rows, int64_t logical_rows,
                                 uint16_t *x_norm, cudaStream_t s) {
-  return launch_pdl(combine_norm_kernel<true, false>, dim3((unsigned)rows), dim3(kCnThreads), 0, s,
+  return launch_pdl(combine_norm_kernel<false>, dim3((unsigned)rows), dim3(kCnThreads), 0, s,
                     1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
                     reinterpret_cast<const uint4 *>(norm_w), norm_eps,
                     reinterpret_cast<uint4 *>(x_norm), nullptr, nullptr, 0.f, 0,
@@ -154,24 +148,16 @@ cudaError_t launch_combine_norm_sinkhorn(const uint16_t *R, const float *pre,
                                          uint16_t *x_norm, cudaStream_t s, uint8_t *mx_q,
                                          uint8_t *mx_s) {
   if (mx_q)
-    return launch_pdl(combine_norm_kernel<true, true, true>, dim3((unsigned)rows),
+    return launch_pdl(combine_norm_kernel<true, true>, dim3((unsigned)rows),
                       dim3(kCnThreads + 32), 0, s, 1, use_pdl(logical_rows),
                       reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
                       reinterpret_cast<const uint4 *>(norm_w), norm_eps,
                       reinterpret_cast<uint4 *>(x_norm), logit, comb, sink_eps, iters,
                       reinterpret_cast<uint2 *>(mx_q), mx_s);
-  return launch_pdl(combine_norm_kernel<true, true>, dim3((unsigned)rows), dim3(kCnThreads + 32),
+  return launch_pdl(combine_norm_kernel<true>, dim3((unsigned)rows), dim3(kCnThreads + 32),
                     0, s, 1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R),
                     reinterpret_cast<const float4 *>(pre), reinterpret_cast<const uint4 *>(norm_w),
                     norm_eps, reinterpret_cast<uint4 *>(x_norm), logit, comb, sink_eps, iters,
-                    (uint2 *)nullptr, (uint8_t *)nullptr);
-}
-
-cudaError_t launch_head_combine(const uint16_t *R, const float *pre, int64_t rows,
-                                int64_t logical_rows, uint16_t *y, cudaStream_t s) {
-  return launch_pdl(combine_norm_kernel<false, false>, dim3((unsigned)rows), dim3(kCnThreads), 0, s,
-                    1, use_pdl(logical_rows), reinterpret_cast<const uint4 *>(R), reinterpret_cast<const float4 *>(pre),
-                    nullptr, 0.f, reinterpret_cast<uint4 *>(y), nullptr, nullptr, 0.f, 0,
                     (uint2 *)nullptr, (uint8_t *)nullptr);
 }
 

@@ -320,6 +320,22 @@ __device__ __forceinline__ void drain1(uint32_t b, uint32_t parity) {
   }
 }
 
+// packed fp32 pairs (fma.rn.f32x2: two independent fp32 FMAs, each rounded
+// as fmaf is)
+__device__ __forceinline__ uint64_t f2_of_bf2(uint32_t w) {   // bf16 pair -> fp32 pair, exact
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+  return r;
+}
+__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float f2_sum(uint64_t v) {   // first + second
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+
 __device__ __forceinline__ float lo_bf(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

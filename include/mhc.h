@@ -101,22 +101,23 @@ const char *mhc_last_cuda_error(void);
  * for a call on `rows` rows: the pre gates [rows, 4] fp32 and the comb logits
  * [rows, 16] fp32 that a two-launch path hands from its tensor-core launch to
  * its streaming combine, each rounded up to 256 bytes (0 for rows <= 0).
- * mhc_hc_head uses the first part; mhc_pre's own kernels use none of it. */
+ * mhc_fused_post_pre uses it; this build's mhc_pre and mhc_hc_head kernels
+ * use none of it. */
 size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
- * or nonzero once a tensor-core kernel (of mhc_pre, mhc_hc_head or
+ * or nonzero once a cluster kernel (of mhc_pre, mhc_hc_head or
  * mhc_fused_post_pre) gave up a bounded wait (it then returned early and
  * its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
  * the device's pending work.  Returns MHC_OK or MHC_ERR_NULL/MHC_ERR_CUDA. */
 int mhc_kernel_status(uint32_t *status, int reset);
 
-/* Where the waits recorded in the status word ended, for diagnosis: bit s
- * (s < 16) of the status word means a bounded wait at site s of the fused pre
- * kernel expired, bit 16 + s that a wait at site s gave up because its CTA had
- * already aborted.  where64[s] (expired) and where64[32 + s] (gave up) hold
- * (tile << 8) | CTA rank in its cluster of the last such event.  where64 has
- * 64 entries.  Synchronous. */
+/* Where the waits of mhc_pre's one-pass kernel ended, for diagnosis: bit s
+ * (s < 16) of its error word means a bounded wait at site s expired, bit
+ * 16 + s that a wait at site s gave up because its CTA had already aborted.
+ * where64[s] (expired) and where64[32 + s] (gave up) hold (tile << 8) | CTA
+ * rank in its cluster of the last such event.  where64 has 64 entries.
+ * Synchronous. */
 int mhc_kernel_status_detail(uint32_t *where64);
 
 /*
@@ -330,14 +331,15 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
  *   pre[i] = sigmoid(mix[i] * scale[0] + base[i]) + hc_eps
  *   y[m,h] = bf16( sum_i pre[i] * R[m, i, h] )     (fp32 sum, one rounding)
  *
- * Chunks of more than 256 rows (logical_rows): two launches, mhc_pre's
- * tensor-core stats kernel built for 4 mixes (the gates go to the
- * workspace), then a streaming combine.  Chunks of up to 256 rows: one
- * launch of 4-CTA clusters that forms the 4 dots in fp32 on the CUDA cores
- * and combines each row from shared memory, reading R once (the workspace
- * is then not used, but must still be passed).  The two paths form the dots
- * differently and agree to the gate tolerance; every row range of a chunk
- * gives the whole-chunk bits.
+ * One launch that reads R once and combines every row from shared memory.
+ * Chunks of more than 256 rows (logical_rows): 16-CTA clusters over 32-row
+ * tiles (head_tile.cu), the 4 dots on the tensor cores against fn split
+ * into bf16 hi + lo, the tile kept in a 12-stage shared-memory ring until
+ * its gates come back.  Chunks of up to 256 rows: 4-CTA clusters that form
+ * the 4 dots in fp32 on the CUDA cores (head_onepass.cu).  The two paths
+ * form the dots differently and agree to the gate tolerance; every row
+ * range of a chunk gives the whole-chunk bits.  Neither uses the workspace,
+ * which is validated as for mhc_pre.
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual after the last layer
