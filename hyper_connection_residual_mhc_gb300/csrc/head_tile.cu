@@ -32,11 +32,13 @@
 //   * the owner warp sums the 16 CTAs' records in CTA order, forms rsqrt,
 //     the mixes and the 4 gates, and sends the gates to all 16 CTAs;
 //   * eight combine warps, once a tile's gates are in, form y from the
-//     tile's stages in shared memory, write it, and free the stages.
+//     tile's stages in shared memory block by block, freeing each stage as
+//     soon as its values are in registers, and write y.
 // The exchanges are asynchronous remote stores (st.async) counted in bytes on
 // the receiver's mbarrier.  The pushes of tile t wait until this CTA's
-// combine is done with tile t - 2 (every owner has then consumed the receive
-// buffer tile t reuses, and this CTA's gate buffer for tile t is free).
+// combine has read the gates of tile t - 2 (every owner has then consumed
+// the receive buffer tile t reuses, and this CTA's gate buffer for tile t is
+// free).
 //
 // Every row is reduced in one fixed order that depends only on its own data,
 // so any row range gives the whole-chunk bits.  Every wait is bounded (~2 s);
@@ -75,7 +77,6 @@ constexpr int kFnBlkBytes = kN * kBk * 2;      // 4096: fn's B tile for one bloc
 constexpr int kDCols = kN;                     // accumulator columns per buffer
 constexpr int kTmemCols = 64;
 constexpr int kRec = 8;                        // pushed record: 4 dots, sum x^2, 3 pad
-constexpr int kChunks = kHs / 8;               // 40 16-byte chunks of a row per stream
 constexpr int kNR = 2, kNG = 2;                // receive and gate buffers
 
 static_assert(kHs % kBk == 0 && kTR % kCl == 0 && kOwn == 2, "");
@@ -92,8 +93,7 @@ constexpr int kCombN = 8, kComb0 = 3;          // kComb0 re-arms the gate barrie
 constexpr int kWarps = 19;
 constexpr int kThreads = kWarps * 32;          // 608
 constexpr int kCombT = kCombN * 32;            // 256
-constexpr int kCombItems = kTR * kChunks / kCombT;   // 5 (row, chunk) items per thread
-static_assert(kRead0 % 4 == 0 && kTR * kChunks == kCombItems * kCombT, "");
+static_assert(kRead0 % 4 == 0 && kCombT == kTR * (kBk / 8), "one (row, chunk) of a block per combine thread");
 
 // 96 registers a thread: warp w runs on SM sub-partition w % 4, whose 16 K
 // registers are allocated to a warp in units of 512; 5 warps x 3072 fit
@@ -110,7 +110,7 @@ enum Bar : int {
   B_SEMPTY = B_SFULL + 2,         // [2] a tile's sums of squares read
   B_RX = B_SEMPTY + 2,            // [kNR] the 16 CTAs' records landed (bytes)
   B_GIN = B_RX + kNR,             // [kNG] the 16 owners' gates landed (bytes)
-  B_GREAD = B_GIN + kNG,          // [kNG] the combine warps are done with the tile
+  B_GREAD = B_GIN + kNG,          // [kNG] the combine warps have read the tile's gates
   B_FNREADY = B_GREAD + kNG,      // fn's B tiles written
   B_DRAIN = B_FNREADY + 1,        // final MMA drain
   B_COUNT = B_DRAIN + 1
@@ -169,7 +169,8 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kOffMisc);
   Abort ab{reinterpret_cast<volatile int *>(sm + C::kOffMisc + 4), crank, &g_htile_error,
            g_htile_where, g_htile_where_aborted};
-  // a push of tile t waits until this CTA's combine is done with tile t - 2
+  // a push of tile t waits until this CTA's combine has read the gates of
+  // tile t - 2
   auto push_ready = [&](int t, int site) -> bool {
     if (t < kNG) return true;
     const int tr = t - kNG;
@@ -446,27 +447,39 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     }
   } else if (is_comb) {
     // ---- combine warps: y of the CTA's columns from the tile's stages --------
-    // thread t: items t + 256 k (k = 0..4) of the tile's 32 rows x 40
-    // 16-byte chunks, row-major
+    // block by block, so each stage is handed back as soon as it is combined:
+    // thread t takes row t / 8, chunk t % 8 of the block's 64 columns
     const int t = comb_index(warp) * 32 + lane;
+    const int rr = t >> 3, c8 = t & 7;
     const float *gin = reinterpret_cast<const float *>(sm + C::kOffGin);
     for (int it = 0; it < T; ++it) {
       const int buf = it % kNG;
       if (!waitw(bar(B_GIN + buf), (uint32_t)((it / kNG) & 1), true, ab, 12, it)) break;
       const int g0 = it * kHb;                    // the tile's first stage
-      const int64_t row0 = (int64_t)(cid + it * ncl) * kTR;
-#pragma unroll
-      for (int k = 0; k < kCombItems; ++k) {
-        const int item = t + kCombT * k;
-        const int rr = item / kChunks, cq = item % kChunks;
-        const int b = cq >> 3, c8 = cq & 7;
-        const uint8_t *st = sm + C::kOffStage + ((g0 + b) % kStages) * kStageBytes;
-        const float4 pq = *reinterpret_cast<const float4 *>(gin + buf * (kTR * kHC) + rr * kHC);
-        const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
+      const int64_t grow = (int64_t)(cid + it * ncl) * kTR + rr;
+      const float4 pq = *reinterpret_cast<const float4 *>(gin + buf * (kTR * kHC) + rr * kHC);
+      const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
+      // every lane has its gates: the gate buffer is free for tile it + kNG
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_GREAD + buf));
+        if (warp == kComb0) mbar_expect_tx(bar(B_GIN + buf), C::kGinBytes);
+      }
+#pragma unroll 1
+      for (int b = 0; b < kHb; ++b) {
+        const int s = (g0 + b) % kStages;
+        const uint8_t *st = sm + C::kOffStage + s * kStageBytes;
         uint4 rv[kHC];
 #pragma unroll
         for (int i = 0; i < kHC; ++i)
           rv[i] = *reinterpret_cast<const uint4 *>(st + sw128_off(4 * rr + i, c8));
+        // the block's values are in registers: hand the stage back
+        uint32_t sink = 0;
+#pragma unroll
+        for (int i = 0; i < kHC; ++i) sink |= rv[i].x;
+        asm volatile("" ::"r"(sink));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_EMPTY + s));
         float yv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -477,18 +490,10 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
             acc = fmaf(pv[i], __uint_as_float(((&rv[i].x)[e >> 1] << sh) & 0xFFFF0000u), acc);
           yv[e] = acc;
         }
-        const int64_t grow = row0 + rr;
         if (grow < a.rows)
-          st_stream(reinterpret_cast<uint4 *>(a.y + grow * kH + (int64_t)crank * kHs + 8 * cq),
+          st_stream(reinterpret_cast<uint4 *>(a.y + grow * kH + (int64_t)crank * kHs + b * kBk +
+                                              8 * c8),
                     pack8_rn(yv));
-      }
-      // every lane is done with the tile: count this warp out of its stages
-      // and its gates, and arm the gate buffer's next phase
-      __syncwarp();
-      if (lane == 0) {
-        for (int b = 0; b < kHb; ++b) mbar_arrive(bar(B_EMPTY + (g0 + b) % kStages));
-        mbar_arrive(bar(B_GREAD + buf));
-        if (warp == kComb0) mbar_expect_tx(bar(B_GIN + buf), C::kGinBytes);
       }
     }
   }
