@@ -108,6 +108,15 @@ __device__ __forceinline__ uint2 mx_block8(const float (&v)[8], uint32_t &scale_
 
 // Streaming (evict-first) 16-byte global accesses for data touched once.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
+// 16 bytes of data that no thread writes during the kernel, without
+// allocating an L1 line (a second read of data that L2 still holds)
+__device__ __forceinline__ uint4 ld_nc_noalloc(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
 
 // ---- programmatic dependent launch -----------------------------------------

@@ -44,7 +44,8 @@
 //   * the Sinkhorn warp runs the 4x4 Sinkhorn of 32 queued rows at a time,
 //     one row per lane, and writes comb.
 //   * combine warps, once a tile's gates are in, read the tile's columns
-//     back (from L2: the stats pass read them a few microseconds earlier),
+//     back (from L2: the stats pass read them a few microseconds earlier;
+//     non-coherent loads that allocate no L1 line),
 //     form y = sum_i pre_i R_i, x_norm = bf16(y / rms(y) * w) (and, in the
 //     MXFP8 build, its E4M3 codes and block scales) and store them.
 // A stage is freed as soon as its MMAs have completed, so the
@@ -651,23 +652,23 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       const int buf = it % kNG;
       if (!waitw(bar(B_GIN + buf), (uint32_t)((it / kNG) & 1), true, ab, 12, it)) break;
       const int64_t row0 = (int64_t)(cid + it * ncl) * kTR;
-      // two rows' loads in flight ahead of the arithmetic
+      // one row's loads at a time: more in flight only added to the load on
+      // the shared-memory / L1 data path the MMAs and TMA also use
       uint4 rv[2][kHC];
       auto load = [&](int u, uint4 (&dst)[kHC]) {
         const int64_t grow = row0 + r0 + kCombRowStep * u;
         if (grow < a.rows) {
           const uint4 *src = reinterpret_cast<const uint4 *>(a.R + grow * kK + col);
 #pragma unroll
-          for (int i = 0; i < kHC; ++i) dst[i] = __ldcs(src + i * (kH / 8));
+          for (int i = 0; i < kHC; ++i) dst[i] = ld_nc_noalloc(src + i * (kH / 8));
         } else {
 #pragma unroll
           for (int i = 0; i < kHC; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       };
-      load(0, rv[0]);
-      load(1, rv[1]);
 #pragma unroll
       for (int u = 0; u < kCombItems; ++u) {
+        load(u, rv[u & 1]);
         const float *gr = gin + buf * (kTR * 8) + (r0 + kCombRowStep * u) * 8;
         const float4 pq = *reinterpret_cast<const float4 *>(gr);
         const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
@@ -682,7 +683,6 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
             acc = fmaf(pv[i], __uint_as_float(((&rv[u & 1][i].x)[e >> 1] << sh) & 0xFFFF0000u), acc);
           v[e] = (acc * rn) * wf[e];
         }
-        if (u + 2 < kCombItems) load(u + 2, rv[u & 1]);
         const uint4 xb = pack8_rn(v);
         const int64_t grow = row0 + r0 + kCombRowStep * u;
         const bool live = grow < a.rows;
