@@ -294,9 +294,14 @@ struct Abort {
   }
 };
 
-// whole warp; the outcome is warp-uniform
+// whole warp; the outcome is warp-uniform.  A phase that has already
+// completed costs one test: the clock is read only once a test has failed.
 __device__ __forceinline__ bool waitw(uint32_t b, uint32_t parity, bool cl, const Abort &ab,
                                       int site, int it) {
+  {
+    const bool done = cl ? mbar_test_cluster(b, parity) : mbar_test(b, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+  }
   const uint64_t t0 = now_ns();
   for (;;) {
     const bool done = cl ? mbar_test_cluster(b, parity) : mbar_test(b, parity);
