@@ -16,8 +16,8 @@
 //     one 64-column block of all four streams, a single 3-D box (columns,
 //     streams, rows) that lands as a [128, 64] bf16 tile with the four
 //     streams of a row adjacent (tile line 4 r + i is stream i of tile row r),
-//     128-byte swizzled.  It also prefetches the boxes two ring-depths ahead
-//     into L2, so a stage is held for an L2 fetch rather than an HBM one.
+//     128-byte swizzled.  (Prefetching boxes into L2 one to four ring depths
+//     ahead changed nothing measurable and is not done.)
 //   * one thread of warp 1 issues tcgen05.mma with that stage as A (M = 128)
 //     and fn's bf16 hi/lo for the block as B (N = 192: for each stream j, the
 //     hi and lo rows of mix c at 48 j + 2 c and 48 j + 2 c + 1), resident in
@@ -92,7 +92,6 @@ constexpr int kOwn = kTR / kCl;                // 2 rows finalised per CTA per t
 constexpr int kSlotBytes = kTR * kBk * 2;      // 4096: one stream's box
 constexpr int kStageBytes = kHC * kSlotBytes;  // 16384: the four streams of a block
 constexpr int kStages = 5;
-constexpr int kAhead = 2 * kStages;            // stages prefetched into L2 ahead of the loads
 constexpr int kM = kHC * kTR;                  // 128: MMA M (line 4 r + i)
 constexpr int kFnRowsPerStream = 2 * kMix;     // 48: hi and lo of 24 mixes, interleaved
 constexpr int kN = kHC * kFnRowsPerStream;     // 192: MMA N
@@ -332,11 +331,6 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
         if (lane == 0) {
           mbar_expect_tx(bar(B_FULL + s), kStageBytes);
           tma_load_3d(stage_addr(s), &tmap, (int)crank * kHs + b * kBk, 0, y, bar(B_FULL + s));
-          // the stage kAhead groups on, fetched into L2 now so that its load
-          // (once a stage is free) is an L2 hit
-          const int ga = g + kAhead, ita = ga / kHb, ba = ga % kHb;
-          if (ita < T)
-            tma_prefetch_3d(&tmap, (int)crank * kHs + ba * kBk, 0, (cid + ita * ncl) * kTR);
         }
         __syncwarp();
       }
