@@ -244,7 +244,7 @@ class Weights:
 
 
 def mhc_prepare_weights(fn, *, stream=None) -> Weights:
-    """fn [24, 20480] f32 -> a handle holding fn's copy and the stats kernel's
+    """fn [24, 20480] f32 -> a handle holding fn's copy and the one-pass kernels
     operand image (see mhc_prepare_weights in include/mhc.h)."""
     import torch
     _need(fn, "fn", torch.float32, (MIX, K))

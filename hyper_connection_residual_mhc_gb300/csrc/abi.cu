@@ -107,9 +107,10 @@ size_t logit_bytes(int64_t rows) {
 
 size_t mhc_pre_workspace_bytes(int64_t rows) {
   if (rows <= 0) return 0;
-  // handed from the stats launch to the combine launch: the pre gates
-  // [rows, 4] fp32, then the comb logits [rows, 16] fp32, each 256-byte
-  // rounded (the decode-size path uses none of it)
+  // handed from the fused call's tensor-core launch to its combine launch:
+  // the pre gates [rows, 4] fp32, then the comb logits [rows, 16] fp32, each
+  // 256-byte rounded (mhc_pre, mhc_hc_head and the decode-size paths use
+  // none of it)
   return gate_bytes(rows) + logit_bytes(rows);
 }
 

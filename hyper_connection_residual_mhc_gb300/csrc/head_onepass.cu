@@ -31,8 +31,8 @@
 // The phases are separated by CTA barriers, and with one 640-thread CTA per
 // SM a tile costs ~3.9 us per cluster in latency rather than bytes (about 550
 // instructions per warp at ~14 cycles each, half of it waiting at barriers),
-// so the library uses this kernel for chunks of up to 256 rows, where one
-// launch beats the two-launch path, and the two launches above.
+// so the library uses this kernel for chunks of up to 256 rows and the tiled
+// kernel (head_tile.cu) above.
 //
 // Every row is reduced in one fixed order that depends only on its own data,
 // so any row range gives the whole-chunk bits.  Every wait is bounded (~2 s);

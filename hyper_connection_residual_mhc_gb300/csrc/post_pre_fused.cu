@@ -9,9 +9,9 @@
 //
 // Unfused, R' is written by hc_post and read back by the stats; here the
 // stats take R' from shared memory where it was just formed, so for them R'
-// costs one write and no read.  The decomposition follows the stats kernel
-// (pre_stats.cu): a cluster of 16 CTAs owns a 128-row tile at a time and CTA
-// s owns hidden columns [320 s, 320 s + 320) of all four streams.  Per tile
+// costs one write and no read.  A cluster of 16 CTAs owns a 128-row tile at
+// a time and CTA s owns hidden columns [320 s, 320 s + 320) of all four
+// streams.  Per tile
 // and CTA the 320 columns go through in ten "half-sets" of 32 columns, four
 // in flight:
 //   * a producer thread loads a half-set -- R_0..3 and y, 128 rows x 32

@@ -108,7 +108,8 @@ __device__ __forceinline__ void sinkhorn_row(const float *__restrict__ logit,
 }
 
 // kSink: a fifth warp runs the row's Sinkhorn while the four combine warps
-// stream R (the stats launch leaves the comb logits in the workspace).
+// stream R (the fused call's tensor-core launch leaves the comb logits in the
+// workspace).
 template <bool kSink, bool kMx = false>
 __global__ void __launch_bounds__(kCnThreads + 32)
 combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
@@ -117,8 +118,8 @@ combine_norm_kernel(const uint4 *__restrict__ R, const float4 *__restrict__ pre,
                     int iters, uint2 *__restrict__ mxq, uint8_t *__restrict__ mxs) {
   pdl_wait();
   pdl_trigger();
-  // last rows first: after mhc_pre's stats launch the most recently read rows
-  // are the ones still in L2
+  // last rows first: after the fused call's tensor-core launch the most
+  // recently written rows are the ones still in L2
   const int64_t row = (int64_t)gridDim.x - 1 - blockIdx.x;
   if (threadIdx.x >= kCnThreads) {
     if constexpr (kSink) sinkhorn_row(logit, comb, row, sink_eps, iters);

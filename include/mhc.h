@@ -243,8 +243,8 @@ int mhc_combine_norm(const uint16_t *R, const float *pre, const uint16_t *norm_w
  *   fn [24, 20480] fp32, device, 16-byte aligned (hc_fn of one sublayer).
  *   Allocates device memory on the current device (about 5.9 MB, the only
  *   allocation libmhc makes) and enqueues on `stream`: a copy of fn, and
- *   fn's bf16 hi/lo operand images for the tensor-core stats kernel and for
- *   the fused post -> pre kernel (the same bits those kernels would form
+ *   fn's bf16 hi/lo operand images for the one-pass pre kernel and for the
+ *   fused post -> pre kernel (the same bits those kernels would form
  *   themselves).  The handle may be
  *   used by calls enqueued after it on `stream`, or on any stream once the
  *   caller has ordered them after it; fn itself may be freed or changed
@@ -391,7 +391,7 @@ int mhc_hc_head(const uint16_t *R, const float *fn, const float *scale, const fl
  *   mhc_fused_post_pre_prepared (same arguments, checks and bits, without
  *   pre_out/mix_out) that also writes x_q [rows, 5120] and x_s [rows, 160]
  *   of the next sublayer's x_norm, as mhc_pre_mxfp8 does: above 48 rows the
- *   combine launch writes them beside x_norm, at decode sizes one more
+ *   fused call's combine launch writes them beside x_norm, at decode sizes one more
  *   launch follows the fused decode kernel.  MHC_ERR_NULL if x_q or x_s is
  *   NULL.
  * mhc_quantize_mxfp8(x, rows, cols, logical_rows, q, s, stream)

@@ -54,6 +54,6 @@ def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch)
     assert bench.traffic_for("mhc_post") == 1234
     (src / "post.cu").write_text("// the kernel, changed since\n")
     assert bench.traffic_for("mhc_post") is None
-    assert bench.traffic_for("mhc_pre_stats") is None          # no entry, no file read error
+    assert bench.traffic_for("no_such_kernel") is None         # no entry, no file read error
     os.remove(tmp_path / "profiles" / "traffic.json")
     assert bench.traffic_for("mhc_post") is None
