@@ -129,13 +129,14 @@ int mhc_kernel_status_detail(uint32_t *where64) {
 
 int mhc_kernel_status(uint32_t *status, int reset) {
   if (!status) return MHC_ERR_NULL;
-  unsigned int w = 0, w2 = 0, w3 = 0, w4 = 0;
+  unsigned int w = 0, w2 = 0, w3 = 0, w4 = 0, w5 = 0;
   cudaError_t e = mhc::head_tile_error_word(&w, reset != 0);
   if (e == cudaSuccess) e = mhc::fused_post_pre_error_word(&w2, reset != 0);
   if (e == cudaSuccess) e = mhc::head_error_word(&w3, reset != 0);
   if (e == cudaSuccess) e = mhc::onepass_error_word(&w4, reset != 0);
+  if (e == cudaSuccess) e = mhc::decode_error_word(&w5, reset != 0);
   if (e != cudaSuccess) return cuda_fail(e);
-  *status = w | w2 | w3 | w4;
+  *status = w | w2 | w3 | w4 | w5;
   return MHC_OK;
 }
 

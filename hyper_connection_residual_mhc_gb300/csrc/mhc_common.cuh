@@ -183,9 +183,10 @@ cudaError_t launch_combine_norm(const uint16_t *R, const float *pre, const uint1
                                 uint16_t *x_norm, cudaStream_t s);
 
 // decode-size chunks (logical_rows <= kDecodeMaxRows): all of mhc_pre in one
-// launch of 16-CTA clusters, up to 8 rows per cluster pass, no scratch
+// launch of 16-CTA clusters, a group of up to 8 rows per cluster, no scratch
 // (pre_decode.cu)
 constexpr int64_t kDecodeMaxRows = 48;
+cudaError_t decode_error_word(unsigned int *out, bool reset);
 cudaError_t launch_pre_decode(const uint16_t *R, const float *fn, const float *scale,
                               const float *base, const uint16_t *norm_w, int64_t rows,
                               int64_t logical_rows, const mhc_params &p, uint16_t *x_norm,

@@ -8,30 +8,30 @@
 // _combine_norm_fused.
 //
 // At these sizes the work is a few MFLOP and a few MB, so time is latency:
-// launches, round trips to L2, and the serial Sinkhorn.  One cluster of 16
-// CTAs takes up to 8 rows; CTA s owns hidden columns [320 s, 320 s + 320) of
-// all four streams (1280 of the 20480 k).  Thread t handles stream t / 80 and
-// four consecutive columns, and keeps its 4 x 24 fn values and its rows' x in
-// registers for the whole kernel:
+// launches, round trips to L2 and between CTAs, and the serial Sinkhorn.
+// One cluster of 16 CTAs takes a group of up to 8 rows; CTA s owns hidden
+// columns [320 s, 320 s + 320) of all four streams (1280 of the 20480 k).
+// Thread t handles stream t / 80 and four consecutive columns, and keeps its
+// 4 x 24 fn values and its rows' x in registers for the whole kernel:
 //   1. per row, the thread's 25 partials (24 dots, sum of squares), summed
 //      over the warp by a fixed transpose tree and over the CTA's 10 warps in
 //      warp order, go to the row's owner CTA (rank = row in the group);
-//   -- cluster barrier --
-//   2. the owner (warp 9 of that CTA) sums the 16 CTAs' partials in rank
-//      order, computes rsqrt and the gates, and sends the 4 pre gates to
-//      every CTA;
-//   -- cluster barrier --
-//   3. each CTA forms y on its 320 columns, sends its partial sum of y^2 to
-//      every CTA -- meanwhile the owner warp runs the Sinkhorn (16 lanes) and
-//      writes post, comb and the exports: nothing downstream in this kernel
-//      needs comb, so the owner arrives at the next barrier before it starts;
-//   -- cluster barrier --
-//   4. each CTA sums the 16 partials in rank order and writes its 320
-//      columns of x_norm.
-// A cluster takes groups of up to 8 rows, as many as spread the chunk over
-// the co-resident clusters.  The barriers are the hardware cluster barrier;
-// every thread of every CTA arrives at each of them (no early exit), so each
-// completes.
+//   2. in the owner CTA, warp 9 sums the 16 CTAs' partials in rank order,
+//      computes rsqrt and the gates, and sends the 4 pre gates to every CTA;
+//      beside it warp 8 forms the same sums of the comb logits and runs the
+//      Sinkhorn (nothing in this kernel waits on comb, an output);
+//   3. warps 0..2 of each CTA form y on its 320 columns and send each warp's
+//      partial sums of y^2 to every CTA;
+//   4. each CTA sums the 48 partials (CTA by CTA, warps in order) and writes
+//      its 320 columns of x_norm.
+// Every exchange is a set of 16-byte st.async stores into the receiving
+// CTA's shared memory, counted as transaction bytes on one of its three
+// mbarriers (partials, gates, y^2), each armed once with the bytes it will
+// receive; a receiver's bounded wait ends when they have landed.  Two
+// hardware cluster barriers remain: one before the first remote store (every
+// CTA's mbarriers exist), its wait overlapping the loads, and one before
+// exit (every CTA has issued its last store), arrived at as each warp
+// finishes sending.
 //
 // Built twice: kPost = false is mhc_pre; kPost = true is mhc_fused_post_pre
 // at these sizes (deepseek_v4.py, the use_fused_mhc_post_pre path): each
@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "mhc_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace mhc {
 
@@ -53,7 +54,11 @@ constexpr int kDRows = 8;                     // rows per cluster
 constexpr int kDHs = kH / kDCl;               // 320 columns per CTA
 constexpr int kDQ = kDHs / 4;                 // 80 threads per stream
 constexpr int kDPart = kMix + 1;              // 24 dots + sum of squares
+constexpr int kDPartV4 = (kDPart + 3) / 4;    // 16-byte stores per row (7)
+constexpr int kDPartV = 4 * kDPartV4;         // the partials padded to 28
 static_assert(kDQ * kHC == kDThreads, "one thread per (stream, 4 columns)");
+
+__device__ unsigned int g_dec_error;   // bit s: a wait at site s expired
 
 __device__ __forceinline__ uint32_t d_smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,20 +73,6 @@ __device__ __forceinline__ uint32_t d_mapa(uint32_t addr, uint32_t cta) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(cta));
   return r;
 }
-__device__ __forceinline__ void d_st_remote(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void d_cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void d_cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void d_cluster_sync() {
-  d_cluster_arrive();
-  d_cluster_wait();
-}
-
 // v[0..31] of every lane -> lane l holds the warp's sum of index l (a fixed
 // pairing tree: halves at distance 16, 8, 4, 2, 1)
 __device__ __forceinline__ float d_transpose_sum32(float (&v)[32], int lane) {
@@ -147,22 +138,86 @@ __device__ __forceinline__ uint2 post_cols(const DecArgs &a, int64_t row, int si
   return o;
 }
 
+// 1/x for x >= 1e-30 or +inf (the Sinkhorn's sums, each holding eps; 1 +
+// exp(-l)): the hardware approximation refined by one Newton step for the
+// reciprocal, r + r (1 - x r) with fused multiply-adds, which leaves it
+// within about an ulp; 0 where the approximation is 0 (x = inf, or 1/x below
+// the normal range), as the IEEE quotient gives.  No branch, so the four
+// reciprocals of a Sinkhorn step overlap.
+__device__ __forceinline__ float d_recip(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r == 0.f ? 0.f : fmaf(r, fmaf(-x, r, 1.0f), r);
+}
+
+// 1/sqrt(x) for x >= 1e-30 or +inf (mean squares plus eps): the hardware
+// approximation refined by one Newton step for the reciprocal square root,
+// r (3 - x r^2) / 2; 0 for x = inf, as 1/sqrt gives
+__device__ __forceinline__ float d_rsqrt(float x) {
+  float r;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r == 0.f ? 0.f : r * fmaf(-0.5f * x * r, r, 1.5f);
+}
+
+// Bounded wait, whole warp, on a barrier that other CTAs' st.async bytes
+// complete (acquire at cluster scope; each barrier has one phase).  Expiry
+// sets bit `site` of the error word and returns false: the warp then carries
+// on with what has landed, so every thread still reaches the final cluster
+// barrier.
+__device__ __forceinline__ bool d_wait(uint32_t b, int site) {
+  if (__all_sync(0xffffffffu, ptx::mbar_test_cluster(b, 0))) return true;
+  const uint64_t t0 = ptx::now_ns();
+  for (;;) {
+    if (__all_sync(0xffffffffu, ptx::mbar_test_cluster(b, 0))) return true;
+    if (__any_sync(0xffffffffu, ptx::now_ns() - t0 > ptx::kTimeoutNs)) {
+      if ((threadIdx.x & 31) == 0) atomicOr(&g_dec_error, 1u << site);
+      return false;
+    }
+  }
+}
+
+constexpr int kOwnerWarp = kDWarps - 1;        // the row owner's gates
+constexpr int kSinkWarp = kDWarps - 2;         // the row owner's Sinkhorn
+static_assert(kSinkWarp * 32 >= kDQ, "the owner warps must not own combine columns");
+static_assert(kDPartV4 * kDRows <= 3 * 32, "the partial stores are warps 0..2's");
+
 template <bool kPost>
 __global__ void __cluster_dims__(kDCl, 1, 1) __launch_bounds__(kDThreads, 1)
 pre_decode_kernel(const DecArgs a) {
-  __shared__ float red[kDWarps][kDRows][32];        // per-warp row partials
-  __shared__ float recv[kDCl][kDRows][kDPart];      // owner: partials from each CTA
-  __shared__ float pre_all[kDRows][kHC];            // gates of the group's rows
-  __shared__ float sq[kDCl][kDRows];                // partial sums of y^2 from each CTA
-  __shared__ uint2 xs[kDRows][kHC][kDQ];            // the CTA's x, for the combine
-  __shared__ float dot[kDRows][kDPart];
+  __shared__ __align__(16) float red[kDWarps][kDRows][32];   // per-warp row partials
+  __shared__ __align__(16) float recv[kDCl][kDPartV];        // owner: its row's partials, per CTA
+  __shared__ __align__(16) float pre_all[kDRows][kHC];       // the group rows' pre gates
+  __shared__ __align__(16) float sq[kDCl][3][kDRows];        // y^2 partials, per CTA and warp
+  __shared__ __align__(16) uint2 xs[kDRows][kHC][kDQ];       // the CTA's x, for the combine
+  __shared__ float dot[kDPartV];                             // owner: 24 dots + sum of x^2
+  __shared__ __align__(8) uint64_t bars[3];                  // partials, gates, y^2 landed
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = d_rank();
-  const int cl = (int)(blockIdx.x / kDCl), ncl = (int)(gridDim.x / kDCl);
   const int si = tid / kDQ, q = tid % kDQ;          // stream, 4-column group
   const int k0 = si * kH + (int)rank * kDHs + 4 * q;
   const int h0 = (int)rank * kDHs + 4 * q;          // threads tid < 80: their columns
+  const int G = a.group;
+  const int64_t row0 = (int64_t)(blockIdx.x / kDCl) * G;
+  const int nr = (int)(a.rows - row0 < G ? a.rows - row0 : G);
+  const int ymsg = nr > 4 ? 2 : 1;                  // float4s of y^2 partials per warp pair
+  const uint32_t b_part = d_smem_addr(&bars[0]), b_gate = d_smem_addr(&bars[1]),
+                 b_sq = d_smem_addr(&bars[2]);
+  if (tid == 0) {
+    ptx::mbar_init(b_part, 1);
+    ptx::mbar_init(b_gate, 1);
+    ptx::mbar_init(b_sq, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // each phase completes once the bytes armed here have landed (bytes that
+    // land first count down from zero)
+    if ((int)rank < nr) ptx::mbar_expect_tx(b_part, kDCl * kDPartV * 4);
+    ptx::mbar_expect_tx(b_gate, nr * kHC * 4);
+    ptx::mbar_expect_tx(b_sq, kDCl * 3 * ymsg * 16);
+  }
+  // no CTA may store into another before that one's barriers exist: arrive
+  // now, wait before the first remote store
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
   // A prepared handle's fn copy is never written after preparation, so its
   // loads may overlap the previous launch's tail; anything else waits first.
   float f[kMix][4];
@@ -175,6 +230,16 @@ pre_decode_kernel(const DecArgs a) {
   };
   if (a.fn_stable) load_fn();
   pdl_wait();
+  // the gate weights of the owner warp (pre and post) and the Sinkhorn warp
+  // (comb), in flight while the partials form
+  float w_sc = 0.f, w_base = 0.f;
+  if (warp == kOwnerWarp && (lane & 15) < 8) {
+    w_sc = __ldg(a.scale + ((lane & 15) < 4 ? 0 : 1));
+    w_base = __ldg(a.base + (lane & 15));
+  } else if (warp == kSinkWarp) {
+    w_sc = __ldg(a.scale + 2);
+    w_base = __ldg(a.base + 8 + (lane & 15));
+  }
   if (!a.fn_stable) load_fn();
   float wf[4] = {0.f, 0.f, 0.f, 0.f};
   if (tid < kDQ) {
@@ -182,118 +247,146 @@ pre_decode_kernel(const DecArgs a) {
     wf[0] = __uint_as_float(wv.x << 16); wf[1] = __uint_as_float(wv.x & 0xFFFF0000u);
     wf[2] = __uint_as_float(wv.y << 16); wf[3] = __uint_as_float(wv.y & 0xFFFF0000u);
   }
-  const int G = a.group;
-  const int64_t ngroups = (a.rows + G - 1) / G;
-
-  for (int64_t g = cl; g < ngroups; g += ncl) {    // uniform across the cluster
-    const int64_t row0 = g * G;
-    const int nr = (int)(a.rows - row0 < G ? a.rows - row0 : G);
-    uint2 xr[kDRows];
+  // the cluster wait while loads are in flight (post_cols uses its loads at
+  // once, so the fused build waits before them)
+  if constexpr (kPost) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  uint2 xr[kDRows];
 #pragma unroll
-    for (int r = 0; r < kDRows; ++r) {
-      if constexpr (kPost)
-        xr[r] = r < nr ? post_cols(a, row0 + r, si, k0, h0) : make_uint2(0u, 0u);
-      else
-        xr[r] = r < nr ? __ldg(reinterpret_cast<const uint2 *>(a.R + (row0 + r) * kK + k0))
-                       : make_uint2(0u, 0u);
+  for (int r = 0; r < kDRows; ++r) {
+    if constexpr (kPost)
+      xr[r] = r < nr ? post_cols(a, row0 + r, si, k0, h0) : make_uint2(0u, 0u);
+    else
+      xr[r] = r < nr ? __ldg(reinterpret_cast<const uint2 *>(a.R + (row0 + r) * kK + k0))
+                     : make_uint2(0u, 0u);
+  }
+  if constexpr (!kPost) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+
+  // ---- 1. partials (row loops unrolled with a uniform guard, so the per-row
+  // arrays stay in registers) ---------------------------------------------------
+#pragma unroll
+  for (int r = 0; r < kDRows; ++r) {
+    if (r >= nr) break;
+    const float x[4] = {__uint_as_float(xr[r].x << 16), __uint_as_float(xr[r].x & 0xFFFF0000u),
+                        __uint_as_float(xr[r].y << 16), __uint_as_float(xr[r].y & 0xFFFF0000u)};
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < kMix; ++c) {
+      float s = x[0] * f[c][0];
+#pragma unroll
+      for (int e = 1; e < 4; ++e) s = fmaf(x[e], f[c][e], s);
+      v[c] = s;
     }
+    float ss = x[0] * x[0];
+#pragma unroll
+    for (int e = 1; e < 4; ++e) ss = fmaf(x[e], x[e], ss);
+    v[kMix] = ss;
+#pragma unroll
+    for (int c = kDPart; c < 32; ++c) v[c] = 0.f;
+    red[warp][r][lane] = d_transpose_sum32(v, lane);
+    xs[r][si][q] = xr[r];
+  }
+  __syncthreads();
+  // row r's 25 sums (in warp order; padded with zeros to 28) to CTA r, as
+  // seven 16-byte stores that count on its partials barrier
+  if (tid < nr * kDPartV4) {
+    const int r = tid / kDPartV4, c0 = 4 * (tid % kDPartV4);
+    float4 s = *reinterpret_cast<const float4 *>(&red[0][r][c0]);
+#pragma unroll
+    for (int w = 1; w < kDWarps; ++w) {
+      const float4 t = *reinterpret_cast<const float4 *>(&red[w][r][c0]);
+      s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+    }
+    ptx::st_async_v4(d_mapa(d_smem_addr(&recv[rank][c0]), (uint32_t)r), s.x, s.y, s.z, s.w,
+                     d_mapa(b_part, (uint32_t)r));
+  }
 
-    // ---- 1. partials (row loops unrolled with a uniform guard, so the
-    // per-row arrays stay in registers) --------------------------------------
+  const unsigned full = 0xffffffffu;
+  const bool own = (int)rank < nr;
+  if (warp == kOwnerWarp && own) {
+    // ---- 2. owner of group row `rank`: the pre and post gates, the mixes -----
+    const int64_t row = row0 + rank;
+    d_wait(b_part, 0);
+    if (lane < kDPart) {
+      float s = 0.f;
 #pragma unroll
-    for (int r = 0; r < kDRows; ++r) {
-      if (r >= nr) break;
-      const float x[4] = {__uint_as_float(xr[r].x << 16), __uint_as_float(xr[r].x & 0xFFFF0000u),
-                          __uint_as_float(xr[r].y << 16), __uint_as_float(xr[r].y & 0xFFFF0000u)};
-      float v[32];
-#pragma unroll
-      for (int c = 0; c < kMix; ++c) {
-        float s = x[0] * f[c][0];
-#pragma unroll
-        for (int e = 1; e < 4; ++e) s = fmaf(x[e], f[c][e], s);
-        v[c] = s;
+      for (int src = 0; src < kDCl; ++src) s += recv[src][lane];
+      dot[lane] = s;
+    }
+    __syncwarp();
+    const float rsq = d_rsqrt(fmaf(dot[kMix], 1.0f / (float)kK, a.p.rms_eps));
+    const int e = lane & 15;                  // lanes 16..31 mirror 0..15
+    float gate = 0.f;
+    if (e < 8) {
+      const float l = fmaf(dot[e] * rsq, w_sc, w_base);
+      const float sg = d_recip(1.0f + expf(-l));
+      gate = e < 4 ? sg + a.p.hc_pre_eps : a.p.post_mult * sg;
+    }
+    // the 4 pre gates: lane d < 16 sends them to CTA d as one 16-byte store
+    const float g0 = __shfl_sync(full, gate, 0), g1 = __shfl_sync(full, gate, 1);
+    const float g2 = __shfl_sync(full, gate, 2), g3 = __shfl_sync(full, gate, 3);
+    if (lane < kDCl)
+      ptx::st_async_v4(d_mapa(d_smem_addr(&pre_all[rank][0]), (uint32_t)lane), g0, g1, g2, g3,
+                       d_mapa(b_gate, (uint32_t)lane));
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    if (lane < 16) {
+      if (e >= 4 && e < 8) a.post[row * kHC + (e - 4)] = gate;
+      if (e < 4 && a.pre_out) a.pre_out[row * kHC + e] = gate;
+      if (a.mix_out) {
+        a.mix_out[row * kMix + e] = dot[e] * rsq;
+        if (e < 8) a.mix_out[row * kMix + 16 + e] = dot[16 + e] * rsq;
       }
-      float ss = x[0] * x[0];
-#pragma unroll
-      for (int e = 1; e < 4; ++e) ss = fmaf(x[e], x[e], ss);
-      v[kMix] = ss;
-#pragma unroll
-      for (int c = kDPart; c < 32; ++c) v[c] = 0.f;
-      red[warp][r][lane] = d_transpose_sum32(v, lane);
-      xs[r][si][q] = xr[r];
     }
-    __syncthreads();
-    for (int t = tid; t < nr * kDPart; t += kDThreads) {
-      const int r = t / kDPart, c = t % kDPart;
-      float s = red[0][r][c];
+  } else if (warp == kSinkWarp && own) {
+    // ---- 2'. the same row's Sinkhorn, beside the owner warp: it feeds only
+    // comb, an output, so nothing else waits on it --------------------------
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    const int64_t row = row0 + rank;
+    d_wait(b_part, 0);
+    // lane e < 16 sums comb dot e, lanes 16.. the sum of squares: the owner
+    // warp's sums, in the same order
+    const int idx = lane < 16 ? 8 + lane : kMix;
+    float s = 0.f;
 #pragma unroll
-      for (int w = 1; w < kDWarps; ++w) s += red[w][r][c];
-      d_st_remote(d_mapa(d_smem_addr(&recv[rank][r][c]), (uint32_t)r), s);
-    }
-    d_cluster_sync();
-
-    // ---- 2. owner of group row `rank` (warp 9, which has no combine work):
-    // the gates go to every CTA first; the Sinkhorn then runs while the other
-    // warps do the combine and the norm (it feeds only comb, an output)
-    constexpr int kOwnerWarp = kDWarps - 1;
-    static_assert(kOwnerWarp * 32 >= kDQ, "the owner warp must not own combine columns");
-    if (warp == kOwnerWarp) {
-      const bool own = (int)rank < nr;
-      const int r = own ? (int)rank : 0;
-      const int64_t row = row0 + r;
-      const int e = lane & 15;                // lanes 16..31 mirror 0..15
-      const unsigned full = 0xffffffffu;
-      float rsq = 0.f, gate = 0.f;
-      if (own) {
-        if (lane < kDPart) {
-          float s = 0.f;
+    for (int src = 0; src < kDCl; ++src) s += recv[src][idx];
+    const float ssq = __shfl_sync(full, s, 16);
+    const float rsq = d_rsqrt(fmaf(ssq, 1.0f / (float)kK, a.p.rms_eps));
+    // exp(logits), then the whole 4x4 in every lane: rows then columns, each
+    // sum paired (c0 + c1) + (c2 + c3) plus eps, each entry times the
+    // reciprocal of its sum
+    const float lg = expf(fmaf(s * rsq, w_sc, w_base));
+    float c[kHC][kHC];
 #pragma unroll
-          for (int src = 0; src < kDCl; ++src) s += recv[src][r][lane];
-          dot[r][lane] = s;
-        }
-        __syncwarp();
-        rsq = 1.0f / sqrtf(dot[r][kMix] / (float)kK + a.p.rms_eps);
-        if (e < 8) {
-          const float l = fmaf(dot[r][e] * rsq, __ldg(a.scale + (e < 4 ? 0 : 1)), __ldg(a.base + e));
-          const float sg = 1.0f / (1.0f + expf(-l));
-          gate = e < 4 ? sg + a.p.hc_pre_eps : a.p.post_mult * sg;
-        }
-        // the 4 pre gates to every CTA of the cluster (lanes 0..3 x 16 CTAs)
-        for (int t = lane; t < kHC * kDCl; t += 32) {
-          const float gv = __shfl_sync(full, gate, t & 3);
-          d_st_remote(d_mapa(d_smem_addr(&pre_all[r][t & 3]), (uint32_t)(t >> 2)), gv);
-        }
+    for (int j = 0; j < kHC; ++j)
+#pragma unroll
+      for (int i = 0; i < kHC; ++i) c[j][i] = __shfl_sync(full, lg, 4 * j + i);
+    for (int k = 0; k < a.p.sinkhorn_iters; ++k) {
+#pragma unroll
+      for (int j = 0; j < kHC; ++j) {
+        const float d = d_recip(((c[j][0] + c[j][1]) + (c[j][2] + c[j][3])) + a.p.hc_sinkhorn_eps);
+#pragma unroll
+        for (int i = 0; i < kHC; ++i) c[j][i] = c[j][i] * d;
       }
-      d_cluster_arrive();        // barrier 2: the gates are out
-      d_cluster_wait();
-      d_cluster_arrive();        // barrier 3: this warp sends no partial sums
-      if (own) {
-        // Sinkhorn on exp(logits): lane e holds comb[e/4][e%4]
-        float cm = expf(fmaf(dot[r][8 + e] * rsq, __ldg(a.scale + 2), __ldg(a.base + 8 + e)));
-        for (int k = 0; k < a.p.sinkhorn_iters; ++k) {
-          float rs = cm + __shfl_xor_sync(full, cm, 1);
-          rs = rs + __shfl_xor_sync(full, rs, 2);
-          cm = cm / (rs + a.p.hc_sinkhorn_eps);
-          float cs = cm + __shfl_xor_sync(full, cm, 4);
-          cs = cs + __shfl_xor_sync(full, cs, 8);
-          cm = cm / (cs + a.p.hc_sinkhorn_eps);
-        }
-        if (lane < 16) {
-          a.comb[row * 16 + e] = cm;
-          if (e >= 4 && e < 8) a.post[row * kHC + (e - 4)] = gate;
-          if (e < 4 && a.pre_out) a.pre_out[row * kHC + e] = gate;
-          if (a.mix_out) {
-            a.mix_out[row * kMix + e] = dot[r][e] * rsq;
-            if (e < 8) a.mix_out[row * kMix + 16 + e] = dot[r][16 + e] * rsq;
-          }
-        }
+#pragma unroll
+      for (int i = 0; i < kHC; ++i) {
+        const float d = d_recip(((c[0][i] + c[1][i]) + (c[2][i] + c[3][i])) + a.p.hc_sinkhorn_eps);
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) c[j][i] = c[j][i] * d;
       }
-      d_cluster_wait();
-      continue;                  // nothing of steps 3 and 4 is this warp's
     }
-    d_cluster_sync();            // barrier 2
-
-    // ---- 3. y on this CTA's columns; partial sums of y^2 to every CTA --------
+    if (lane < kHC) {
+      float4 *o = reinterpret_cast<float4 *>(a.comb + row * 16);
+#pragma unroll
+      for (int j = 0; j < kHC; ++j)
+        if (j == lane) o[j] = make_float4(c[j][0], c[j][1], c[j][2], c[j][3]);
+    }
+  } else if (warp >= 3) {
+    // warps 3..9 without an owner's work: nothing of steps 3 and 4 is theirs
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  } else {
+    // ---- 3. y on this CTA's columns (threads tid < 80); each warp's partial
+    // sums of y^2 to every CTA ------------------------------------------------
+    d_wait(b_gate, 1);
     float y[kDRows][4];
     float sy[kDRows];
 #pragma unroll
@@ -325,42 +418,48 @@ pre_decode_kernel(const DecArgs a) {
         for (int e = 0; e < 4; ++e) y[r][e] = 0.f;
       }
     }
-    // warps 0..2 (the 80 threads, zeros elsewhere): lane l < 8 gets the
-    // warp's sum for row l -- a fixed tree (halves 4, 2, 1, then 8, 16)
-    if (warp < 3) {
+    // lane l < 8 gets the warp's sum for row l -- a fixed tree (halves 4, 2,
+    // 1, then 8, 16)
 #pragma unroll
-      for (int w = 4; w >= 1; w >>= 1) {
-        const bool up = (lane & w) != 0;
+    for (int w = 4; w >= 1; w >>= 1) {
+      const bool up = (lane & w) != 0;
 #pragma unroll
-        for (int jj = 0; jj < w; ++jj) {
-          const float send = up ? sy[jj] : sy[jj + w];
-          const float keep = up ? sy[jj + w] : sy[jj];
-          sy[jj] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
+      for (int jj = 0; jj < w; ++jj) {
+        const float send = up ? sy[jj] : sy[jj + w];
+        const float keep = up ? sy[jj + w] : sy[jj];
+        sy[jj] = keep + __shfl_xor_sync(full, send, w);
       }
-      float s = sy[0];
-      s += __shfl_xor_sync(0xffffffffu, s, 8);
-      s += __shfl_xor_sync(0xffffffffu, s, 16);
-      if (lane < kDRows) red[warp][lane][0] = s;
     }
-    // warps 0..8 only: the owner warp has left for its Sinkhorn
-    asm volatile("bar.sync 1, %0;" ::"n"(kOwnerWarp * 32) : "memory");
-    if (tid < nr * kDCl) {
-      const int r = tid / kDCl, dst = tid % kDCl;
-      const float s = (red[0][r][0] + red[1][r][0]) + red[2][r][0];
-      d_st_remote(d_mapa(d_smem_addr(&sq[rank][r]), (uint32_t)dst), s);
+    float s = sy[0];
+    s += __shfl_xor_sync(full, s, 8);
+    s += __shfl_xor_sync(full, s, 16);
+    // lane l: this warp's rows 4 (l / 16) .. + 3 to CTA l % 16, one 16-byte
+    // store
+    {
+      const int dst = lane & 15, hf = lane >> 4;
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float t = __shfl_sync(full, s, 4 * hf + e);
+        v[e] = 4 * hf + e < nr ? t : 0.f;
+      }
+      if (hf < ymsg)
+        ptx::st_async_v4(d_mapa(d_smem_addr(&sq[rank][warp][4 * hf]), (uint32_t)dst), v[0], v[1],
+                         v[2], v[3], d_mapa(b_sq, (uint32_t)dst));
     }
-    d_cluster_sync();
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     // ---- 4. x_norm on this CTA's columns ---------------------------------------
+    d_wait(b_sq, 2);
     if (tid < kDQ) {
 #pragma unroll
       for (int r = 0; r < kDRows; ++r) {
         if (r >= nr) break;
         float tot = 0.f;
 #pragma unroll
-        for (int src = 0; src < kDCl; ++src) tot += sq[src][r];
-        const float rn = 1.0f / sqrtf(tot / (float)kH + a.p.norm_eps);
+        for (int src = 0; src < kDCl; ++src) tot += (sq[src][0][r] + sq[src][1][r]) + sq[src][2][r];
+        const float rn = d_rsqrt(fmaf(tot, 1.0f / (float)kH, a.p.norm_eps));
         float v[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = (y[r][e] * rn) * wf[e];
@@ -371,8 +470,10 @@ pre_decode_kernel(const DecArgs a) {
       }
     }
   }
-  // the next launch may start scheduling once every CTA got here
+  // the next launch may start scheduling once every CTA got here; no CTA
+  // leaves before every CTA of the cluster has issued its last store
   pdl_trigger();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 std::mutex g_dec_mu;
@@ -422,8 +523,11 @@ cudaError_t launch_decode(DecArgs a, int64_t logical_rows, cudaStream_t s) {
   // does not depend on the grouping)
   int64_t grp = (logical_rows + ncl_max - 1) / ncl_max;
   grp = grp < 1 ? 1 : (grp > kDRows ? kDRows : grp);
+  // one group per cluster (a chunk of up to 48 rows needs at most 8
+  // clusters; more would queue behind the co-resident ones)
   const int64_t groups = (a.rows + grp - 1) / grp;
-  const int clusters = (int)(groups < ncl_max ? groups : ncl_max);
+  if (groups > kDecodeMaxRows) return cudaErrorInvalidValue;
+  const int clusters = (int)groups;
   a.group = (int)grp;
   // (the cluster shape is the kernel's compile-time __cluster_dims__)
   return launch_pdl(pre_decode_kernel<kPost>, dim3((unsigned)(clusters * kDCl)), dim3(kDThreads),
@@ -431,6 +535,15 @@ cudaError_t launch_decode(DecArgs a, int64_t logical_rows, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t decode_error_word(unsigned int *out, bool reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_dec_error, sizeof(unsigned int));
+  if (e == cudaSuccess && reset) {
+    const unsigned int z = 0;
+    e = cudaMemcpyToSymbol(g_dec_error, &z, sizeof z);
+  }
+  return e;
+}
 
 cudaError_t launch_pre_decode(const uint16_t *R, const float *fn, const float *scale,
                               const float *base, const uint16_t *norm_w, int64_t rows,

@@ -107,8 +107,9 @@ size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
  * or nonzero once a cluster kernel (of mhc_pre, mhc_hc_head or
- * mhc_fused_post_pre) gave up a bounded wait (it then returned early and
- * its outputs are incomplete).  reset != 0 clears it.  Synchronous: waits for
+ * mhc_fused_post_pre, at any size) gave up a bounded wait (it then returned
+ * early, or finished on what had landed: its outputs are incomplete).
+ * reset != 0 clears it.  Synchronous: waits for
  * the device's pending work.  Returns MHC_OK or MHC_ERR_NULL/MHC_ERR_CUDA. */
 int mhc_kernel_status(uint32_t *status, int reset);
 

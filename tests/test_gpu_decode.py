@@ -65,3 +65,15 @@ def test_same_rows_through_both_paths_agree(torch, mhc, oracle_mod):
     _check_pre(torch, big, o, c)
     # the two paths sum in different orders: equal gates to fp32 rounding
     assert (dec["pre"] - big["pre"]).abs().max().item() <= 2e-6
+
+
+def test_decode_waits_all_complete(torch, mhc):
+    # groups of 1..6 rows a cluster (one or two 16-byte stores of y^2
+    # partials per warp and CTA pair), full and partial last groups, then the
+    # status word: no bounded wait of the decode kernel may have expired
+    assert mhc.mhc_kernel_status(reset=True) == 0
+    for rows, logical in ((1, 1), (5, 5), (40, 40), (45, 45), (48, 48), (3, 48), (7, 48)):
+        c = Case(torch, rows, 120 + rows)
+        c.gpu_pre(torch, mhc, logical_rows=logical)
+    torch.cuda.synchronize()
+    assert mhc.mhc_kernel_status() == 0
