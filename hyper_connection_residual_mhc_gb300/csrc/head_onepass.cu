@@ -228,12 +228,12 @@ head_onepass_kernel(const HeadArgs a) {
           for (int src = 0; src < kHCl; ++src) acc += recv[(s * kHCl + src) * kTV + r * kNP + j];
           d[j] = acc;
         }
-        const float rsq = 1.0f / sqrtf(d[kHeadMixes] / (float)kK + a.norm_eps);
+        const float rsq = rsqrt_nr(fmaf(d[kHeadMixes], 1.0f / (float)kK, a.norm_eps));
         const bool mine = r0 + r < a.rows && rank == 0;
 #pragma unroll
         for (int c = 0; c < kHeadMixes; ++c) {
           const float mx = d[c] * rsq;
-          const float sg = 1.0f / (1.0f + expf(-fmaf(mx, sc, __ldg(a.base + c))));
+          const float sg = rcp_nr(1.0f + expf(-fmaf(mx, sc, __ldg(a.base + c))));
           gate[r * kHC + c] = sg + a.hc_eps;
           if (mine && a.pre_out) a.pre_out[(r0 + r) * kHC + c] = sg + a.hc_eps;
           if (mine && a.mix_out) a.mix_out[(r0 + r) * kHeadMixes + c] = mx;

@@ -424,9 +424,9 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
       __syncwarp();
       if (lane == 0) mbar_expect_tx(bar(B_RX + rb), C::kRxBytes);
       const float sq = __shfl_sync(full, v, hb + kMixes);
-      const float rsq = 1.0f / sqrtf(sq / (float)kK + a.norm_eps);
+      const float rsq = rsqrt_nr(fmaf(sq, 1.0f / (float)kK, a.norm_eps));
       const float mx = v * rsq;
-      const float sg = 1.0f / (1.0f + expf(-fmaf(mx, sc, bs)));
+      const float sg = rcp_nr(1.0f + expf(-fmaf(mx, sc, bs)));
       const float gate = sg + a.hc_eps;
       float pg[kHC];
 #pragma unroll

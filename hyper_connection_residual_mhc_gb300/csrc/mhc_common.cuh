@@ -119,6 +119,27 @@ __device__ __forceinline__ uint4 ld_nc_noalloc(const uint4 *p) {
 }
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
 
+// 1/x for x >= 1e-30 or +inf (the Sinkhorn's sums, each holding eps; 1 +
+// exp(-l)): the hardware approximation refined by one Newton step for the
+// reciprocal, r + r (1 - x r) with fused multiply-adds, which leaves it
+// within about an ulp; 0 where the approximation is 0 (x = inf, or 1/x below
+// the normal range), as the IEEE quotient gives.  No branch, so the four
+// reciprocals of a Sinkhorn step overlap.
+__device__ __forceinline__ float rcp_nr(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r == 0.f ? 0.f : fmaf(r, fmaf(-x, r, 1.0f), r);
+}
+
+// 1/sqrt(x) for x >= 1e-30 or +inf (mean squares plus eps): the hardware
+// approximation refined by one Newton step for the reciprocal square root,
+// r (3 - x r^2) / 2; 0 for x = inf, as 1/sqrt gives
+__device__ __forceinline__ float rsqrt_nr(float x) {
+  float r;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r == 0.f ? 0.f : r * fmaf(-0.5f * x * r, r, 1.5f);
+}
+
 // ---- programmatic dependent launch -----------------------------------------
 // The library's launches carry programmatic stream serialization, so a
 // kernel's CTAs may be scheduled while the kernel before it on the stream is

@@ -385,11 +385,11 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
       rq[e] = acc0;
       if (e + 16 <= kMix) rq[e + 16] = acc1;
       __syncwarp();
-      const float rsq = 1.0f / sqrtf(rq[kMix] / (float)kK + a.rms_eps);
+      const float rsq = rsqrt_nr(fmaf(rq[kMix], 1.0f / (float)kK, a.rms_eps));
       float gate = 0.f;
       if (e < 8) {
         const float l = fmaf(rq[e] * rsq, e < 4 ? sc0 : sc1, bgate);
-        const float sg = 1.0f / (1.0f + expf(-l));
+        const float sg = rcp_nr(1.0f + expf(-l));
         gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
       }
       const float lc = fmaf(rq[8 + e] * rsq, sc2, bcomb);

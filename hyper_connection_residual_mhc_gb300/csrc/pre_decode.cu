@@ -138,27 +138,6 @@ __device__ __forceinline__ uint2 post_cols(const DecArgs &a, int64_t row, int si
   return o;
 }
 
-// 1/x for x >= 1e-30 or +inf (the Sinkhorn's sums, each holding eps; 1 +
-// exp(-l)): the hardware approximation refined by one Newton step for the
-// reciprocal, r + r (1 - x r) with fused multiply-adds, which leaves it
-// within about an ulp; 0 where the approximation is 0 (x = inf, or 1/x below
-// the normal range), as the IEEE quotient gives.  No branch, so the four
-// reciprocals of a Sinkhorn step overlap.
-__device__ __forceinline__ float d_recip(float x) {
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r == 0.f ? 0.f : fmaf(r, fmaf(-x, r, 1.0f), r);
-}
-
-// 1/sqrt(x) for x >= 1e-30 or +inf (mean squares plus eps): the hardware
-// approximation refined by one Newton step for the reciprocal square root,
-// r (3 - x r^2) / 2; 0 for x = inf, as 1/sqrt gives
-__device__ __forceinline__ float d_rsqrt(float x) {
-  float r;
-  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r == 0.f ? 0.f : r * fmaf(-0.5f * x * r, r, 1.5f);
-}
-
 // Bounded wait, whole warp, on a barrier that other CTAs' st.async bytes
 // complete (acquire at cluster scope; each barrier has one phase).  Expiry
 // sets bit `site` of the error word and returns false: the warp then carries
@@ -313,12 +292,12 @@ pre_decode_kernel(const DecArgs a) {
       dot[lane] = s;
     }
     __syncwarp();
-    const float rsq = d_rsqrt(fmaf(dot[kMix], 1.0f / (float)kK, a.p.rms_eps));
+    const float rsq = rsqrt_nr(fmaf(dot[kMix], 1.0f / (float)kK, a.p.rms_eps));
     const int e = lane & 15;                  // lanes 16..31 mirror 0..15
     float gate = 0.f;
     if (e < 8) {
       const float l = fmaf(dot[e] * rsq, w_sc, w_base);
-      const float sg = d_recip(1.0f + expf(-l));
+      const float sg = rcp_nr(1.0f + expf(-l));
       gate = e < 4 ? sg + a.p.hc_pre_eps : a.p.post_mult * sg;
     }
     // the 4 pre gates: lane d < 16 sends them to CTA d as one 16-byte store
@@ -350,7 +329,7 @@ pre_decode_kernel(const DecArgs a) {
 #pragma unroll
     for (int src = 0; src < kDCl; ++src) s += recv[src][idx];
     const float ssq = __shfl_sync(full, s, 16);
-    const float rsq = d_rsqrt(fmaf(ssq, 1.0f / (float)kK, a.p.rms_eps));
+    const float rsq = rsqrt_nr(fmaf(ssq, 1.0f / (float)kK, a.p.rms_eps));
     // exp(logits), then the whole 4x4 in every lane: rows then columns, each
     // sum paired (c0 + c1) + (c2 + c3) plus eps, each entry times the
     // reciprocal of its sum
@@ -363,13 +342,13 @@ pre_decode_kernel(const DecArgs a) {
     for (int k = 0; k < a.p.sinkhorn_iters; ++k) {
 #pragma unroll
       for (int j = 0; j < kHC; ++j) {
-        const float d = d_recip(((c[j][0] + c[j][1]) + (c[j][2] + c[j][3])) + a.p.hc_sinkhorn_eps);
+        const float d = rcp_nr(((c[j][0] + c[j][1]) + (c[j][2] + c[j][3])) + a.p.hc_sinkhorn_eps);
 #pragma unroll
         for (int i = 0; i < kHC; ++i) c[j][i] = c[j][i] * d;
       }
 #pragma unroll
       for (int i = 0; i < kHC; ++i) {
-        const float d = d_recip(((c[0][i] + c[1][i]) + (c[2][i] + c[3][i])) + a.p.hc_sinkhorn_eps);
+        const float d = rcp_nr(((c[0][i] + c[1][i]) + (c[2][i] + c[3][i])) + a.p.hc_sinkhorn_eps);
 #pragma unroll
         for (int j = 0; j < kHC; ++j) c[j][i] = c[j][i] * d;
       }
@@ -459,7 +438,7 @@ pre_decode_kernel(const DecArgs a) {
         float tot = 0.f;
 #pragma unroll
         for (int src = 0; src < kDCl; ++src) tot += (sq[src][0][r] + sq[src][1][r]) + sq[src][2][r];
-        const float rn = d_rsqrt(fmaf(tot, 1.0f / (float)kH, a.p.norm_eps));
+        const float rn = rsqrt_nr(fmaf(tot, 1.0f / (float)kH, a.p.norm_eps));
         float v[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = (y[r][e] * rn) * wf[e];

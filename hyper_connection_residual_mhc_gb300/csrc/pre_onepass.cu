@@ -531,13 +531,13 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
 #pragma unroll
       for (int p = 0; p < kNGram; ++p) G[p] = val(24 + p);
       const float ssx = (G[0] + G[1]) + (G[2] + G[3]);
-      const float rsq = 1.0f / sqrtf(ssx / (float)kK + a.rms_eps);
+      const float rsq = rsqrt_nr(fmaf(ssx, 1.0f / (float)kK, a.rms_eps));
       const float dg = e < 8 ? v0 : 0.f;          // dot e (gates)
       const float dc = val(8 + e);                // dot 8 + e (comb logit e)
       float gate = 0.f;
       if (e < 8) {
         const float l = fmaf(dg * rsq, e < 4 ? sc0 : sc1, bgate);
-        const float sg = 1.0f / (1.0f + expf(-l));
+        const float sg = rcp_nr(1.0f + expf(-l));
         gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
       }
       const float lc = fmaf(dc * rsq, sc2, bcomb);
@@ -554,7 +554,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       off = fmaf(p[1] * p[3], G[8], off);
       off = fmaf(p[2] * p[3], G[9], off);
       const float ssy = fmaxf(fmaf(2.0f, off, diag), 0.f);
-      const float rn = 1.0f / sqrtf(ssy / (float)kH + a.norm_eps);
+      const float rn = rsqrt_nr(fmaf(ssy, 1.0f / (float)kH, a.norm_eps));
       // broadcast this row's pre gates and 1/rms(y): lane e -> CTA e, 32
       // bytes counted on that CTA's gate barrier
       {
@@ -589,9 +589,9 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
   } else if (warp == kSinkWarp) {
     // ---- Sinkhorn warp: hc_split_sinkhorn's 4x4 Sinkhorn, one row per lane --
     // Row sums pair (c0 + c1) + (c2 + c3), likewise the column sums; eps is
-    // added to every sum, and each entry is multiplied by the correctly
-    // rounded reciprocal of it (four divisions per step instead of sixteen:
-    // each division's slow-path branch serialises it).
+    // added to every sum, and each entry is multiplied by its reciprocal
+    // (rcp_nr: no branch, so a step's four reciprocals overlap; an IEEE
+    // division or reciprocal per sum serialised them, 8 us a batch).
     const float *sk = reinterpret_cast<const float *>(sm + C::kOffSk);
     const int nb = (T + kSkTiles - 1) / kSkTiles;
     const int r = lane & (kSkRows - 1);
@@ -614,13 +614,13 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       for (int k = 0; k < a.iters; ++k) {
 #pragma unroll
         for (int j = 0; j < kHC; ++j) {
-          const float d = 1.0f / (((c[j][0] + c[j][1]) + (c[j][2] + c[j][3])) + a.sink_eps);
+          const float d = rcp_nr(((c[j][0] + c[j][1]) + (c[j][2] + c[j][3])) + a.sink_eps);
 #pragma unroll
           for (int i = 0; i < kHC; ++i) c[j][i] = c[j][i] * d;
         }
 #pragma unroll
         for (int i = 0; i < kHC; ++i) {
-          const float d = 1.0f / (((c[0][i] + c[1][i]) + (c[2][i] + c[3][i])) + a.sink_eps);
+          const float d = rcp_nr(((c[0][i] + c[1][i]) + (c[2][i] + c[3][i])) + a.sink_eps);
 #pragma unroll
           for (int j = 0; j < kHC; ++j) c[j][i] = c[j][i] * d;
         }

@@ -62,7 +62,7 @@ __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const f
     // the 4 combine warps only (a block may carry a Sinkhorn warp besides)
     asm volatile("bar.sync 1, %0;" ::"n"(kCnThreads) : "memory");
     const float tot = ((red[0] + red[1]) + red[2]) + red[3];
-    const float rn = 1.0f / sqrtf(tot / (float)kH + norm_eps);
+    const float rn = rsqrt_nr(fmaf(tot, 1.0f / (float)kH, norm_eps));
 
 #pragma unroll
     for (int q = 0; q < kCnChunks; ++q) {
@@ -88,8 +88,8 @@ __device__ __forceinline__ void combine_row(const uint4 *__restrict__ R, const f
 
 // The row's 4x4 Sinkhorn (hc_split_sinkhorn) from its 16 comb logits, by one
 // warp: lane e holds comb[e/4][e%4] (lanes 16..31 mirror 0..15); each
-// iteration divides by the row sums (pairs (c0 + c1) + (c2 + c3)), then by
-// the column sums, eps added to every sum.
+// iteration scales by the reciprocals of the row sums (pairs (c0 + c1) +
+// (c2 + c3)), then of the column sums, eps added to every sum.
 __device__ __forceinline__ void sinkhorn_row(const float *__restrict__ logit,
                                              float *__restrict__ comb, int64_t row, float eps,
                                              int iters) {
@@ -99,10 +99,10 @@ __device__ __forceinline__ void sinkhorn_row(const float *__restrict__ logit,
   for (int k = 0; k < iters; ++k) {
     float rs = cm + __shfl_xor_sync(full, cm, 1);
     rs = rs + __shfl_xor_sync(full, rs, 2);
-    cm = cm / (rs + eps);
+    cm = cm * rcp_nr(rs + eps);
     float cs = cm + __shfl_xor_sync(full, cm, 4);
     cs = cs + __shfl_xor_sync(full, cs, 8);
-    cm = cm / (cs + eps);
+    cm = cm * rcp_nr(cs + eps);
   }
   if (lane < 16) comb[row * 16 + e] = cm;
 }
