@@ -337,7 +337,9 @@ def mhc_pre_noalloc(R, fn, scale, base, norm_w, x_norm, post, comb, *, logical_r
                     params=None, pre_out=None, mix_out=None, stream=None):
     """mhc_pre for callers that cannot provide device scratch (see mhc_pre_noalloc
     in include/mhc.h).  Allocates nothing: every output is passed in, and the
-    kernels take no scratch.  The same launches and bits as mhc_pre."""
+    kernels take no scratch.  mhc_pre's launches and bits below 2048 logical
+    rows; from 2048 on, the one-pass build that keeps fn resident (mhc_pre's
+    values to within fp32 summation order)."""
     import torch
     rows = int(R.shape[0])
     _need(R, "R", torch.bfloat16, (rows, HC, H))

@@ -107,11 +107,14 @@ size_t logit_bytes(int64_t rows) {
 
 size_t mhc_pre_workspace_bytes(int64_t rows) {
   if (rows <= 0) return 0;
-  // handed from the fused call's tensor-core launch to its combine launch:
-  // the pre gates [rows, 4] fp32, then the comb logits [rows, 16] fp32, each
-  // 256-byte rounded (mhc_pre, mhc_hc_head and the decode-size paths use
-  // none of it)
-  return gate_bytes(rows) + logit_bytes(rows);
+  // mhc_pre: fn's operand image for the streamed one-pass build (chunks of
+  // kStreamMinRows rows and more).  The fused call's tensor-core launch hands
+  // its combine launch the pre gates [rows, 4] fp32, then the comb logits
+  // [rows, 16] fp32, each 256-byte rounded.  mhc_hc_head and the decode-size
+  // paths use none of it.
+  const size_t handoff = gate_bytes(rows) + logit_bytes(rows);
+  const size_t img = mhc::fn_b_img_bytes();
+  return handoff > img ? handoff : img;
 }
 
 size_t mhc_fused_post_pre_workspace_bytes(int64_t rows) {
@@ -206,9 +209,21 @@ int pre_impl(const uint16_t *R, const float *fn, const uint8_t *fn_b_img, const 
       ce = mhc::launch_mx_quantize(x_norm, rows, MHC_HIDDEN, logical_rows, mx_q, mx_s, s);
   } else {
     // one launch that reads R from HBM once (fn's operand tiles from the
-    // handle's image when prepared)
-    ce = mhc::launch_pre_onepass(R, fn, fn_b_img, scale, base, norm_w, rows, logical_rows, p,
-                                 x_norm, post, comb, pre_out, mix_out, s, mx_q, mx_s);
+    // handle's image when prepared).  A chunk that takes the streamed build
+    // without a handle gets its image written into the workspace first, so
+    // mhc_pre and mhc_pre_prepared give the same bits; without a workspace
+    // (mhc_pre_noalloc) the resident build runs.
+    const uint8_t *img = fn_b_img;
+    ce = cudaSuccess;
+    if (!img && logical_rows >= mhc::kStreamMinRows && workspace &&
+        workspace_bytes >= mhc::fn_b_img_bytes()) {
+      uint8_t *ws_img = static_cast<uint8_t *>(workspace);
+      ce = mhc::launch_fn_b_img(fn, ws_img, s);
+      img = ws_img;
+    }
+    if (ce == cudaSuccess)
+      ce = mhc::launch_pre_onepass(R, fn, img, scale, base, norm_w, rows, logical_rows, p,
+                                   x_norm, post, comb, pre_out, mix_out, s, mx_q, mx_s);
   }
   return ce == cudaSuccess ? MHC_OK : cuda_fail(ce);
 }

@@ -273,21 +273,27 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
 cudaError_t launch_fn_prep_sw64(const float *fn, uint8_t *fnp, cudaStream_t s, bool pdl);
 cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset);
 
-// all of mhc_pre in one launch of 16-CTA clusters that reads R from HBM once
-// (pre_onepass.cu): 32-row tiles, the four streams of a 64-column block as
-// one MMA operand against fn's hi/lo for all four streams, one cluster
-// exchange per tile, the combine re-reading its tile from L2.  fn_img: NULL,
-// or the prepared-weights image of fn_b_img_bytes() (then fn is not read).
-// mx_q / mx_s non-NULL: x_norm's MXFP8 codes [rows, 5120] and linear ue8m0
-// scales [rows, 160] as well.
+// all of mhc_pre in one launch that reads R from HBM once (pre_onepass.cu):
+// 32-row tiles, the four streams of a 64-column block as one MMA operand
+// against fn's hi/lo for all four streams, one cluster exchange per tile, the
+// combine re-reading its tile from L2.  Two builds: 16-CTA clusters with fn's
+// tiles resident (fn_img NULL: converted from fn in the kernel; else bulk
+// copied from the image), and, for chunks of kStreamMinRows rows and more
+// with fn_img given, 8-CTA clusters that stream fn's tiles from the image
+// beside each block of R (144 SMs instead of 112).  fn_img: NULL, or fn's
+// image of fn_b_img_bytes() (then fn is not read).  mx_q / mx_s non-NULL:
+// x_norm's MXFP8 codes [rows, 5120] and linear ue8m0 scales [rows, 160] as
+// well.
+constexpr int64_t kStreamMinRows = 2048;
 cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t *fn_img,
                                const float *scale, const float *base, const uint16_t *norm_w,
                                int64_t rows, int64_t logical_rows, const mhc_params &p,
                                uint16_t *x_norm, float *post, float *comb, float *pre_out,
                                float *mix_out, cudaStream_t s, uint8_t *mx_q = nullptr,
                                uint8_t *mx_s = nullptr);
-// prepared weights: fn [24, 20480] fp32 -> the one-pass kernel's B tiles of
-// all 16 cluster ranks (fn_b_img_bytes() bytes)
+// fn [24, 20480] fp32 -> the one-pass kernels' B tiles, laid out for 16 ranks
+// of 320 columns (fn_b_img_bytes() bytes); the prepared weights hold one, and
+// mhc_pre writes one into its workspace for the streamed build
 size_t fn_b_img_bytes();
 cudaError_t launch_fn_b_img(const float *fn, uint8_t *img, cudaStream_t s);
 cudaError_t onepass_error_word(unsigned int *out, bool reset);

@@ -83,12 +83,13 @@ namespace {
 using namespace ptx;
 
 // ---- geometry -------------------------------------------------------------
-constexpr int kCl = 16;                        // CTAs per cluster (K split)
-constexpr int kHs = kH / kCl;                  // 320 hidden columns per CTA
+// Two builds.  kCl = 16: a CTA takes 1280 k (320 hidden columns of all four
+// streams) and keeps fn's operand tiles for them resident in shared memory
+// (120 KB); 7 such clusters fit, 112 SMs.  kCl = 8: a CTA takes 2560 k and
+// streams fn's tile of each block from the prepared image beside the block's
+// R box; 18 clusters fit, 144 SMs.
 constexpr int kBk = 64;                        // hidden columns per box (128-byte rows)
-constexpr int kHb = kHs / kBk;                 // 5 blocks (stages) per tile
 constexpr int kTR = 32;                        // rows per tile
-constexpr int kOwn = kTR / kCl;                // 2 rows finalised per CTA per tile
 constexpr int kSlotBytes = kTR * kBk * 2;      // 4096: one stream's box
 constexpr int kStageBytes = kHC * kSlotBytes;  // 16384: the four streams of a block
 constexpr int kStages = 5;
@@ -101,9 +102,10 @@ constexpr int kD2Col = 2 * kDCols;             // the Gram accumulator (128 colu
 constexpr int kTmemCols = 512;
 constexpr int kRec = 36;                       // pushed record: 24 dots, 10 Gram, 2 pad
 constexpr int kNGram = 10;                     // Gram entries (i <= j)
-constexpr int kChunks = kHs / 8;               // 40 16-byte chunks of a row per stream
+// the prepared image is laid out for 16 ranks of 5 blocks; rank s of the
+// 8-CTA build reads ranks 2 s and 2 s + 1, i.e. blocks 10 s .. 10 s + 9
+constexpr int kImgRanks = 16, kImgHs = kH / kImgRanks, kImgHb = kImgHs / kBk;
 
-static_assert(kHs % kBk == 0 && kTR % kCl == 0 && kOwn == 2, "");
 static_assert(kD2Col + kM <= kTmemCols, "two dot accumulators and the Gram fit in tensor memory");
 static_assert(kN % 16 == 0 && kN <= 256, "MMA N for M = 128");
 
@@ -118,12 +120,28 @@ constexpr int kThreads = kWarps * 32;          // 608
 constexpr int kCombT = kCombN * 32;            // 320 combine threads
 constexpr int kNR = kOwnerN;                   // receive buffers (one per owner warp)
 constexpr int kNG = 4;                         // gate buffers (tiles the combine may lag)
-constexpr int kSkTiles = 16;                   // tiles per Sinkhorn batch (32 rows)
-constexpr int kSkRows = kSkTiles * kOwn;
+constexpr int kSkRows = 32;                    // rows per Sinkhorn batch (one per lane)
 static_assert(kRead0 % 4 == 0, "lane quarters follow warp & 3");
-static_assert(kCombT % kChunks == 0 && (kTR * kChunks) % kCombT == 0, "combine items tile evenly");
-constexpr int kCombItems = kTR * kChunks / kCombT;   // 4 rows per combine thread
-constexpr int kCombRowStep = kCombT / kChunks;       // 8
+
+template <int kCl_>
+struct Geo {
+  static constexpr int kCl = kCl_;                 // CTAs per cluster (K split)
+  static constexpr bool kStream = kCl_ == 8;       // fn streamed beside each R box
+  static constexpr int kHs = kH / kCl;             // hidden columns per CTA
+  static constexpr int kHb = kHs / kBk;            // blocks (stages) per tile
+  static constexpr int kOwn = kTR / kCl;           // rows finalised per CTA per tile
+  static constexpr int kPairs = kOwn / 2;          // owner passes, two rows each
+  static constexpr int kSkTiles = kSkRows / kOwn;  // tiles per Sinkhorn batch
+  static constexpr int kChunks = kHs / 8;          // 16-byte chunks of a row per stream
+  static constexpr int kCombItems = kTR * kChunks / kCombT;   // rows per combine thread
+  static constexpr int kCombRowStep = kCombT / kChunks;
+  static constexpr int kRing = kStageBytes + (kStream ? kN * kBk * 2 : 0);   // a ring stage
+  static constexpr int kFnItems = kHb * kHC * kMix * 8;   // 8-k items of a CTA's fn slice
+  static_assert(kCl == 16 || kCl == 8, "the two builds");
+  static_assert(kHs % kBk == 0 && kTR % kCl == 0 && kOwn % 2 == 0, "");
+  static_assert(kCombT % kChunks == 0 && (kTR * kChunks) % kCombT == 0, "combine items tile evenly");
+  static_assert(kCl <= 16, "one owner lane per destination CTA");
+};
 
 // mbarrier slots (arrays are given explicit, non-overlapping ranges)
 enum Bar : int {
@@ -143,12 +161,13 @@ enum Bar : int {
 };
 static_assert(B_COUNT == 2 * kStages + 5 + kNR + 2 * kNG + 6, "barrier slots overlap");
 
-template <bool kMx>
+template <bool kMx, int kCl>
 struct Cfg {
-  static constexpr int kOffFn = 0;                                    // [5 blocks][192][64] bf16
-  static constexpr int kOffStage = kOffFn + kHb * kFnBlkBytes;        // [5][128][64] bf16
-  static constexpr int kOffRx = kOffStage + kStages * kStageBytes;    // [kNR][16 src][2 rows][36]
-  static constexpr int kRxBytes = kCl * kOwn * kRec * 4;
+  using G = Geo<kCl>;
+  static constexpr int kOffFn = 0;                                    // resident build: [5 blocks][192][64] bf16
+  static constexpr int kOffStage = G::kStream ? 0 : G::kHb * kFnBlkBytes;   // [5 stages][128 (+ 192 streamed)][64] bf16
+  static constexpr int kOffRx = kOffStage + kStages * G::kRing;       // [kNR][kCl src][kOwn rows][36]
+  static constexpr int kRxBytes = kCl * G::kOwn * kRec * 4;
   static constexpr int kOffGin = kOffRx + kNR * kRxBytes;             // [kNG][32 rows][8]
   static constexpr int kGinBytes = kTR * 8 * 4;
   static constexpr int kOffSk = kOffGin + kNG * kGinBytes;            // [2][32 rows][16] logits
@@ -157,7 +176,7 @@ struct Cfg {
   static constexpr int kOffMisc = kOffBar + B_COUNT * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;             // slack to align the base
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
-  static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kFnBlkBytes % 1024 == 0,
+  static_assert(kOffStage % 1024 == 0 && G::kRing % 1024 == 0 && kFnBlkBytes % 1024 == 0,
                 "SW128 tiles need 1024-byte alignment");
   static_assert(kOffRx % 16 == 0 && kOffGin % 16 == 0 && kOffSk % 16 == 0 && kOffBar % 8 == 0,
                 "vector and barrier alignment");
@@ -171,14 +190,14 @@ constexpr uint32_t kIdescG = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kM
                              ((uint32_t)(kM >> 4) << 24);
 
 // fn's 8 consecutive k (16-byte chunk q of hidden block b, stream j, mix c)
-// of cluster rank `rank` -> bf16 hi = bf16(f) into B row 48 j + 2 c and lo =
+// of image rank `rank` (16 ranks of 320 columns) -> bf16 hi = bf16(f) into B row 48 j + 2 c and lo =
 // bf16(f - hi) into row 48 j + 2 c + 1 of the block's tile (K-major,
 // 128-byte swizzle).  The in-kernel conversion and the prepared-weights image both use
 // this routine, so they give the same bits.
 __device__ __forceinline__ void fn_b_item(const float *__restrict__ fn, int rank, int b, int j,
                                           int c, int q, uint8_t *tile) {
   const float4 *src = reinterpret_cast<const float4 *>(fn + (int64_t)c * kK + j * kH +
-                                                       rank * kHs + b * kBk + 8 * q);
+                                                       rank * kImgHs + b * kBk + 8 * q);
   const float4 f0 = __ldg(src), f1 = __ldg(src + 1);
   const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
   uint32_t hw[4], lw[4];
@@ -195,7 +214,7 @@ __device__ __forceinline__ void fn_b_item(const float *__restrict__ fn, int rank
   *reinterpret_cast<uint4 *>(tile + (nl >> 3) * 1024 + (nl & 7) * 128 + ((q ^ (nl & 7)) << 4)) =
       make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
-constexpr int kFnItems = kHb * kHC * kMix * 8;   // 3840 items of 8 k per rank
+constexpr int kImgItems = kImgHb * kHC * kMix * 8;   // 3840 items of 8 k per image rank
 
 struct OnePassArgs {
   const uint16_t *R;
@@ -221,10 +240,11 @@ struct OnePassArgs {
 // so 19 warps x 3072 fit the 64 K-register file with one block per SM)
 constexpr int kMaxRegs = 96;
 static_assert(kWarps * ((kMaxRegs * 32 + 511) / 512 * 512) <= 65536, "register budget of one block per SM");
-template <bool kMx>
+template <bool kMx, int kCl>
 __global__ void __maxnreg__(kMaxRegs)
 pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a) {
-  using C = Cfg<kMx>;
+  using G = Geo<kCl>;
+  using C = Cfg<kMx, kCl>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -234,7 +254,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
   const int cid = (int)cluster_id(), ncl = (int)cluster_count();
   const int T = cid < a.num_tiles ? (a.num_tiles - 1 - cid) / ncl + 1 : 0;   // our tiles
   auto bar = [&](int i) -> uint32_t { return sb + C::kOffBar + 8u * (uint32_t)i; };
-  auto stage_addr = [&](int s) -> uint32_t { return sb + C::kOffStage + (uint32_t)(s * kStageBytes); };
+  auto stage_addr = [&](int s) -> uint32_t { return sb + C::kOffStage + (uint32_t)(s * G::kRing); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kOffMisc);
   Abort ab{reinterpret_cast<volatile int *>(sm + C::kOffMisc + 4), crank, &g_onepass_error,
            g_onepass_where, g_onepass_where_aborted};
@@ -266,7 +286,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_DFULL + b), 1);
       mbar_init(bar(B_DEMPTY + b), kReadN);
-      mbar_init(bar(B_SKFULL + b), kSkTiles);
+      mbar_init(bar(B_SKFULL + b), G::kSkTiles);
       mbar_init(bar(B_SKFREE + b), 1);
     }
     for (int b = 0; b < kNG; ++b) {
@@ -275,7 +295,9 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     }
     for (int b = 0; b < kNR; ++b) mbar_init(bar(B_RX + b), 1);
     mbar_init(bar(B_D2EMPTY), kReadN);
-    mbar_init(bar(B_FNREADY), a.fn_img ? 1 : kCombN);
+    // (streamed: no resident tiles to wait for, the phase completes at once)
+    mbar_init(bar(B_FNREADY), G::kStream || a.fn_img ? 1 : kCombN);
+    if (G::kStream) mbar_arrive(bar(B_FNREADY));
     mbar_init(bar(B_DRAIN), 1);
     // the byte-counted barriers are armed for their first phase here; each
     // later phase is armed by the side that consumed the previous one
@@ -291,11 +313,12 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
 
-  // fn's B tiles for this CTA's columns: from the prepared image (bulk copies
-  // by the MMA warp) or converted by the combine warps
-  if (a.fn_img) {
+  // fn's B tiles for this CTA's columns (resident build): from the prepared
+  // image (bulk copies by the MMA warp) or converted by the combine warps
+  if (G::kStream) {
+  } else if (a.fn_img) {
     if (warp == kMmaWarp && lane == 0) {
-      constexpr uint32_t kImg = kHb * kFnBlkBytes, kPart = kImg / 4;
+      constexpr uint32_t kImg = G::kHb * kFnBlkBytes, kPart = kImg / 4;
       static_assert(kImg % 64 == 0 && kImg < (1u << 20), "bulk copies of 16-byte multiples");
       mbar_expect_tx(bar(B_FNREADY), kImg);
       const uint8_t *src = a.fn_img + (size_t)crank * kImg;
@@ -304,7 +327,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     }
   } else if (warp >= kComb0 && warp < kComb0 + kCombN) {
     const int t = (warp - kComb0) * 32 + lane;
-    for (int item = t; item < kFnItems; item += kCombT) {
+    for (int item = t; item < G::kFnItems; item += kCombT) {
       const int q = item & 7, c = (item >> 3) % kMix, j = (item / (8 * kMix)) % kHC,
                 b = item / (8 * kMix * kHC);
       fn_b_item(a.fn, (int)crank, b, j, c, q, sm + C::kOffFn + b * kFnBlkBytes);
@@ -322,15 +345,21 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
       const int y = (cid + it * ncl) * kTR;
-      for (int b = 0; b < kHb; ++b, ++g) {
+      for (int b = 0; b < G::kHb; ++b, ++g) {
         const int s = g % kStages;
         if (!waitw(bar(B_EMPTY + s), (uint32_t)((g / kStages) & 1) ^ 1, false, ab, 1, it)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          mbar_expect_tx(bar(B_FULL + s), kStageBytes);
-          tma_load_3d(stage_addr(s), &tmap, (int)crank * kHs + b * kBk, 0, y, bar(B_FULL + s));
+          mbar_expect_tx(bar(B_FULL + s), G::kRing);
+          tma_load_3d(stage_addr(s), &tmap, (int)crank * G::kHs + b * kBk, 0, y, bar(B_FULL + s));
+          // streamed build: the block's fn tile lands in the same stage (image
+          // blocks 10 crank + b: this CTA's 2560 k)
+          if (G::kStream)
+            bulk_load(stage_addr(s) + kStageBytes,
+                      a.fn_img + ((size_t)crank * G::kHb + b) * kFnBlkBytes, kFnBlkBytes,
+                      bar(B_FULL + s));
         }
         __syncwarp();
       }
@@ -351,7 +380,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       if (!waitw(bar(B_DEMPTY + buf), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 2, it)) break;
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)(buf * kDCols);
-      for (int b = 0; b < kHb; ++b, ++g) {
+      for (int b = 0; b < G::kHb; ++b, ++g) {
         const int s = g % kStages;
         if (!waitw(bar(B_FULL + s), (uint32_t)((g / kStages) & 1), false, ab, 3, it)) {
           ok = false;
@@ -367,7 +396,8 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
         tc_fence_after();
         if (lane == 0) {
           const uint64_t ad = sw128_desc(stage_addr(s));
-          const uint64_t bd = sw128_desc(sb + C::kOffFn + b * kFnBlkBytes);
+          const uint64_t bd = sw128_desc(G::kStream ? stage_addr(s) + kStageBytes
+                                                    : sb + C::kOffFn + b * kFnBlkBytes);
 #pragma unroll
           for (int kk = 0; kk < kBk / 16; ++kk)
             tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (b | kk) != 0);
@@ -387,7 +417,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     __syncwarp();
     drain1(bar(B_DRAIN), 0);
     // the fn image copies have landed before the CTA may leave
-    if (a.fn_img) drain1(bar(B_FNREADY), 0);
+    if (!G::kStream && a.fn_img) drain1(bar(B_FNREADY), 0);
     __syncwarp();
   } else if (warp >= kRead0 && warp < kRead0 + kReadN) {
     // ---- readout warps: accumulators -> owners' receive buffers -------------
@@ -456,9 +486,10 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       if (lane == 0) mbar_arrive(bar(B_DEMPTY + buf));
       if (!push_ready(it, 7)) break;
       const int rb = it % kNR;
-      const uint32_t owner = (uint32_t)(r >> 1);
+      const uint32_t owner = (uint32_t)(r / G::kOwn);
       const uint32_t dst = mapa(sb + C::kOffRx + (uint32_t)(rb * C::kRxBytes +
-                                                            ((int)crank * kOwn + (r & 1)) * kRec * 4),
+                                                            ((int)crank * G::kOwn + r % G::kOwn) *
+                                                                kRec * 4),
                                 owner);
       const uint32_t rbar = mapa(bar(B_RX + rb), owner);
       // the row's Gram entries from the quad: diagonal, then i < j
@@ -491,10 +522,10 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       __syncwarp();
     }
   } else if (warp >= kOwner0 && warp < kOwner0 + kOwnerN) {
-    // ---- owner warps: finalise rows 2 crank, 2 crank + 1 of every other tile --
+    // ---- owner warps: finalise rows kOwn crank .. + kOwn - 1 of every other
+    // tile, two rows a pass (16 lanes a row)
     const int ow = warp - kOwner0;
     const int sub = lane >> 4, e = lane & 15;    // row of the pair, lane of 16
-    const int n = (int)crank * kOwn + sub;        // tile row
     const float *rx = reinterpret_cast<const float *>(sm + C::kOffRx + ow * C::kRxBytes);
     float *sk = reinterpret_cast<float *>(sm + C::kOffSk);
     const float sc0 = __ldg(a.scale), sc1 = __ldg(a.scale + 1), sc2 = __ldg(a.scale + 2);
@@ -503,87 +534,99 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     const unsigned full = 0xffffffffu;
     for (int it = ow; it < T; it += kOwnerN) {
       const uint32_t use = (uint32_t)(it / kNR);
-      const int64_t grow = (int64_t)(cid + it * ncl) * kTR + n;
       if (!waitw(bar(B_RX + ow), use & 1, true, ab, 10, it)) break;
-      // this row's 34 partials from the 16 CTAs, summed in CTA order: lane e
-      // holds values e, e + 16 and (e < 2) e + 32 of the record
-      float v0 = 0.f, v1 = 0.f, v2 = 0.f;
+      const int bt = it / G::kSkTiles, skb = bt & 1;
+      bool ok = true;
+      for (int pp = 0; pp < G::kPairs; ++pp) {
+        const int own = 2 * pp + sub;               // row among this CTA's kOwn
+        const int n = (int)crank * G::kOwn + own;    // tile row
+        const int64_t grow = (int64_t)(cid + it * ncl) * kTR + n;
+        // this row's 34 partials from the kCl CTAs, summed in CTA order: lane
+        // e holds values e, e + 16 and (e < 2) e + 32 of the record
+        float v0 = 0.f, v1 = 0.f, v2 = 0.f;
 #pragma unroll
-      for (int src = 0; src < kCl; ++src) {
-        const float *rec = rx + (src * kOwn + sub) * kRec;
-        v0 += rec[e];
-        v1 += rec[e + 16];
-        if (e < 2) v2 += rec[e + 32];
-      }
-      // arm the buffer's next phase (tile it + kNR, whose stores can only
-      // come after this tile's gates, which depend on the sums just read)
-      __syncwarp();
-      if (lane == 0) mbar_expect_tx(bar(B_RX + ow), C::kRxBytes);
-      // record: dots 0..23 at 0..23, Gram entries 0..9 at 24..33
-      const int hb = lane & 16;                   // first lane of this row's half
-      auto val = [&](int idx) -> float {          // record value idx of this row
-        const float a0 = __shfl_sync(full, v0, hb + (idx & 15));
-        const float a1 = __shfl_sync(full, v1, hb + ((idx - 16) & 15));
-        const float a2 = __shfl_sync(full, v2, hb + ((idx - 32) & 15));
-        return idx < 16 ? a0 : (idx < 32 ? a1 : a2);
-      };
-      float G[kNGram];
-#pragma unroll
-      for (int p = 0; p < kNGram; ++p) G[p] = val(24 + p);
-      const float ssx = (G[0] + G[1]) + (G[2] + G[3]);
-      const float rsq = rsqrt_nr(fmaf(ssx, 1.0f / (float)kK, a.rms_eps));
-      const float dg = e < 8 ? v0 : 0.f;          // dot e (gates)
-      const float dc = val(8 + e);                // dot 8 + e (comb logit e)
-      float gate = 0.f;
-      if (e < 8) {
-        const float l = fmaf(dg * rsq, e < 4 ? sc0 : sc1, bgate);
-        const float sg = rcp_nr(1.0f + expf(-l));
-        gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
-      }
-      const float lc = fmaf(dc * rsq, sc2, bcomb);
-      float p[kHC];
-#pragma unroll
-      for (int i = 0; i < kHC; ++i) p[i] = __shfl_sync(full, gate, hb + i);
-      // sum_h y^2 = p^T G p in a fixed order, clamped at 0 against rounding
-      const float diag = fmaf(p[3] * p[3], G[3], fmaf(p[2] * p[2], G[2],
-                              fmaf(p[1] * p[1], G[1], (p[0] * p[0]) * G[0])));
-      float off = (p[0] * p[1]) * G[4];
-      off = fmaf(p[0] * p[2], G[5], off);
-      off = fmaf(p[0] * p[3], G[6], off);
-      off = fmaf(p[1] * p[2], G[7], off);
-      off = fmaf(p[1] * p[3], G[8], off);
-      off = fmaf(p[2] * p[3], G[9], off);
-      const float ssy = fmaxf(fmaf(2.0f, off, diag), 0.f);
-      const float rn = rsqrt_nr(fmaf(ssy, 1.0f / (float)kH, a.norm_eps));
-      // broadcast this row's pre gates and 1/rms(y): lane e -> CTA e, 32
-      // bytes counted on that CTA's gate barrier
-      {
-        const uint32_t gbuf = (uint32_t)(it % kNG);
-        const uint32_t dst = mapa(sb + C::kOffGin + gbuf * C::kGinBytes + (uint32_t)(n * 32),
-                                  (uint32_t)e);
-        const uint32_t gbar = mapa(bar(B_GIN) + 8u * gbuf, (uint32_t)e);
-        st_async_v4(dst, p[0], p[1], p[2], p[3], gbar);
-        st_async_v4(dst + 16, rn, 0.f, 0.f, 0.f, gbar);
-      }
-      // outputs of the row: post, optional pre and mixes
-      if (grow < a.rows) {
-        if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
-        if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
-        if (a.mix_out) {
-          a.mix_out[grow * kMix + e] = v0 * rsq;
-          if (e < 8) a.mix_out[grow * kMix + 16 + e] = v1 * rsq;
+        for (int src = 0; src < kCl; ++src) {
+          const float *rec = rx + (src * G::kOwn + own) * kRec;
+          v0 += rec[e];
+          v1 += rec[e + 16];
+          if (e < 2) v2 += rec[e + 32];
         }
+        // once every row is read, arm the buffer's next phase (tile it + kNR,
+        // whose stores can only come after this tile's gates, which depend on
+        // the sums just read)
+        __syncwarp();
+        if (pp == G::kPairs - 1 && lane == 0) mbar_expect_tx(bar(B_RX + ow), C::kRxBytes);
+        // record: dots 0..23 at 0..23, Gram entries 0..9 at 24..33
+        const int hb = lane & 16;                   // first lane of this row's half
+        auto val = [&](int idx) -> float {          // record value idx of this row
+          const float a0 = __shfl_sync(full, v0, hb + (idx & 15));
+          const float a1 = __shfl_sync(full, v1, hb + ((idx - 16) & 15));
+          const float a2 = __shfl_sync(full, v2, hb + ((idx - 32) & 15));
+          return idx < 16 ? a0 : (idx < 32 ? a1 : a2);
+        };
+        float G2[kNGram];
+#pragma unroll
+        for (int q = 0; q < kNGram; ++q) G2[q] = val(24 + q);
+        const float ssx = (G2[0] + G2[1]) + (G2[2] + G2[3]);
+        const float rsq = rsqrt_nr(fmaf(ssx, 1.0f / (float)kK, a.rms_eps));
+        const float dg = e < 8 ? v0 : 0.f;          // dot e (gates)
+        const float dc = val(8 + e);                // dot 8 + e (comb logit e)
+        float gate = 0.f;
+        if (e < 8) {
+          const float l = fmaf(dg * rsq, e < 4 ? sc0 : sc1, bgate);
+          const float sg = rcp_nr(1.0f + expf(-l));
+          gate = e < 4 ? sg + a.pre_eps : a.post_mult * sg;
+        }
+        const float lc = fmaf(dc * rsq, sc2, bcomb);
+        float p[kHC];
+#pragma unroll
+        for (int i = 0; i < kHC; ++i) p[i] = __shfl_sync(full, gate, hb + i);
+        // sum_h y^2 = p^T G p in a fixed order, clamped at 0 against rounding
+        const float diag = fmaf(p[3] * p[3], G2[3], fmaf(p[2] * p[2], G2[2],
+                                fmaf(p[1] * p[1], G2[1], (p[0] * p[0]) * G2[0])));
+        float off = (p[0] * p[1]) * G2[4];
+        off = fmaf(p[0] * p[2], G2[5], off);
+        off = fmaf(p[0] * p[3], G2[6], off);
+        off = fmaf(p[1] * p[2], G2[7], off);
+        off = fmaf(p[1] * p[3], G2[8], off);
+        off = fmaf(p[2] * p[3], G2[9], off);
+        const float ssy = fmaxf(fmaf(2.0f, off, diag), 0.f);
+        const float rn = rsqrt_nr(fmaf(ssy, 1.0f / (float)kH, a.norm_eps));
+        // broadcast this row's pre gates and 1/rms(y): lane e -> CTA e, 32
+        // bytes counted on that CTA's gate barrier
+        if (e < kCl) {
+          const uint32_t gbuf = (uint32_t)(it % kNG);
+          const uint32_t dst = mapa(sb + C::kOffGin + gbuf * C::kGinBytes + (uint32_t)(n * 32),
+                                    (uint32_t)e);
+          const uint32_t gbar = mapa(bar(B_GIN) + 8u * gbuf, (uint32_t)e);
+          st_async_v4(dst, p[0], p[1], p[2], p[3], gbar);
+          st_async_v4(dst + 16, rn, 0.f, 0.f, 0.f, gbar);
+        }
+        // outputs of the row: post, optional pre and mixes
+        if (grow < a.rows) {
+          if (e >= 4 && e < 8) a.post[grow * kHC + (e - 4)] = gate;
+          if (a.pre_out && e < 4) a.pre_out[grow * kHC + e] = gate;
+          if (a.mix_out) {
+            a.mix_out[grow * kMix + e] = v0 * rsq;
+            if (e < 8) a.mix_out[grow * kMix + 16 + e] = v1 * rsq;
+          }
+        }
+        // queue the comb logits for the Sinkhorn warp (row kOwn (it %
+        // kSkTiles) + own of batch it / kSkTiles)
+        if (pp == 0 &&
+            !waitw(bar(B_SKFREE + skb), (uint32_t)((bt >> 1) & 1) ^ 1, false, ab, 8, it)) {
+          ok = false;
+          break;
+        }
+        sk[skb * (kSkRows * 16) + ((it % G::kSkTiles) * G::kOwn + own) * 16 + e] = lc;
+        __syncwarp();
       }
-      // queue the comb logits for the Sinkhorn warp (row 2 (it % 16) + sub of
-      // batch it / 16); the last tile completes its batch's count
-      const int bt = it / kSkTiles, skb = bt & 1;
-      if (!waitw(bar(B_SKFREE + skb), (uint32_t)((bt >> 1) & 1) ^ 1, false, ab, 8, it)) break;
-      sk[skb * (kSkRows * 16) + ((it % kSkTiles) * kOwn + sub) * 16 + e] = lc;
-      __syncwarp();
+      if (!ok) break;
+      // the tile's rows are queued; the last tile completes its batch's count
       if (lane == 0) {
         mbar_arrive(bar(B_SKFULL + skb));
         if (it == T - 1)
-          for (int k = it % kSkTiles + 1; k < kSkTiles; ++k) mbar_arrive(bar(B_SKFULL + skb));
+          for (int k = it % G::kSkTiles + 1; k < G::kSkTiles; ++k) mbar_arrive(bar(B_SKFULL + skb));
       }
     }
   } else if (warp == kSinkWarp) {
@@ -593,13 +636,13 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     // (rcp_nr: no branch, so a step's four reciprocals overlap; an IEEE
     // division or reciprocal per sum serialised them, 8 us a batch).
     const float *sk = reinterpret_cast<const float *>(sm + C::kOffSk);
-    const int nb = (T + kSkTiles - 1) / kSkTiles;
+    const int nb = (T + G::kSkTiles - 1) / G::kSkTiles;
     const int r = lane & (kSkRows - 1);
-    const int tl = r / kOwn, sub = r % kOwn;     // tile within the batch, row of the pair
+    const int tl = r / G::kOwn, sub = r % G::kOwn;   // tile within the batch, row of the CTA's
     for (int bt = 0; bt < nb; ++bt) {
       const int skb = bt & 1;
       if (!waitw(bar(B_SKFULL + skb), (uint32_t)((bt >> 1) & 1), false, ab, 9, bt)) break;
-      const int tile = bt * kSkTiles + tl;
+      const int tile = bt * G::kSkTiles + tl;
       const bool valid = lane < kSkRows && tile < T;
       // lanes without a row run on ones: a zero matrix would send every
       // division down its slow path (0 / d)
@@ -625,7 +668,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
           for (int j = 0; j < kHC; ++j) c[j][i] = c[j][i] * d;
         }
       }
-      const int64_t grow = (int64_t)(cid + tile * ncl) * kTR + (int)crank * kOwn + sub;
+      const int64_t grow = (int64_t)(cid + tile * ncl) * kTR + (int)crank * G::kOwn + sub;
       if (valid && grow < a.rows) {
         float4 *o = reinterpret_cast<float4 *>(a.comb + grow * 16);
 #pragma unroll
@@ -634,12 +677,12 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     }
   } else {
     // ---- combine warps: x_norm of the CTA's columns, read back from L2 ------
-    // thread t: 16-byte chunk cq = t % 40 of the CTA's 320 columns, tile rows
-    // t / 40 + 8 u (u = 0..3)
+    // thread t: 16-byte chunk cq = t % kChunks of the CTA's kHs columns, tile
+    // rows t / kChunks + kCombRowStep u
     const int t = (warp - kComb0) * 32 + lane;
-    const int cq = t % kChunks, r0 = t / kChunks;
+    const int cq = t % G::kChunks, r0 = t / G::kChunks;
     const float *gin = reinterpret_cast<const float *>(sm + C::kOffGin);
-    const int64_t col = (int64_t)crank * kHs + 8 * cq;
+    const int64_t col = (int64_t)crank * G::kHs + 8 * cq;
     float wf[8];
     unpack8(__ldg(reinterpret_cast<const uint4 *>(a.norm_w + col)), wf);
     for (int it = 0; it < T; ++it) {
@@ -650,7 +693,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       // the shared-memory / L1 data path the MMAs and TMA also use
       uint4 rv[2][kHC];
       auto load = [&](int u, uint4 (&dst)[kHC]) {
-        const int64_t grow = row0 + r0 + kCombRowStep * u;
+        const int64_t grow = row0 + r0 + G::kCombRowStep * u;
         if (grow < a.rows) {
           const uint4 *src = reinterpret_cast<const uint4 *>(a.R + grow * kK + col);
 #pragma unroll
@@ -661,9 +704,9 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
         }
       };
 #pragma unroll
-      for (int u = 0; u < kCombItems; ++u) {
+      for (int u = 0; u < G::kCombItems; ++u) {
         load(u, rv[u & 1]);
-        const float *gr = gin + buf * (kTR * 8) + (r0 + kCombRowStep * u) * 8;
+        const float *gr = gin + buf * (kTR * 8) + (r0 + G::kCombRowStep * u) * 8;
         const float4 pq = *reinterpret_cast<const float4 *>(gr);
         const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
         const float rn = gr[4];
@@ -678,7 +721,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
           v[e] = (acc * rn) * wf[e];
         }
         const uint4 xb = pack8_rn(v);
-        const int64_t grow = row0 + r0 + kCombRowStep * u;
+        const int64_t grow = row0 + r0 + G::kCombRowStep * u;
         const bool live = grow < a.rows;
         if (live) st_stream(reinterpret_cast<uint4 *>(a.x_norm + grow * kH + col), xb);
         if constexpr (kMx) {
@@ -720,21 +763,22 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
 // ---- host side -------------------------------------------------------------------
 constexpr int kMaxDev = 64;
 std::mutex g_dev_mu;
-template <bool kMx>
+template <bool kMx, int kCl>
 int g_max_clusters[kMaxDev];   // 0: not yet configured on that device
 
-template <bool kMx>
+template <bool kMx, int kCl>
 cudaError_t configure(int dev, int *max_clusters) {
   std::lock_guard<std::mutex> lock(g_dev_mu);
-  if (g_max_clusters<kMx>[dev] > 0) {
-    *max_clusters = g_max_clusters<kMx>[dev];
+  if (g_max_clusters<kMx, kCl>[dev] > 0) {
+    *max_clusters = g_max_clusters<kMx, kCl>[dev];
     return cudaSuccess;
   }
-  constexpr int kSmemBytes = Cfg<kMx>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(pre_onepass_kernel<kMx>,
+  constexpr int kSmemBytes = Cfg<kMx, kCl>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(pre_onepass_kernel<kMx, kCl>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pre_onepass_kernel<kMx>,
+  // a cluster of 16 is a non-portable size
+  if (e == cudaSuccess && kCl > 8)
+    e = cudaFuncSetAttribute(pre_onepass_kernel<kMx, kCl>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -749,15 +793,15 @@ cudaError_t configure(int dev, int *max_clusters) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, pre_onepass_kernel<kMx>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, pre_onepass_kernel<kMx, kCl>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
-  g_max_clusters<kMx>[dev] = n;
+  g_max_clusters<kMx, kCl>[dev] = n;
   *max_clusters = n;
   return cudaSuccess;
 }
 
-template <bool kMx>
+template <bool kMx, int kCl>
 cudaError_t launch(const OnePassArgs &a, int64_t logical_rows, cudaStream_t s) {
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -766,7 +810,7 @@ cudaError_t launch(const OnePassArgs &a, int64_t logical_rows, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   int max_clusters = 0;
-  e = configure<kMx>(dev, &max_clusters);
+  e = configure<kMx, kCl>(dev, &max_clusters);
   if (e != cudaSuccess) return e;
 
   // R as a 3-D tensor (hidden column, stream, row): a box of 64 columns x
@@ -786,31 +830,32 @@ cudaError_t launch(const OnePassArgs &a, int64_t logical_rows, cudaStream_t s) {
   // depend on it at all)
   const int64_t chunk_tiles = (logical_rows + kTR - 1) / kTR;
   const int clusters = (int)(chunk_tiles < max_clusters ? chunk_tiles : max_clusters);
-  return launch_pdl(pre_onepass_kernel<kMx>, dim3((unsigned)(clusters * kCl)), dim3(kThreads),
-                    Cfg<kMx>::kSmemBytes, s, kCl, use_pdl(logical_rows), map, a);
+  return launch_pdl(pre_onepass_kernel<kMx, kCl>, dim3((unsigned)(clusters * kCl)),
+                    dim3(kThreads), Cfg<kMx, kCl>::kSmemBytes, s, kCl, use_pdl(logical_rows),
+                    map, a);
 }
 
-// ---- prepared weights: fn's B tiles of every cluster rank ----------------------
+// ---- prepared weights: fn's B tiles of every image rank ------------------------
 // [16 ranks][5 blocks][192 rows][64 k] bf16 in the kernel's shared-memory
-// layout, written once by mhc_prepare_weights
+// layout, written once by mhc_prepare_weights (or into mhc_pre's workspace)
 __global__ void __launch_bounds__(256) fn_b_img_kernel(const float *__restrict__ fn,
                                                        uint8_t *__restrict__ img) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x * 256 + threadIdx.x;
-  if (t >= kCl * kFnItems) return;
-  const int rank = t / kFnItems, item = t % kFnItems;
+  if (t >= kImgRanks * kImgItems) return;
+  const int rank = t / kImgItems, item = t % kImgItems;
   const int q = item & 7, c = (item >> 3) % kMix, j = (item / (8 * kMix)) % kHC,
             b = item / (8 * kMix * kHC);
-  fn_b_item(fn, rank, b, j, c, q, img + ((size_t)rank * kHb + b) * kFnBlkBytes);
+  fn_b_item(fn, rank, b, j, c, q, img + ((size_t)rank * kImgHb + b) * kFnBlkBytes);
 }
 
 }  // namespace
 
-size_t fn_b_img_bytes() { return (size_t)kCl * kHb * kFnBlkBytes; }
+size_t fn_b_img_bytes() { return (size_t)kImgRanks * kImgHb * kFnBlkBytes; }
 
 cudaError_t launch_fn_b_img(const float *fn, uint8_t *img, cudaStream_t s) {
-  constexpr int kItems = kCl * kFnItems;
+  constexpr int kItems = kImgRanks * kImgItems;
   return launch_pdl(fn_b_img_kernel, dim3((kItems + 255) / 256), dim3(256), 0, s, 1, false, fn,
                     img);
 }
@@ -828,8 +873,15 @@ cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t
   a.num_tiles = (int)((rows + kTR - 1) / kTR);
   a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.sink_eps = p.hc_sinkhorn_eps;
   a.post_mult = p.post_mult; a.norm_eps = p.norm_eps; a.iters = p.sinkhorn_iters;
-  if (mx_q) return launch<true>(a, logical_rows, s);
-  return launch<false>(a, logical_rows, s);
+  // chunks of kStreamMinRows rows and more take the streamed build when fn's
+  // image is at hand (the choice depends on logical_rows, so every shard of
+  // a chunk takes the same build)
+  if (fn_img && logical_rows >= kStreamMinRows) {
+    if (mx_q) return launch<true, 8>(a, logical_rows, s);
+    return launch<false, 8>(a, logical_rows, s);
+  }
+  if (mx_q) return launch<true, 16>(a, logical_rows, s);
+  return launch<false, 16>(a, logical_rows, s);
 }
 
 cudaError_t onepass_error_where(unsigned int *out64) {

@@ -98,11 +98,14 @@ const char *mhc_strerror(int code);
 const char *mhc_last_cuda_error(void);
 
 /* Bytes of device scratch mhc_pre, mhc_hc_head and mhc_fused_post_pre take
- * for a call on `rows` rows: the pre gates [rows, 4] fp32 and the comb logits
- * [rows, 16] fp32 that a two-launch path hands from its tensor-core launch to
- * its streaming combine, each rounded up to 256 bytes (0 for rows <= 0).
- * mhc_fused_post_pre uses it; this build's mhc_pre and mhc_hc_head kernels
- * use none of it. */
+ * for a call on `rows` rows (0 for rows <= 0): the larger of
+ *   - fn's operand image, 1,966,080 bytes: mhc_pre writes it there for a
+ *     chunk of 2048 rows or more (logical_rows), whose one-pass launch
+ *     streams it (see mhc_pre);
+ *   - the pre gates [rows, 4] fp32 and the comb logits [rows, 16] fp32 that
+ *     mhc_fused_post_pre's tensor-core launch hands its combine launch, each
+ *     rounded up to 256 bytes.
+ * mhc_hc_head and the decode-size paths use none of it. */
 size_t mhc_pre_workspace_bytes(int64_t rows);
 
 /* Read libmhc's device status word on the current device into *status: 0,
@@ -141,15 +144,19 @@ int mhc_kernel_status_detail(uint32_t *where64);
  * prefill_sp.py, _combine_norm_fused, requires.)
  *
  * Chunks of more than 48 rows (logical_rows > 48) take one launch that reads
- * R from HBM once (pre_onepass.cu): a cluster of 16 CTAs splits each 32-row
+ * R from HBM once (pre_onepass.cu): a cluster of CTAs splits each 32-row
  * tile by hidden columns, streams R with TMA, runs the 24 projections and each
  * row's 4x4 stream Gram matrix on the tensor cores (fn split into bf16 hi +
  * lo), exchanges the partial sums between the CTAs of the cluster, finalises
  * gates, Sinkhorn and 1/rms(y) = 1/sqrt(p^T G p / 5120 + norm_eps), and
- * combines the tile's columns again from L2.  Decode-size chunks
- * (logical_rows <= 48) take one latency-shaped launch (pre_decode.cu): 16-CTA
- * clusters of CUDA-core work, up to 8 rows per cluster pass.  Neither path
- * touches the workspace.
+ * combines the tile's columns again from L2.  Below 2048 logical rows the
+ * clusters have 16 CTAs that hold fn's operand tiles in shared memory; from
+ * 2048 rows on they have 8 CTAs (144 SMs busy instead of 112) that stream
+ * fn's tiles from an image beside R, and the call first writes that image
+ * (a conversion launch) into the workspace.  Decode-size chunks
+ * (logical_rows <= 48) take one latency-shaped launch (pre_decode.cu):
+ * 16-CTA clusters of CUDA-core work, a group of up to 8 rows per cluster;
+ * they do not touch the workspace.
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual rows
@@ -161,9 +168,8 @@ int mhc_kernel_status_detail(uint32_t *where64);
  *   workspace, workspace_bytes  device scratch of at least
  *            mhc_pre_workspace_bytes(rows) bytes, 256-byte aligned; its
  *            contents on entry do not matter; the call owns it until the
- *            stream reaches the end of the call.  It is validated (and may be
- *            used by a later build); this build's kernels leave it untouched,
- *            and mhc_pre_noalloc is the same call without it.
+ *            stream reaches the end of the call.  Written (fn's image) only
+ *            by chunks of 2048 rows or more.
  * Outputs (fp32 unless stated)
  *   x_norm   [rows, 5120] bf16         normalised combine (sublayer input)
  *   post     [rows, 4]                 post gate
@@ -187,9 +193,13 @@ int mhc_pre(const uint16_t *R, const float *fn, const float *scale, const float 
  * with no device allocator.
  *
  * Same arguments, outputs and validation as mhc_pre, minus the workspace.
- * mhc_pre's kernels take no scratch, so this runs exactly mhc_pre's launches
- * (the decode-size launch up to 48 logical rows, the one-pass launch above)
- * and gives mhc_pre's bits.  It allocates nothing (no cudaMalloc, no cudaFree,
+ * Below 2048 logical rows it runs exactly mhc_pre's launches (the
+ * decode-size launch up to 48 logical rows, the one-pass launch above) and
+ * gives mhc_pre's bits.  From 2048 rows on, with no scratch for fn's image,
+ * it runs the one-pass launch that keeps fn's tiles resident (16-CTA
+ * clusters): the same outputs to within fp32 summation order (the oracle's
+ * tolerances), and every row range of a chunk still gives the whole-chunk
+ * bits.  It allocates nothing (no cudaMalloc, no cudaFree,
  * no allocating library call) and holds no state between calls, so calls on
  * any streams or host threads may overlap.  mhc_pre_noalloc_max_rows()
  * returns the library-wide row limit (2^24).
@@ -340,7 +350,7 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
  * the 4 dots in fp32 on the CUDA cores (head_onepass.cu).  The two paths
  * form the dots differently and agree to the gate tolerance; every row
  * range of a chunk gives the whole-chunk bits.  Neither uses the workspace,
- * which is validated as for mhc_pre.
+ * which is validated as for mhc_pre (mhc_pre_workspace_bytes(rows)).
  *
  * Arguments
  *   R        [rows, 4, 5120] bf16      residual after the last layer

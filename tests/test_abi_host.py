@@ -62,11 +62,15 @@ def test_strerror_and_defaults(lib):
     assert p.sinkhorn_iters == 20 and p.post_mult == 2.0
     assert abs(p.rms_eps - 1e-6) < 1e-12 and abs(p.norm_eps - 1e-6) < 1e-12
     assert lib.mhc_pre_workspace_bytes(0) == 0
-    # the pre gates [rows, 4] then the comb logits [rows, 16], fp32, each
-    # 256-byte rounded
-    assert lib.mhc_pre_workspace_bytes(1000) == 16128 + 64000
-    assert lib.mhc_pre_workspace_bytes(1) == 256 + 256
-    assert lib.mhc_pre_workspace_bytes(257) == 4352 + 16640
+    # the larger of fn's operand image (16 ranks x 5 blocks x 192 x 64 bf16,
+    # for mhc_pre's streamed build) and the fused call's hand-off: the pre
+    # gates [rows, 4] then the comb logits [rows, 16], fp32, each 256-byte
+    # rounded
+    img = 16 * 5 * 192 * 64 * 2
+    assert lib.mhc_pre_workspace_bytes(1) == img
+    assert lib.mhc_pre_workspace_bytes(1000) == img
+    assert lib.mhc_pre_workspace_bytes(24576) == img          # hand-off 1966080 too
+    assert lib.mhc_pre_workspace_bytes(30001) == 480256 + 1920256
 
 
 A = 1 << 32          # fake, 256-byte aligned device addresses, far apart

@@ -8,8 +8,9 @@ take no scratch, so it is mhc_pre without the workspace argument.  Checked
 here through the C ABI:
   * against the fp64 oracle element by element, on two calls in a row with
     different sizes and inputs (one-pass launch), and at 8 rows (decode-size
-    launch);
-  * bit-equal to mhc_pre on the same inputs;
+    launch); on sampled rows of a 2100-row chunk (the one-pass build that
+    keeps fn resident, where mhc_pre streams it from its workspace);
+  * bit-equal to mhc_pre on the same inputs below 2048 rows;
   * 4 row shards of a 2048-row chunk (logical_rows = 2048) give the full
     call's bits;
   * the host-side row limit (also covered without a GPU in test_abi_host).
@@ -106,6 +107,32 @@ def test_noalloc_against_the_oracle_two_calls_in_a_row(env, oracle_mod, sizes):
         m.mhc_pre(*args, x_norm=xn, post=post, comb=comb, pre_out=pre, mix_out=mix)
         torch.cuda.synchronize()
         _assert_same_bits(torch, outs, ref, f"noalloc vs mhc_pre at {R.shape[0]} rows")
+
+
+def test_noalloc_above_the_streamed_threshold_against_the_oracle(env, oracle_mod):
+    # 2100 rows: mhc_pre runs the 8-CTA build on fn's image in its workspace;
+    # noalloc, without one, the 16-CTA build with fn resident.  Both meet the
+    # oracle; their bits may differ by summation order.
+    torch, m = env
+    rows = 2100
+    R, W, args = _inputs(torch, rows, 46)
+    outs = _outputs(torch, rows)
+    _noalloc(m, args, outs)
+    ref = _outputs(torch, rows)
+    xn, post, comb, pre, mix = ref
+    m.mhc_pre(*args, x_norm=xn, post=post, comb=comb, pre_out=pre, mix_out=mix)
+    torch.cuda.synchronize()
+    idx = np.r_[0:64, 1000:1064, rows - 64:rows]
+    o = P.oracle_rows_parallel(oracle_mod.pre, R[idx], rows=len(idx), fn=W.fn, scale=W.scale,
+                               base=W.base, w=W.norm_w)
+    for got in (outs, ref):
+        g_xn, g_post, g_comb, g_pre, g_mix = got
+        P.check_mix(g_mix.cpu().numpy()[idx], o["mix"])
+        P.check_gates(g_pre.cpu().numpy()[idx], g_post.cpu().numpy()[idx], o, W.scale, R[idx], W.fn)
+        P.check_abs(g_comb.cpu().numpy()[idx], o["comb"], 1e-6, "comb")
+        P.check_bf16(_bits(torch, g_xn)[idx], o["x_norm"], "x_norm",
+                     term_mag=P.combine_term_magnitude(R[idx], o["pre"], W.norm_w, 1e-6))
+    assert m.mhc_kernel_status() == 0
 
 
 def test_noalloc_row_shards_give_the_whole_chunk_bits(env):
