@@ -9,11 +9,12 @@
 //
 // Unfused, R' is written by hc_post and read back by the stats; here the
 // stats take R' from shared memory where it was just formed, so for them R'
-// costs one write and no read.  A cluster of 16 CTAs owns a 128-row tile at
-// a time and CTA s owns hidden columns [320 s, 320 s + 320) of all four
-// streams.  Per tile
-// and CTA the 320 columns go through in ten "half-sets" of 32 columns, four
-// in flight:
+// costs one write and no read.  A cluster owns a 128-row tile at a time and
+// CTA s owns a contiguous range of hidden columns of all four streams: 320
+// columns in 16-CTA clusters, or, for chunks of 2048 rows and more, 640 in
+// 8-CTA clusters (15 of those fit, 120 SMs, against 7 of 16, 112 SMs).  Per
+// tile and CTA the columns go through in "half-sets" of 32 columns, four in
+// flight:
 //   * a producer thread loads a half-set -- R_0..3 and y, 128 rows x 32
 //     columns each, 64-byte swizzle, 40 KB, by TMA, and the four streams' fn
 //     blocks for those columns (bf16 hi + lo, 12 KB) by bulk copy from an
@@ -29,13 +30,15 @@
 //     stages; the buffer is refilled once those MMAs have completed;
 //   * four readout warps load the accumulator, push each row's 24 partials
 //     and sum of squares to the row's owner CTA, then, as owners, reduce the
-//     16 CTAs' partials in CTA order and write the gates and comb logits.
+//     cluster's partials in CTA order and write the gates and comb logits.
 // The combine + RMSNorm and the Sinkhorn of the next pre then run as the
 // pre pass's streaming launch (pre_simt.cu) on R_out.
 //
 // Every wait is bounded (~2 s); on expiry a CTA raises an abort flag, records
 // the site in this kernel's error word, drains its copies and MMAs, frees its
 // tensor memory and returns.
+#include <type_traits>
+
 #include "mhc_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -48,11 +51,8 @@ __device__ unsigned int g_fpp_where_aborted[32];
 namespace {
 using namespace ptx;
 
-constexpr int kCl = 16;                       // CTAs per cluster (K split)
 constexpr int kTile = 128;                    // rows per tile = UMMA M
-constexpr int kHs = kH / kCl;                 // 320 columns per CTA
 constexpr int kBh = 32;                       // columns per half-set (64-byte rows)
-constexpr int kNh = kHs / kBh;                // 10 half-sets per tile
 constexpr int kN = 2 * kMix;                  // fn hi (24) + lo (24)
 constexpr int kStageBytes = kTile * kBh * 2;  // 8192: one stream (or y), 128 rows x 32
 constexpr int kFnBlkBytes = kN * kBh * 2;     // 3072: fn hi/lo for 32 k (64-byte rows)
@@ -60,7 +60,6 @@ constexpr int kSetBytes = (kHC + 1) * kStageBytes + kHC * kFnBlkBytes;  // R_0..
 constexpr int kBufs = 4;                      // half-sets in flight
 constexpr int kFnBlocks = kK / kBh;           // 640 fn blocks of 32 k
 constexpr int kRw = 28;                       // receive words per row
-constexpr int kOwn = kTile / kCl;             // 8 rows finalised per CTA
 constexpr int kTmemCols = 128;
 
 // warps: 0 TMA producer; 1 MMA; 2..9 converters; 10..13 readout, then owners
@@ -75,10 +74,7 @@ static_assert(kConvN * 32 * kItems == kTile * (kBh / 8), "one item per (row, 8 c
 
 // shared memory (from a 1024-byte aligned base)
 constexpr int kOffBuf = 0;                                    // [kBufs][R_0..3, y, fn x 4]
-constexpr int kOffRecv = kOffBuf + kBufs * kSetBytes;         // [16 src][8 rows][kRw]
-constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;      // [8 rows][kRw]
-constexpr int kOffSs = kOffRed + kOwn * kRw * 4;              // [2][128] sum x^2
-constexpr int kOffBar = kOffSs + 2 * kTile * 4;
+constexpr int kOffRecv = kOffBuf + kBufs * kSetBytes;         // [kCl src][kOwn rows][kRw]
 enum Bar : int {
   B_FULL = 0,                    // [kBufs] a half-set landed (copy bytes)
   B_CONV = B_FULL + kBufs,       // [kBufs] converted to R' (8 converter warps)
@@ -94,9 +90,26 @@ enum Bar : int {
   B_COUNT = B_DRAIN + 1
 };
 static_assert(B_COUNT == 3 * kBufs + 3 * 2 + 5, "barrier slots overlap");
-constexpr int kOffMisc = kOffBar + B_COUNT * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
+
+// Two builds: kCl = 16 CTAs a cluster, 320 columns (10 half-sets) and 8 owned
+// rows a CTA; kCl = 8 (chunks of kStreamMinRows rows and more), 640 columns
+// (20 half-sets) and 16 owned rows: 15 such clusters fit, 120 SMs, where 7
+// 16-CTA clusters hold 112.
+template <int kCl_>
+struct FGeo {
+  static constexpr int kCl = kCl_;                          // CTAs per cluster (K split)
+  static constexpr int kHs = kH / kCl;                      // columns per CTA
+  static constexpr int kNh = kHs / kBh;                     // half-sets per tile
+  static constexpr int kOwn = kTile / kCl;                  // rows finalised per CTA
+  static constexpr int kOwnPasses = kOwn / 8;               // the 128 owner threads take 8 rows a pass
+  static constexpr int kOffRed = kOffRecv + kCl * kOwn * kRw * 4;   // [kOwn rows][kRw]
+  static constexpr int kOffSs = kOffRed + kOwn * kRw * 4;           // [2][128] sum x^2
+  static constexpr int kOffBar = kOffSs + 2 * kTile * 4;
+  static constexpr int kOffMisc = kOffBar + B_COUNT * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kCl == 16 || kCl == 8, "the two builds");
+  static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
+};
 static_assert(kOffBuf % 1024 == 0 && kStageBytes % 1024 == 0 && kFnBlkBytes % 1024 == 0 &&
                   kSetBytes % 1024 == 0, "64-byte swizzle tiles need 512-byte alignment");
 static_assert(kOffRecv % 16 == 0, "");
@@ -121,9 +134,14 @@ struct FusedArgs {
   float rms_eps, pre_eps, post_mult;
 };
 
+template <int kCl>
 __global__ void __launch_bounds__(kThreads, 1)
 post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
                       const __grid_constant__ CUtensorMap map_y, const FusedArgs a) {
+  using F = FGeo<kCl>;
+  constexpr int kHs = F::kHs, kNh = F::kNh, kOwn = F::kOwn;
+  constexpr int kOffRed = F::kOffRed, kOffSs = F::kOffSs, kOffBar = F::kOffBar,
+                kOffMisc = F::kOffMisc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -314,13 +332,12 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
       if (lane == 0) mbar_arrive(bar(B_SSREADY + tb));
     }
   } else {
-    // ---- readout (one thread per tile row), then owners of 8 rows ------------
+    // ---- readout (one thread per tile row), then owners of kOwn rows --------
     const int quarter = warp & 3;               // a warp reads TMEM lanes 32*(warp%4) .. +31
     const int row = 32 * quarter + lane;
     const float *ssbuf = reinterpret_cast<const float *>(sm + kOffSs);
     const int o = (warp - kRead0) * 32 + lane; // owner thread 0..127
-    const int oq = o >> 4, e = o & 15;          // owned row (of 8), lane of 16
-    const int row_t = (int)crank * kOwn + oq;
+    const int oq = o >> 4, e = o & 15;          // owned row (of 8 a pass), lane of 16
     const float *recv = reinterpret_cast<const float *>(sm + kOffRecv);
     float *red = reinterpret_cast<float *>(sm + kOffRed);
     const float sc0 = __ldg(a.scale), sc1 = __ldg(a.scale + 1), sc2 = __ldg(a.scale + 2);
@@ -350,8 +367,8 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
 #pragma unroll
       for (int c = 16; c < 24; ++c) mix[c] = a1[c - 16] + a2[c - 8];
       if (!waitw(bar(B_PFREE), (uint32_t)(t & 1) ^ 1, true, ab, 6, t)) break;
-      const uint32_t dm = mapa(sb + kOffRecv + (uint32_t)(((crank * kOwn + (row & 7)) * kRw) * 4),
-                               (uint32_t)(row >> 3));
+      const uint32_t dm = mapa(sb + kOffRecv + (uint32_t)(((crank * kOwn + (row % kOwn)) * kRw) * 4),
+                               (uint32_t)(row / kOwn));
 #pragma unroll
       for (int v = 0; v < 6; ++v)
         st_cluster_v4(dm + 16 * v, mix[4 * v], mix[4 * v + 1], mix[4 * v + 2], mix[4 * v + 3]);
@@ -364,15 +381,20 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
         if (lane == 0) arrive_all_ctas(bar(B_PREADY), kCl);
         __syncwarp();
       }
-      // ---- as owners: the 16 CTAs' partials of row oq, in CTA order ----------
-      const int64_t grow = (int64_t)(cid + t * ncl) * kTile + row_t;
+      // ---- as owners: the kCl CTAs' partials of rows oq + 8 h, in CTA order ---
       if (!waitw(bar(B_PREADY), (uint32_t)(t & 1), true, ab, 8, t)) break;
-      float acc0 = 0.f, acc1 = 0.f;
+      float acc0[F::kOwnPasses], acc1[F::kOwnPasses];
 #pragma unroll
-      for (int src = 0; src < kCl; ++src) acc0 += recv[(src * kOwn + oq) * kRw + e];
-      if (e + 16 <= kMix) {
+      for (int h = 0; h < F::kOwnPasses; ++h) {
+        const int oq2 = oq + 8 * h;
+        acc0[h] = 0.f;
+        acc1[h] = 0.f;
 #pragma unroll
-        for (int src = 0; src < kCl; ++src) acc1 += recv[(src * kOwn + oq) * kRw + e + 16];
+        for (int src = 0; src < kCl; ++src) acc0[h] += recv[(src * kOwn + oq2) * kRw + e];
+        if (e + 16 <= kMix) {
+#pragma unroll
+          for (int src = 0; src < kCl; ++src) acc1[h] += recv[(src * kOwn + oq2) * kRw + e + 16];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_OPULL));
@@ -381,9 +403,13 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
         if (lane == 0) arrive_all_ctas(bar(B_PFREE), kCl);
         __syncwarp();
       }
-      float *rq = red + oq * kRw;
-      rq[e] = acc0;
-      if (e + 16 <= kMix) rq[e + 16] = acc1;
+#pragma unroll
+      for (int h = 0; h < F::kOwnPasses; ++h) {
+      const int oq2 = oq + 8 * h;
+      const int64_t grow = (int64_t)(cid + t * ncl) * kTile + (int)crank * kOwn + oq2;
+      float *rq = red + oq2 * kRw;
+      rq[e] = acc0[h];
+      if (e + 16 <= kMix) rq[e + 16] = acc1[h];
       __syncwarp();
       const float rsq = rsqrt_nr(fmaf(rq[kMix], 1.0f / (float)kK, a.rms_eps));
       float gate = 0.f;
@@ -404,6 +430,7 @@ post_pre_fused_kernel(const __grid_constant__ CUtensorMap map_r,
         }
       }
       __syncwarp();
+      }
     }
   }
 
@@ -454,18 +481,23 @@ __global__ void __launch_bounds__(256) fn_prep_sw64_kernel(const float *__restri
 }
 
 std::mutex g_fpp_mu;
+template <int kCl>
 int g_fpp_clusters[64];   // per device: co-resident clusters (0: not configured)
 
+template <int kCl>
 cudaError_t fpp_configure(int dev, int *max_clusters) {
   std::lock_guard<std::mutex> lock(g_fpp_mu);
-  if (g_fpp_clusters[dev] > 0) {
-    *max_clusters = g_fpp_clusters[dev];
+  if (g_fpp_clusters<kCl>[dev] > 0) {
+    *max_clusters = g_fpp_clusters<kCl>[dev];
     return cudaSuccess;
   }
-  cudaError_t e = cudaFuncSetAttribute(post_pre_fused_kernel,
+  constexpr int kSmemBytes = FGeo<kCl>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(post_pre_fused_kernel<kCl>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(post_pre_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  // a cluster of 16 is a non-portable size
+  if (e == cudaSuccess && kCl > 8)
+    e = cudaFuncSetAttribute(post_pre_fused_kernel<kCl>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute at[1];
@@ -479,10 +511,10 @@ cudaError_t fpp_configure(int dev, int *max_clusters) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, post_pre_fused_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, post_pre_fused_kernel<kCl>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
-  g_fpp_clusters[dev] = n;
+  g_fpp_clusters<kCl>[dev] = n;
   *max_clusters = n;
   return cudaSuccess;
 }
@@ -523,9 +555,6 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int max_clusters = 0;
-  e = fpp_configure(dev, &max_clusters);
-  if (e != cudaSuccess) return e;
   CUtensorMap map_r, map_y;
   if (!encode_rows(&map_r, R, kK, rows) || !encode_rows(&map_y, y, kH, rows))
     return cudaErrorInvalidValue;
@@ -544,11 +573,21 @@ cudaError_t launch_post_pre_fused(const uint16_t *R, const uint16_t *y, const fl
   a.rows = rows;
   a.num_tiles = (int)((rows + kTile - 1) / kTile);
   a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.post_mult = p.post_mult;
-  // grid from the chunk's row count only (per-row arithmetic never depends on it)
-  const int64_t chunk_tiles = (logical_rows + kTile - 1) / kTile;
-  const int clusters = (int)(chunk_tiles < max_clusters ? chunk_tiles : max_clusters);
-  return launch_pdl(post_pre_fused_kernel, dim3((unsigned)(clusters * kCl)), dim3(kThreads),
-                    kSmemBytes, s, kCl, use_pdl(logical_rows), map_r, map_y, a);
+  // build and grid from the chunk's row count only (per-row arithmetic never
+  // depends on the grid; the build fixes the order of the cross-CTA sums)
+  auto go = [&](auto cl) -> cudaError_t {
+    constexpr int kCl = decltype(cl)::value;
+    int max_clusters = 0;
+    cudaError_t e2 = fpp_configure<kCl>(dev, &max_clusters);
+    if (e2 != cudaSuccess) return e2;
+    const int64_t chunk_tiles = (logical_rows + kTile - 1) / kTile;
+    const int clusters = (int)(chunk_tiles < max_clusters ? chunk_tiles : max_clusters);
+    return launch_pdl(post_pre_fused_kernel<kCl>, dim3((unsigned)(clusters * kCl)),
+                      dim3(kThreads), FGeo<kCl>::kSmemBytes, s, kCl, use_pdl(logical_rows),
+                      map_r, map_y, a);
+  };
+  if (logical_rows >= kStreamMinRows) return go(std::integral_constant<int, 8>());
+  return go(std::integral_constant<int, 16>());
 }
 
 cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset) {
