@@ -152,8 +152,9 @@ def test_fused_full_size_sampled_rows(torch, mhc, oracle_mod):
     _check(torch, oracle_mod, c, g, idx)
 
 
-def test_fused_shards_and_repeat_are_bit_exact(torch, mhc, oracle_mod):
-    rows = 1500
+@pytest.mark.parametrize("rows", [1500, 2048])
+def test_fused_shards_and_repeat_are_bit_exact(torch, mhc, oracle_mod, rows):
+    # 2048 rows: the 8-CTA build (from 2048 logical rows)
     c = Chain(torch, oracle_mod, rows, 33)
     full = c.gpu(torch, mhc)
     again = c.gpu(torch, mhc)

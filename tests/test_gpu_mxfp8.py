@@ -81,8 +81,9 @@ def test_swizzle_matches_oracle(torch, mhc, rows, groups):
     assert np.array_equal(out.cpu().numpy(), oracle.swizzle_128x4(s))
 
 
-@pytest.mark.parametrize("rows", [8, 48, 1500])
+@pytest.mark.parametrize("rows", [8, 48, 1500, 4096])
 def test_pre_mxfp8(torch, mhc, rows):
+    # 4096 rows: the streamed 8-CTA build of the one-pass kernel (from 2048 rows)
     W = synth.weights(10)
     R = _bf(torch, synth.residual(10, rows))
     fn = torch.from_numpy(W.fn).cuda()
@@ -105,18 +106,20 @@ def test_pre_mxfp8(torch, mhc, rows):
     assert mhc.mhc_kernel_status() == 0
 
 
-def test_pre_mxfp8_row_shards(torch, mhc):
-    # 1500 rows as 4 shards of 375 (logical_rows = 1500): every output,
-    # codes and scales included, equals the whole-chunk call's
-    rows, W = 1500, synth.weights(11)
+@pytest.mark.parametrize("rows", [1500, 4096])
+def test_pre_mxfp8_row_shards(torch, mhc, rows):
+    # 4 shards (logical_rows = rows): every output, codes and scales
+    # included, equals the whole-chunk call's
+    W = synth.weights(11)
     R = _bf(torch, synth.residual(11, rows))
     h = mhc.mhc_prepare_weights(torch.from_numpy(W.fn).cuda())
     scale = torch.from_numpy(W.scale).cuda()
     base = torch.from_numpy(W.base).cuda()
     w = _bf(torch, W.norm_w)
     full = mhc.mhc_pre_mxfp8(R, h, scale, base, w)
-    parts = [mhc.mhc_pre_mxfp8(R[r0:r0 + 375], h, scale, base, w, logical_rows=rows)
-             for r0 in range(0, rows, 375)]
+    sh = rows // 4
+    parts = [mhc.mhc_pre_mxfp8(R[r0:r0 + sh], h, scale, base, w, logical_rows=rows)
+             for r0 in range(0, rows, sh)]
     torch.cuda.synchronize()
     for k in range(5):
         assert torch.equal(full[k], torch.cat([p[k] for p in parts])), k
