@@ -9,9 +9,14 @@
 // _combine_norm_fused does it (y kept in fp32, the weight applied before the
 // single cast).
 //
-// Decomposition.  A cluster of 16 CTAs owns a 32-row tile at a time; CTA s
-// owns hidden columns [320 s, 320 s + 320) of all four streams (1280 of a
-// row's 20480 k).
+// Decomposition.  A cluster owns a 32-row tile at a time; CTA s of the
+// cluster owns a contiguous range of hidden columns of all four streams.  Two
+// builds (kCl): 16 CTAs of 320 columns (1280 of a row's 20480 k) with fn's
+// operand tiles resident in shared memory, and, for chunks of kStreamMinRows
+// rows and more when fn's image is given, 8 CTAs of 640 columns that stream
+// fn's tile of each block into the same ring stage as the block of R (the
+// 120 KB of resident fn no longer fill shared memory; 15 such clusters fit,
+// 120 SMs, where 7 of 16 hold 112).
 //   * warp 0 streams the tile's R through a 5-stage ring with TMA: a stage is
 //     one 64-column block of all four streams, a single 3-D box (columns,
 //     streams, rows) that lands as a [128, 64] bf16 tile with the four
@@ -21,8 +26,8 @@
 //   * one thread of warp 1 issues tcgen05.mma with that stage as A (M = 128)
 //     and fn's bf16 hi/lo for the block as B (N = 192: for each stream j, the
 //     hi and lo rows of mix c at 48 j + 2 c and 48 j + 2 c + 1), resident in
-//     shared memory; D[4 r + i][48 j + n] accumulates over the CTA's five
-//     blocks in tensor memory, and only the j = i blocks are used.
+//     shared memory or in the stage; D[4 r + i][48 j + n] accumulates over
+//     the CTA's blocks in tensor memory, and only the j = i blocks are used.
 //   * the same thread issues a second MMA with the stage as both operands
 //     (N = 128): D2[4 r + i][4 r' + j] = sum_h R_i[r][h] R_j[r'][h], whose
 //     diagonal 4x4 blocks are each row's stream Gram matrix
@@ -33,12 +38,13 @@
 //     each lane's own stream block of the accumulator, add hi + lo, sum the
 //     four streams of a row across its four adjacent lanes in a fixed order,
 //     and send each row's 24 partial dots and 10 Gram entries to the CTA
-//     that finalises the row (CTA s owns tile rows 2s, 2s + 1).
-//   * owner warps (one per receive buffer, alternating tiles) sum the 16
-//     partials in CTA order, form rsqrt, the mixes, the gates, the comb logits
-//     and 1/rms(y) = 1/sqrt(p^T G p / 5120 + norm_eps), broadcast the 4 pre
-//     gates and 1/rms(y) of their rows to all 16 CTAs, write post, and queue
-//     the comb logits for the Sinkhorn warp.
+//     that finalises the row (CTA s owns kOwn = 32 / kCl tile rows).
+//   * owner warps (one per receive buffer, alternating tiles) sum the
+//     cluster's partials in CTA order, form rsqrt, the mixes, the gates, the
+//     comb logits and 1/rms(y) = 1/sqrt(p^T G p / 5120 + norm_eps), two rows
+//     a pass, broadcast the 4 pre gates and 1/rms(y) of their rows to every
+//     CTA of the cluster, write post, and queue the comb logits for the
+//     Sinkhorn warp.
 //   * both exchanges are asynchronous remote stores (st.async) counted in
 //     bytes on the receiver's mbarrier, so neither side fences or signals.
 //   * the Sinkhorn warp runs the 4x4 Sinkhorn of 32 queued rows at a time,
