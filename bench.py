@@ -589,7 +589,7 @@ def run_op(args):
         # mhc_pre's bytes plus the codes (1 B per x_norm value) and scales (1 B
         # per 32 values)
         nbytes = M * (PRE_BYTES_ROW + H + H // 32) + PRE_BYTES_CALL
-        launches = 2            # stats + combine; at decode sizes decode kernel + quantizer
+        launches = 1 if M > 48 else 2   # the one-pass launch; at decode sizes decode kernel + quantizer
         metric = "mhc_pre_mxfp8 rows/s (mhc_pre + MXFP8 x_norm) and achieved HBM GB/s"
         workload = (f"M={M} rows: R[M,4,5120] bf16, fn[24,20480] f32 (seed {SEED}), prepared "
                     f"once; mhc_pre_prepared alone: {plain_ms:.4f} ms/step")
@@ -665,10 +665,9 @@ def run_op(args):
                        "graph_us": graph_us, "graph_chain": args.chain},
             "roofline": {"bound": "latency", "algorithmic_bytes_per_step": nbytes,
                          "achieved_gbs_graph": nbytes / (graph_us * 1e-6) / 1e9},
-            # per step: prefill sizes 3 (stats, combine, post) or, fused with fn
-            # prepared, 2 (fused kernel, combine); decode sizes 2, or 1 fused
-            "gpu_launches": ((2 if args.fused else 3) if LM > 48 else (1 if args.fused else 2))
-                            * args.steps * args.chain,
+            # per step: prefill sizes 2 (the one-pass pre, post) or, fused with
+            # fn prepared, 2 (fused kernel, combine); decode sizes 2, or 1 fused
+            "gpu_launches": (2 if LM > 48 else (1 if args.fused else 2)) * args.steps * args.chain,
         }
         print(json.dumps(line), flush=True)
         return
