@@ -1,6 +1,7 @@
 """Decode-size chunks (logical_rows <= 48): mhc_pre runs as one launch of
-16-CTA clusters on the CUDA cores (up to 8 rows per cluster pass, K split over
-the cluster, partials and gates exchanged through distributed shared memory).
+16-CTA clusters on the CUDA cores (a group of up to 8 rows per cluster, K split
+over the cluster; partials, gates and sums of y^2 exchanged by asynchronous
+stores into distributed shared memory, counted on mbarriers).
 Parity against the oracle with the pre pass's tolerances, on both sides of the
 48-row switch, plus the row-shard bits within a decode chunk.
 """

@@ -94,7 +94,7 @@ def test_hc_head_full_size_sampled_rows(torch, mhc, oracle_mod, rows):
     _check(torch, y, pre, mix, R[idx], o, idx)
 
 
-@pytest.mark.parametrize("rows", [256, 2048])    # the one-pass and the two-launch path
+@pytest.mark.parametrize("rows", [256, 2048])    # the <= 256-row kernel and the tile kernel
 def test_hc_head_row_shards_and_repeat_are_bit_exact(torch, mhc, rows):
     R = synth.residual(WL[rows].seed if rows in WL else 50, rows)
     hw = synth.head_weights(2)

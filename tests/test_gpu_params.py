@@ -1,5 +1,7 @@
-"""Non-default scalars on every pre path: the tensor-core stats (> 48 rows),
-the decode-size launch (<= 48 rows) and the fused post->pre, against the
+"""Non-default scalars on every pre path: the one-pass tensor-core launch
+(> 48 rows; its resident 16-CTA build, and its streamed 8-CTA build for chunks
+of 2048 rows and more), the decode-size launch (<= 48 rows) and the fused
+post->pre, against the
 oracle run with the same scalars (deepseek_v4.py, DeepseekV4DecoderLayer.hc_pre
 passes rms_eps, hc_pre_eps, hc_sinkhorn_eps, post_mult and sinkhorn_repeat
 through to the kernels).  Catches a scalar that is accepted but not used."""
@@ -69,15 +71,17 @@ def _oracle(oracle, R, W):
                                   iters=s["iters"])
 
 
-@pytest.mark.parametrize("rows", [8, 200])        # decode-size launch, tensor-core stats
-def test_pre_with_other_scalars(torch, mhc, oracle_mod, rows):
+# decode-size launch; the one-pass launch, resident build; the streamed build
+# (200 rows as a shard of a 2048-row chunk)
+@pytest.mark.parametrize("rows,logical", [(8, 8), (200, 200), (200, 2048)])
+def test_pre_with_other_scalars(torch, mhc, oracle_mod, rows, logical):
     R = synth.residual(70 + rows, rows)
     W = synth.weights(70 + rows)
     pre = torch.empty((rows, HC), dtype=torch.float32, device="cuda")
     mix = torch.empty((rows, MIX), dtype=torch.float32, device="cuda")
     xn, post, comb = mhc.mhc_pre(_bf(torch, R), _f(torch, W.fn), _f(torch, W.scale),
-                                 _f(torch, W.base), _bf(torch, W.norm_w), params=_params(mhc),
-                                 pre_out=pre, mix_out=mix)
+                                 _f(torch, W.base), _bf(torch, W.norm_w), logical_rows=logical,
+                                 params=_params(mhc), pre_out=pre, mix_out=mix)
     torch.cuda.synchronize()
     g = {"x_norm": xn, "post": post, "comb": comb, "pre": pre, "mix": mix}
     _check(torch, g, _oracle(oracle_mod, R, W), R, W)

@@ -9,7 +9,8 @@ buffer: step i + 1's pre writes the buffer that step i's post reads
 (write-after-read), and each post reads what its own pre wrote
 (read-after-write).  Every step's outputs must be bit-identical to the same
 step run alone.  Sizes cover the one-launch decode pre (48 rows), the
-two-launch pre with the attribute (128, 2048) and without it (4096).
+one-pass pre with the attribute (128: the resident 16-CTA build; 2048: the
+streamed 8-CTA build, after its fn-image launch) and without it (4096).
 """
 import numpy as np
 import pytest
