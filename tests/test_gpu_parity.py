@@ -159,8 +159,9 @@ def test_full_size_sampled_rows(torch, mhc, oracle_mod, rows):
 
 
 def test_chunk_larger_than_the_headline_sampled_rows(torch, mhc, oracle_mod):
-    # 40001 rows: 313 tiles over the co-resident clusters (many rounds), a
-    # 65-row last tile, and 1.6 GB of R -- sizes past every workload above
+    # 40001 rows: 1251 tiles of 32 rows over the co-resident clusters of the
+    # streamed build (many rounds), a 1-row last tile, and 1.6 GB of R --
+    # sizes past every workload above
     rows = 40001
     c = Case(torch, rows, 77)
     idx = np.unique(np.concatenate([[0, 127, 128, 20000, rows - 65, rows - 1],
