@@ -695,8 +695,10 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       const int buf = it % kNG;
       if (!waitw(bar(B_GIN + buf), (uint32_t)((it / kNG) & 1), true, ab, 12, it)) break;
       const int64_t row0 = (int64_t)(cid + it * ncl) * kTR;
-      // one row's loads at a time: more in flight only added to the load on
-      // the shared-memory / L1 data path the MMAs and TMA also use
+      // one row's loads at a time in the resident build (more in flight only
+      // added to the load on the shared-memory / L1 data path the MMAs and TMA
+      // also use); two in the streamed build, whose combine walks twice the
+      // columns a tile
       uint4 rv[2][kHC];
       auto load = [&](int u, uint4 (&dst)[kHC]) {
         const int64_t grow = row0 + r0 + G::kCombRowStep * u;
@@ -709,9 +711,16 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
           for (int i = 0; i < kHC; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       };
+      // the streamed build: the next row's loads in flight while this one is
+      // combined
+      if (G::kStream) load(0, rv[0]);
 #pragma unroll
       for (int u = 0; u < G::kCombItems; ++u) {
-        load(u, rv[u & 1]);
+        if (G::kStream) {
+          if (u + 1 < G::kCombItems) load(u + 1, rv[(u + 1) & 1]);
+        } else {
+          load(u, rv[u & 1]);
+        }
         const float *gr = gin + buf * (kTR * 8) + (r0 + G::kCombRowStep * u) * 8;
         const float4 pq = *reinterpret_cast<const float4 *>(gr);
         const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
