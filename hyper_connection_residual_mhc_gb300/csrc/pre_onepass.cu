@@ -698,7 +698,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       // one row's loads at a time in the resident build (more in flight only
       // added to the load on the shared-memory / L1 data path the MMAs and TMA
       // also use); two in the streamed build, whose combine walks twice the
-      // columns a tile
+      // columns a tile, unless it also quantizes (MXFP8), where one is faster
       uint4 rv[2][kHC];
       auto load = [&](int u, uint4 (&dst)[kHC]) {
         const int64_t grow = row0 + r0 + G::kCombRowStep * u;
@@ -713,10 +713,10 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
       };
       // the streamed build: the next row's loads in flight while this one is
       // combined
-      if (G::kStream) load(0, rv[0]);
+      if (G::kStream && !kMx) load(0, rv[0]);
 #pragma unroll
       for (int u = 0; u < G::kCombItems; ++u) {
-        if (G::kStream) {
+        if (G::kStream && !kMx) {
           if (u + 1 < G::kCombItems) load(u + 1, rv[(u + 1) & 1]);
         } else {
           load(u, rv[u & 1]);
