@@ -276,11 +276,11 @@ cudaError_t fused_post_pre_error_word(unsigned int *out, bool reset);
 // all of mhc_pre in one launch that reads R from HBM once (pre_onepass.cu):
 // 32-row tiles, the four streams of a 64-column block as one MMA operand
 // against fn's hi/lo for all four streams, one cluster exchange per tile, the
-// combine re-reading its tile from L2.  Two builds: 16-CTA clusters with fn's
-// tiles resident (fn_img NULL: converted from fn in the kernel; else bulk
-// copied from the image), and, for chunks of kStreamMinRows rows and more
-// with fn_img given, 8-CTA clusters that stream fn's tiles from the image
-// beside each block of R (144 SMs instead of 112).  fn_img: NULL, or fn's
+// combine re-reading its tile from L2.  fn_img NULL: 16-CTA clusters with
+// fn's tiles converted into shared memory by the kernel.  fn_img given:
+// 16-CTA clusters below kStreamMinRows rows and 8-CTA clusters from there on
+// (120 SMs instead of 112), both streaming fn's tile of each block from the
+// image beside the block of R.  fn_img: NULL, or fn's
 // image of fn_b_img_bytes() (then fn is not read).  mx_q / mx_s non-NULL:
 // x_norm's MXFP8 codes [rows, 5120] and linear ue8m0 scales [rows, 160] as
 // well.

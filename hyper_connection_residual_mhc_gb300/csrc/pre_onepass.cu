@@ -10,13 +10,16 @@
 // single cast).
 //
 // Decomposition.  A cluster owns a 32-row tile at a time; CTA s of the
-// cluster owns a contiguous range of hidden columns of all four streams.  Two
-// builds (kCl): 16 CTAs of 320 columns (1280 of a row's 20480 k) with fn's
-// operand tiles resident in shared memory, and, for chunks of kStreamMinRows
-// rows and more when fn's image is given, 8 CTAs of 640 columns that stream
-// fn's tile of each block into the same ring stage as the block of R (the
-// 120 KB of resident fn no longer fill shared memory; 15 such clusters fit,
-// 120 SMs, where 7 of 16 hold 112).
+// cluster owns a contiguous range of hidden columns of all four streams.
+// Builds (kCl, kS): 16 CTAs of 320 columns (1280 of a row's 20480 k) with
+// fn's operand tiles resident in shared memory (no image: converted in the
+// kernel); the same with fn's tile of each block streamed from the image into
+// the ring stage beside the block of R (an image given, fewer than
+// kStreamMinRows rows: no 120 KB copy before the first MMA); and, for chunks
+// of kStreamMinRows rows and more with the image, 8 CTAs of 640 columns,
+// streamed (the 120 KB of resident fn no longer fill shared memory; 15 such
+// clusters fit, 120 SMs, where 7 of 16 hold 112).  All builds of one cluster
+// size do the same arithmetic on the same operand bytes: the same bits.
 //   * warp 0 streams the tile's R through a 5-stage ring with TMA: a stage is
 //     one 64-column block of all four streams, a single 3-D box (columns,
 //     streams, rows) that lands as a [128, 64] bf16 tile with the four
@@ -89,11 +92,10 @@ namespace {
 using namespace ptx;
 
 // ---- geometry -------------------------------------------------------------
-// Two builds.  kCl = 16: a CTA takes 1280 k (320 hidden columns of all four
-// streams) and keeps fn's operand tiles for them resident in shared memory
-// (120 KB); 7 such clusters fit, 112 SMs.  kCl = 8: a CTA takes 2560 k and
-// streams fn's tile of each block from the prepared image beside the block's
-// R box; 18 clusters fit, 144 SMs.
+// kCl = 16: a CTA takes 1280 k (320 hidden columns of all four streams);
+// fn's operand tiles for them stay resident in shared memory (120 KB) or,
+// with kS, stream beside each block of R; 7 such clusters fit, 112 SMs.
+// kCl = 8 (always streamed): a CTA takes 2560 k; 15 clusters fit, 120 SMs.
 constexpr int kBk = 64;                        // hidden columns per box (128-byte rows)
 constexpr int kTR = 32;                        // rows per tile
 constexpr int kSlotBytes = kTR * kBk * 2;      // 4096: one stream's box
@@ -129,10 +131,10 @@ constexpr int kNG = 4;                         // gate buffers (tiles the combin
 constexpr int kSkRows = 32;                    // rows per Sinkhorn batch (one per lane)
 static_assert(kRead0 % 4 == 0, "lane quarters follow warp & 3");
 
-template <int kCl_>
+template <int kCl_, bool kS_ = (kCl_ == 8)>
 struct Geo {
   static constexpr int kCl = kCl_;                 // CTAs per cluster (K split)
-  static constexpr bool kStream = kCl_ == 8;       // fn streamed beside each R box
+  static constexpr bool kStream = kS_;             // fn streamed beside each R box
   static constexpr int kHs = kH / kCl;             // hidden columns per CTA
   static constexpr int kHb = kHs / kBk;            // blocks (stages) per tile
   static constexpr int kOwn = kTR / kCl;           // rows finalised per CTA per tile
@@ -167,9 +169,9 @@ enum Bar : int {
 };
 static_assert(B_COUNT == 2 * kStages + 5 + kNR + 2 * kNG + 6, "barrier slots overlap");
 
-template <bool kMx, int kCl>
+template <bool kMx, int kCl, bool kS>
 struct Cfg {
-  using G = Geo<kCl>;
+  using G = Geo<kCl, kS>;
   static constexpr int kOffFn = 0;                                    // resident build: [5 blocks][192][64] bf16
   static constexpr int kOffStage = G::kStream ? 0 : G::kHb * kFnBlkBytes;   // [5 stages][128 (+ 192 streamed)][64] bf16
   static constexpr int kOffRx = kOffStage + kStages * G::kRing;       // [kNR][kCl src][kOwn rows][36]
@@ -246,11 +248,11 @@ struct OnePassArgs {
 // so 19 warps x 3072 fit the 64 K-register file with one block per SM)
 constexpr int kMaxRegs = 96;
 static_assert(kWarps * ((kMaxRegs * 32 + 511) / 512 * 512) <= 65536, "register budget of one block per SM");
-template <bool kMx, int kCl>
+template <bool kMx, int kCl, bool kS>
 __global__ void __maxnreg__(kMaxRegs)
 pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a) {
-  using G = Geo<kCl>;
-  using C = Cfg<kMx, kCl>;
+  using G = Geo<kCl, kS>;
+  using C = Cfg<kMx, kCl, kS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -778,22 +780,22 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
 // ---- host side -------------------------------------------------------------------
 constexpr int kMaxDev = 64;
 std::mutex g_dev_mu;
-template <bool kMx, int kCl>
+template <bool kMx, int kCl, bool kS>
 int g_max_clusters[kMaxDev];   // 0: not yet configured on that device
 
-template <bool kMx, int kCl>
+template <bool kMx, int kCl, bool kS>
 cudaError_t configure(int dev, int *max_clusters) {
   std::lock_guard<std::mutex> lock(g_dev_mu);
-  if (g_max_clusters<kMx, kCl>[dev] > 0) {
-    *max_clusters = g_max_clusters<kMx, kCl>[dev];
+  if (g_max_clusters<kMx, kCl, kS>[dev] > 0) {
+    *max_clusters = g_max_clusters<kMx, kCl, kS>[dev];
     return cudaSuccess;
   }
-  constexpr int kSmemBytes = Cfg<kMx, kCl>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(pre_onepass_kernel<kMx, kCl>,
+  constexpr int kSmemBytes = Cfg<kMx, kCl, kS>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(pre_onepass_kernel<kMx, kCl, kS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   // a cluster of 16 is a non-portable size
   if (e == cudaSuccess && kCl > 8)
-    e = cudaFuncSetAttribute(pre_onepass_kernel<kMx, kCl>,
+    e = cudaFuncSetAttribute(pre_onepass_kernel<kMx, kCl, kS>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -808,15 +810,15 @@ cudaError_t configure(int dev, int *max_clusters) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, pre_onepass_kernel<kMx, kCl>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, pre_onepass_kernel<kMx, kCl, kS>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
-  g_max_clusters<kMx, kCl>[dev] = n;
+  g_max_clusters<kMx, kCl, kS>[dev] = n;
   *max_clusters = n;
   return cudaSuccess;
 }
 
-template <bool kMx, int kCl>
+template <bool kMx, int kCl, bool kS>
 cudaError_t launch(const OnePassArgs &a, int64_t logical_rows, cudaStream_t s) {
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -825,7 +827,7 @@ cudaError_t launch(const OnePassArgs &a, int64_t logical_rows, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   int max_clusters = 0;
-  e = configure<kMx, kCl>(dev, &max_clusters);
+  e = configure<kMx, kCl, kS>(dev, &max_clusters);
   if (e != cudaSuccess) return e;
 
   // R as a 3-D tensor (hidden column, stream, row): a box of 64 columns x
@@ -845,8 +847,8 @@ cudaError_t launch(const OnePassArgs &a, int64_t logical_rows, cudaStream_t s) {
   // depend on it at all)
   const int64_t chunk_tiles = (logical_rows + kTR - 1) / kTR;
   const int clusters = (int)(chunk_tiles < max_clusters ? chunk_tiles : max_clusters);
-  return launch_pdl(pre_onepass_kernel<kMx, kCl>, dim3((unsigned)(clusters * kCl)),
-                    dim3(kThreads), Cfg<kMx, kCl>::kSmemBytes, s, kCl, use_pdl(logical_rows),
+  return launch_pdl(pre_onepass_kernel<kMx, kCl, kS>, dim3((unsigned)(clusters * kCl)),
+                    dim3(kThreads), Cfg<kMx, kCl, kS>::kSmemBytes, s, kCl, use_pdl(logical_rows),
                     map, a);
 }
 
@@ -888,15 +890,20 @@ cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t
   a.num_tiles = (int)((rows + kTR - 1) / kTR);
   a.rms_eps = p.rms_eps; a.pre_eps = p.hc_pre_eps; a.sink_eps = p.hc_sinkhorn_eps;
   a.post_mult = p.post_mult; a.norm_eps = p.norm_eps; a.iters = p.sinkhorn_iters;
-  // chunks of kStreamMinRows rows and more take the streamed build when fn's
-  // image is at hand (the choice depends on logical_rows, so every shard of
-  // a chunk takes the same build)
+  // with fn's image at hand: chunks of kStreamMinRows rows and more take the
+  // 8-CTA build, smaller ones the 16-CTA build streaming fn (the choice
+  // depends on logical_rows, so every shard of a chunk takes the same build,
+  // and fn's source does not change the bits)
   if (fn_img && logical_rows >= kStreamMinRows) {
-    if (mx_q) return launch<true, 8>(a, logical_rows, s);
-    return launch<false, 8>(a, logical_rows, s);
+    if (mx_q) return launch<true, 8, true>(a, logical_rows, s);
+    return launch<false, 8, true>(a, logical_rows, s);
   }
-  if (mx_q) return launch<true, 16>(a, logical_rows, s);
-  return launch<false, 16>(a, logical_rows, s);
+  if (fn_img) {
+    if (mx_q) return launch<true, 16, true>(a, logical_rows, s);
+    return launch<false, 16, true>(a, logical_rows, s);
+  }
+  if (mx_q) return launch<true, 16, false>(a, logical_rows, s);
+  return launch<false, 16, false>(a, logical_rows, s);
 }
 
 cudaError_t onepass_error_where(unsigned int *out64) {

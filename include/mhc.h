@@ -150,10 +150,12 @@ int mhc_kernel_status_detail(uint32_t *where64);
  * lo), exchanges the partial sums between the CTAs of the cluster, finalises
  * gates, Sinkhorn and 1/rms(y) = 1/sqrt(p^T G p / 5120 + norm_eps), and
  * combines the tile's columns again from L2.  Below 2048 logical rows the
- * clusters have 16 CTAs that hold fn's operand tiles in shared memory; from
- * 2048 rows on they have 8 CTAs (144 SMs busy instead of 112) that stream
- * fn's tiles from an image beside R, and the call first writes that image
- * (a conversion launch) into the workspace.  Decode-size chunks
+ * clusters have 16 CTAs, which convert fn's operand tiles into shared memory
+ * (mhc_pre) or stream them from the prepared image (mhc_pre_prepared); from
+ * 2048 rows on they have 8 CTAs (120 SMs busy instead of 112) that stream
+ * fn's tiles from an image beside R, and mhc_pre first writes that image (a
+ * conversion launch) into the workspace.  Every row's arithmetic is the same
+ * whichever source fn comes from.  Decode-size chunks
  * (logical_rows <= 48) take one latency-shaped launch (pre_decode.cu):
  * 16-CTA clusters of CUDA-core work, a group of up to 8 rows per cluster;
  * they do not touch the workspace.
