@@ -47,7 +47,7 @@ PRE_BYTES_CALL = MIX * K * 4 + H * 2 + 3 * 4 + MIX * 4         # fn, norm_w, sca
 PRE_LAUNCHES, POST_LAUNCHES = 1, 1                             # kernels per call
 KERNEL_SRC = {"mhc_post": ["post.cu", "mhc_common.cuh"],
               "mhc_pre": ["pre_onepass.cu", "tc_ptx.cuh", "mhc_common.cuh"]}
-KERNEL_NAME = {"mhc_post": "post_kernel", "mhc_pre": "pre_onepass_kernel<false, 8>"}
+KERNEL_NAME = {"mhc_post": "post_kernel", "mhc_pre": "pre_onepass_kernel<false, 8, true>"}
 
 
 def peaks():
