@@ -360,7 +360,10 @@ int64_t mhc_pre_noalloc_max_rows(void) { return kMaxRows; }
 
 // Allocation-free mhc_pre: mhc_pre's kernels (the decode-size launch and the
 // one-pass launch) take no scratch, so this is mhc_pre without the workspace
-// argument: the same launches, the same bits.
+// argument.  Below kStreamMinRows logical rows it runs mhc_pre's launches and
+// gives its bits; from there on, with no room for fn's image, the one-pass
+// launch keeps fn's tiles resident (16-CTA clusters) and its bits follow that
+// build's summation order (still the same for every row shard of a chunk).
 int mhc_pre_noalloc(const uint16_t *R, const float *fn, const float *scale, const float *base,
                     const uint16_t *norm_w, int64_t rows, int64_t logical_rows,
                     const mhc_params *p, uint16_t *x_norm, float *post, float *comb,

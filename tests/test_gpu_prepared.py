@@ -70,6 +70,30 @@ def test_prepared_equals_mhc_pre_bits(torch, mhc, rows):
     assert mhc.mhc_kernel_status() == 0
 
 
+@pytest.mark.parametrize("rows", [1500, 4096])
+def test_prepared_row_shards_reproduce_whole_chunk_bits(torch, mhc, rows):
+    # prefill_sp.py, sp_logical_rows / shard_range: rank r of 4 runs rows
+    # [r*M/4, (r+1)*M/4) with the whole chunk's row count as the key; 1500
+    # rows take the 16-CTA streamed build, 4096 the 8-CTA one
+    W = synth.weights(14)
+    R = _bf(torch, synth.residual(14, rows))
+    scale = torch.from_numpy(W.scale).cuda()
+    base = torch.from_numpy(W.base).cuda()
+    w = _bf(torch, W.norm_w)
+    handle = mhc.mhc_prepare_weights(torch.from_numpy(W.fn).cuda())
+    full = _run(torch, lambda pre, mix: mhc.mhc_pre_prepared(R, handle, scale, base, w,
+                                                             pre_out=pre, mix_out=mix), rows)
+    s = rows // 4
+    for r in range(4):
+        lo, hi = r * s, (r + 1) * s
+        got = _run(torch, lambda pre, mix: mhc.mhc_pre_prepared(
+            R[lo:hi], handle, scale, base, w, logical_rows=rows, pre_out=pre, mix_out=mix), s)
+        for k in full:
+            assert torch.equal(got[k], full[k][lo:hi]), (k, r)
+    handle.release()
+    assert mhc.mhc_kernel_status() == 0
+
+
 def test_released_handle_is_refused(torch, mhc):
     W = synth.weights(3)
     handle = mhc.mhc_prepare_weights(torch.from_numpy(W.fn).cuda())
