@@ -44,7 +44,7 @@ def _run(torch, call, rows):
     return {"x_norm": xn, "post": post, "comb": comb, "pre": pre, "mix": mix}
 
 
-@pytest.mark.parametrize("rows", [8, 1500, 4096])
+@pytest.mark.parametrize("rows", [8, 49, 129, 1500, 4096])
 def test_prepared_equals_mhc_pre_bits(torch, mhc, rows):
     W = synth.weights(9)
     R = _bf(torch, synth.residual(9, rows))
