@@ -87,6 +87,25 @@ def test_pre_with_other_scalars(torch, mhc, oracle_mod, rows, logical):
     _check(torch, g, _oracle(oracle_mod, R, W), R, W)
 
 
+# the prepared call: the one-pass launch streaming fn from the handle's image
+# (16-CTA clusters below 2048 logical rows, 8-CTA from there on)
+@pytest.mark.parametrize("rows,logical", [(200, 200), (200, 2048)])
+def test_prepared_pre_with_other_scalars(torch, mhc, oracle_mod, rows, logical):
+    R = synth.residual(80 + rows, rows)
+    W = synth.weights(80 + rows)
+    handle = mhc.mhc_prepare_weights(_f(torch, W.fn))
+    pre = torch.empty((rows, HC), dtype=torch.float32, device="cuda")
+    mix = torch.empty((rows, MIX), dtype=torch.float32, device="cuda")
+    xn, post, comb = mhc.mhc_pre_prepared(_bf(torch, R), handle, _f(torch, W.scale),
+                                          _f(torch, W.base), _bf(torch, W.norm_w),
+                                          logical_rows=logical, params=_params(mhc),
+                                          pre_out=pre, mix_out=mix)
+    torch.cuda.synchronize()
+    handle.release()
+    g = {"x_norm": xn, "post": post, "comb": comb, "pre": pre, "mix": mix}
+    _check(torch, g, _oracle(oracle_mod, R, W), R, W)
+
+
 def test_fused_post_pre_with_other_scalars(torch, mhc, oracle_mod):
     rows = 200
     R = synth.residual(91, rows)
