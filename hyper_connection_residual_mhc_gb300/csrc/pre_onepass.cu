@@ -304,7 +304,7 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     for (int b = 0; b < kNR; ++b) mbar_init(bar(B_RX + b), 1);
     mbar_init(bar(B_D2EMPTY), kReadN);
     // (streamed: no resident tiles to wait for, the phase completes at once)
-    mbar_init(bar(B_FNREADY), G::kStream || a.fn_img ? 1 : kCombN);
+    mbar_init(bar(B_FNREADY), G::kStream ? 1 : kCombN);
     if (G::kStream) mbar_arrive(bar(B_FNREADY));
     mbar_init(bar(B_DRAIN), 1);
     // the byte-counted barriers are armed for their first phase here; each
@@ -321,19 +321,9 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
 
-  // fn's B tiles for this CTA's columns (resident build): from the prepared
-  // image (bulk copies by the MMA warp) or converted by the combine warps
-  if (G::kStream) {
-  } else if (a.fn_img) {
-    if (warp == kMmaWarp && lane == 0) {
-      constexpr uint32_t kImg = G::kHb * kFnBlkBytes, kPart = kImg / 4;
-      static_assert(kImg % 64 == 0 && kImg < (1u << 20), "bulk copies of 16-byte multiples");
-      mbar_expect_tx(bar(B_FNREADY), kImg);
-      const uint8_t *src = a.fn_img + (size_t)crank * kImg;
-      for (int i = 0; i < 4; ++i)
-        bulk_load(sb + C::kOffFn + i * kPart, src + i * kPart, kPart, bar(B_FNREADY));
-    }
-  } else if (warp >= kComb0 && warp < kComb0 + kCombN) {
+  // fn's B tiles for this CTA's columns (resident build, which runs only
+  // without an image): converted by the combine warps
+  if (!G::kStream && warp >= kComb0 && warp < kComb0 + kCombN) {
     const int t = (warp - kComb0) * 32 + lane;
     for (int item = t; item < G::kFnItems; item += kCombT) {
       const int q = item & 7, c = (item >> 3) % kMix, j = (item / (8 * kMix)) % kHC,
@@ -424,8 +414,6 @@ pre_onepass_kernel(const __grid_constant__ CUtensorMap tmap, const OnePassArgs a
     if (lane == 0) tc_commit(bar(B_DRAIN));
     __syncwarp();
     drain1(bar(B_DRAIN), 0);
-    // the fn image copies have landed before the CTA may leave
-    if (!G::kStream && a.fn_img) drain1(bar(B_FNREADY), 0);
     __syncwarp();
   } else if (warp >= kRead0 && warp < kRead0 + kReadN) {
     // ---- readout warps: accumulators -> owners' receive buffers -------------
@@ -902,6 +890,7 @@ cudaError_t launch_pre_onepass(const uint16_t *R, const float *fn, const uint8_t
     if (mx_q) return launch<true, 16, true>(a, logical_rows, s);
     return launch<false, 16, true>(a, logical_rows, s);
   }
+  // the resident build: fn converted inside the kernel, no image
   if (mx_q) return launch<true, 16, false>(a, logical_rows, s);
   return launch<false, 16, false>(a, logical_rows, s);
 }

@@ -3,8 +3,8 @@
 The handle holds a copy of fn and the one-pass kernel's bf16 hi/lo operand image,
 written by a prep kernel through the same conversion routine the kernel uses
 itself, so mhc_pre_prepared must give exactly mhc_pre's bits -- on the decode
-path (which reads the fp32 copy) and on the tensor-core path (which copies
-the image instead of converting fn).
+path (which reads the fp32 copy) and on the tensor-core path (which streams
+fn's tiles from the image instead of converting fn).
 """
 import numpy as np
 import pytest
