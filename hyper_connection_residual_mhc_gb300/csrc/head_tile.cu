@@ -8,31 +8,34 @@
 // stream-major), pre_i = sigmoid(mix_i * scale + base_i) + hc_eps,
 // y = sum_i pre_i R_i, cast once to bf16.
 //
-// With 4 mixes fn's operand tiles take 20 KB of shared memory per CTA, so
+// With 4 mixes fn's operand tiles take 40 KB of shared memory per CTA, so
 // the rest holds a ring deep enough to keep each tile until its gates have
 // come back: the combine reads the tile from shared memory, not again from
 // L2 or HBM.
 //
-// Decomposition.  A cluster of 16 CTAs owns a 32-row tile at a time; CTA s
-// owns hidden columns [320 s, 320 s + 320) of all four streams.
-//   * warp 0 streams each 64-column block of a tile as one 3-D TMA box
-//     (columns, streams, rows) that lands as 128 lines 4 r + i (stream i of
-//     tile row r), 128-byte swizzled, through a 12-stage ring;
+// Decomposition.  A cluster of 8 CTAs owns a 16-row tile at a time; CTA s
+// owns hidden columns [640 s, 640 s + 640) of all four streams.
+//   * warp 0 streams the tile through an 11-stage ring with TMA: a stage is
+//     two 64-column blocks (2 p, 2 p + 1), each a 3-D box (columns, streams,
+//     rows) of 8 KB, landing as lines 64 h + 4 r + i (block 2 p + h, stream i
+//     of tile row r), 128-byte swizzled;
 //   * one thread of warp 1 issues tcgen05.mma with the stage as A (M = 128)
-//     and fn's bf16 hi and lo as B (N = 32: for each stream j, the hi and lo
-//     rows of mix c at 8 j + 2 c and 8 j + 2 c + 1), resident in shared
-//     memory; D[4 r + i][8 j + n] accumulates over the tile's five blocks in
-//     tensor memory, and only the j = i blocks are used;
+//     and fn's bf16 hi and lo for both blocks as B (N = 64: for block half h
+//     and stream j, the hi and lo rows of mix c at 32 h + 8 j + 2 c and
+//     32 h + 8 j + 2 c + 1), resident in shared memory; D[64 h + 4 r + i]
+//     [32 h' + 8 j + n] accumulates over the tile's five stages in tensor
+//     memory, and only the h' = h, j = i blocks are used;
 //   * four sum-of-squares warps (one thread per line) add the squares of
 //     each stage's lines in packed fp32 pairs;
-//   * four readout warps take each line's own stream block of the
-//     accumulator, add hi + lo, sum the four streams of a row in a fixed
-//     order, and send each row's 4 dots and sum of squares to the CTA that
-//     finalises the row (CTA s owns tile rows 2 s, 2 s + 1);
-//   * the owner warp sums the 16 CTAs' records in CTA order, forms rsqrt,
-//     the mixes and the 4 gates, and sends the gates to all 16 CTAs;
+//   * four readout warps (lane quarter q: half q / 2, rows 8 (q % 2) ..)
+//     take each line's own block of the accumulator, add hi + lo, sum the
+//     four streams of a row in a fixed order, and send each row's 4 dots and
+//     sum of squares over that half's columns to the CTA that finalises the
+//     row (CTA s owns tile rows 2 s, 2 s + 1): 16 records a row;
+//   * the owner warp sums the 16 records in (CTA, half) order, forms rsqrt,
+//     the mixes and the 4 gates, and sends the gates to all 8 CTAs;
 //   * eight combine warps, once a tile's gates are in, form y from the
-//     tile's stages in shared memory block by block, freeing each stage as
+//     tile's stages in shared memory stage by stage, freeing each stage as
 //     soon as its values are in registers, and write y.
 // The exchanges are asynchronous remote stores (st.async) counted in bytes on
 // the receiver's mbarrier.  The pushes of tile t wait until this CTA's
@@ -61,27 +64,32 @@ namespace {
 using namespace ptx;
 
 // ---- geometry -------------------------------------------------------------
-constexpr int kCl = 16;                        // CTAs per cluster (K split)
-constexpr int kHs = kH / kCl;                  // 320 hidden columns per CTA
+constexpr int kCl = 8;                         // CTAs per cluster (K split)
+constexpr int kHs = kH / kCl;                  // 640 hidden columns per CTA
 constexpr int kBk = 64;                        // hidden columns per box (128-byte rows)
-constexpr int kHb = kHs / kBk;                 // 5 blocks (stages) per tile
-constexpr int kTR = 32;                        // rows per tile
-constexpr int kM = kHC * kTR;                  // 128: MMA M (line 4 r + i)
+constexpr int kHb = kHs / kBk;                 // 10 blocks per tile
+constexpr int kHalves = 2;                     // blocks per stage: lines 64 h + 4 r + i
+constexpr int kSt = kHb / kHalves;             // 5 stages per tile
+constexpr int kTR = 16;                        // rows per tile
+constexpr int kM = kHalves * kHC * kTR;        // 128: MMA M
 constexpr int kOwn = kTR / kCl;                // 2 rows finalised per CTA per tile
-constexpr int kStageBytes = kM * kBk * 2;      // 16384
-constexpr int kStages = 12;
+constexpr int kHalfBytes = kHC * kTR * kBk * 2;     // 8192: one block of a tile
+constexpr int kStageBytes = kHalves * kHalfBytes;   // 16384
+constexpr int kStages = 11;
 constexpr int kMixes = kHC;                    // hc_head: one mix per stream
 constexpr int kFnRowsPerStream = 2 * kMixes;   // 8: hi and lo of 4 mixes, interleaved
-constexpr int kN = kHC * kFnRowsPerStream;     // 32: MMA N
-constexpr int kFnBlkBytes = kN * kBk * 2;      // 4096: fn's B tile for one block
+constexpr int kNh = kHC * kFnRowsPerStream;    // 32: fn rows of one half
+constexpr int kN = kHalves * kNh;              // 64: MMA N (half h at 32 h)
+constexpr int kFnBlkBytes = kN * kBk * 2;      // 8192: fn's B tile for one stage
 constexpr int kDCols = kN;                     // accumulator columns per buffer
-constexpr int kTmemCols = 64;
+constexpr int kTmemCols = 128;
 constexpr int kRec = 8;                        // pushed record: 4 dots, sum x^2, 3 pad
+constexpr int kSrc = kCl * kHalves;            // records per row: one per CTA and half
 constexpr int kNR = 2, kNG = 2;                // receive and gate buffers
 
-static_assert(kHs % kBk == 0 && kTR % kCl == 0 && kOwn == 2, "");
+static_assert(kHb % kHalves == 0 && kTR % kCl == 0 && kOwn == 2 && kM == 128, "");
 static_assert(2 * kDCols <= kTmemCols, "two accumulators fit in tensor memory");
-static_assert(kStages >= 2 * kHb, "the ring holds the tile being combined and the next one");
+static_assert(kStages >= 2 * kSt, "the ring holds the tile being combined and the next one");
 
 // ---- warp roles -------------------------------------------------------------
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kOwnerWarp = 2;
@@ -93,7 +101,7 @@ constexpr int kCombN = 8, kComb0 = 3;          // kComb0 re-arms the gate barrie
 constexpr int kWarps = 19;
 constexpr int kThreads = kWarps * 32;          // 608
 constexpr int kCombT = kCombN * 32;            // 256
-static_assert(kRead0 % 4 == 0 && kCombT == kTR * (kBk / 8), "one (row, chunk) of a block per combine thread");
+static_assert(kRead0 % 4 == 0 && kCombT == kHalves * kTR * (kBk / 8), "one (half, row, chunk) of a stage per combine thread");
 
 // 96 registers a thread: warp w runs on SM sub-partition w % 4, whose 16 K
 // registers are allocated to a warp in units of 512; 5 warps x 3072 fit
@@ -118,14 +126,14 @@ enum Bar : int {
 static_assert(B_COUNT == 2 * kStages + 8 + kNR + 2 * kNG + 2, "barrier slots overlap");
 
 struct Cfg {
-  static constexpr int kOffFn = 0;                                    // [5 blocks][32][64] bf16
-  static constexpr int kOffStage = kOffFn + kHb * kFnBlkBytes;        // [12][128][64] bf16
+  static constexpr int kOffFn = 0;                                    // [5 stages][64][64] bf16
+  static constexpr int kOffStage = kOffFn + kSt * kFnBlkBytes;        // [11][128][64] bf16
   static constexpr int kOffRx = kOffStage + kStages * kStageBytes;    // [kNR][16 src][2 rows][8]
-  static constexpr int kRxBytes = kCl * kOwn * kRec * 4;
-  static constexpr int kOffGin = kOffRx + kNR * kRxBytes;             // [kNG][32 rows][4]
+  static constexpr int kRxBytes = kSrc * kOwn * kRec * 4;
+  static constexpr int kOffGin = kOffRx + kNR * kRxBytes;             // [kNG][16 rows][4]
   static constexpr int kGinBytes = kTR * kHC * 4;
-  static constexpr int kOffSs = kOffGin + kNG * kGinBytes;            // [2][32 rows] sum x^2
-  static constexpr int kOffBar = kOffSs + 2 * kTR * 4;
+  static constexpr int kOffSs = kOffGin + kNG * kGinBytes;            // [2][2 halves][16 rows] sum x^2
+  static constexpr int kOffBar = kOffSs + 2 * kHalves * kTR * 4;
   static constexpr int kOffMisc = kOffBar + B_COUNT * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;             // slack to align the base
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block limit");
@@ -134,7 +142,7 @@ struct Cfg {
 };
 
 // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// M = 128, N = 32
+// M = 128, N = 64
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) |
                             ((uint32_t)(kM >> 4) << 24);
 
@@ -216,7 +224,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     const int t = comb_index(warp) * 32 + lane;
     for (int item = t; item < kHb * kHC * kMixes * 8; item += kCombT) {
       const int q = item & 7, c = (item >> 3) % kMixes, j = (item / (8 * kMixes)) % kHC,
-                b = item / (8 * kMixes * kHC);
+                b = item / (8 * kMixes * kHC);          // block b = 2 stage + half
       const float4 *src = reinterpret_cast<const float4 *>(a.fn + (int64_t)c * kK + j * kH +
                                                            (int)crank * kHs + b * kBk + 8 * q);
       const float4 f0 = __ldg(src), f1 = __ldg(src + 1);
@@ -229,8 +237,8 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
         hw[e] = pack2_rn(h0, h1);
         lw[e] = pack2_rn(f[2 * e] - h0, f[2 * e + 1] - h1);
       }
-      uint8_t *tile = sm + C::kOffFn + b * kFnBlkBytes;
-      const int nh = kFnRowsPerStream * j + 2 * c;
+      uint8_t *tile = sm + C::kOffFn + (b / kHalves) * kFnBlkBytes;
+      const int nh = kNh * (b % kHalves) + kFnRowsPerStream * j + 2 * c;
       *reinterpret_cast<uint4 *>(tile + sw128_off(nh, q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4 *>(tile + sw128_off(nh + 1, q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
@@ -246,7 +254,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
       const int y = (cid + it * ncl) * kTR;
-      for (int b = 0; b < kHb; ++b, ++g) {
+      for (int b = 0; b < kSt; ++b, ++g) {
         const int s = g % kStages;
         if (!waitw(bar(B_EMPTY + s), (uint32_t)((g / kStages) & 1) ^ 1, false, ab, 1, it)) {
           ok = false;
@@ -254,7 +262,9 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
         }
         if (lane == 0) {
           mbar_expect_tx(bar(B_FULL + s), kStageBytes);
-          tma_load_3d(stage_addr(s), &tmap, (int)crank * kHs + b * kBk, 0, y, bar(B_FULL + s));
+          tma_load_3d(stage_addr(s), &tmap, (int)crank * kHs + 2 * b * kBk, 0, y, bar(B_FULL + s));
+          tma_load_3d(stage_addr(s) + kHalfBytes, &tmap, (int)crank * kHs + (2 * b + 1) * kBk, 0, y,
+                      bar(B_FULL + s));
         }
         __syncwarp();
       }
@@ -275,7 +285,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
       if (!waitw(bar(B_DEMPTY + buf), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 3, it)) break;
       tc_fence_after();
       const uint32_t d = tmem + (uint32_t)(buf * kDCols);
-      for (int b = 0; b < kHb; ++b, ++g) {
+      for (int b = 0; b < kSt; ++b, ++g) {
         const int s = g % kStages;
         if (!waitw(bar(B_FULL + s), (uint32_t)((g / kStages) & 1), false, ab, 4, it)) {
           ok = false;
@@ -308,7 +318,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     bool ok = true;
     for (int it = 0; it < T && ok; ++it) {
       uint64_t acc = 0ull;
-      for (int b = 0; b < kHb; ++b, ++g) {
+      for (int b = 0; b < kSt; ++b, ++g) {
         const int s = g % kStages;
         if (!waitw(bar(B_FULL + s), (uint32_t)((g / kStages) & 1), false, ab, 5, it)) {
           ok = false;
@@ -343,7 +353,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
       v = v + __shfl_xor_sync(0xffffffffu, v, 2);
       const int buf = it & 1;
       if (!waitw(bar(B_SEMPTY + buf), (uint32_t)((it >> 1) & 1) ^ 1, false, ab, 6, it)) break;
-      if ((l & 3) == 0) ss[buf * kTR + (l >> 2)] = v;
+      if ((l & 3) == 0) ss[(buf * kHalves + (l >> 6)) * kTR + ((l & 63) >> 2)] = v;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_SFULL + buf));
     }
@@ -351,8 +361,8 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     // ---- readout warps: the row's 4 dots and sum of squares to its owner -------
     // lane l of quarter q holds line 32 q + l = 4 r + i; its useful columns
     // are 8 i .. 8 i + 7
-    const int quarter = warp & 3;
-    const int i_s = lane & 3, r = 8 * quarter + (lane >> 2);
+    const int quarter = warp & 3, hq = quarter >> 1;   // half of the stage
+    const int i_s = lane & 3, r = 8 * (quarter & 1) + (lane >> 2);
     const float *ss = reinterpret_cast<const float *>(sm + C::kOffSs);
     const unsigned full = 0xffffffffu;
     for (int it = 0; it < T; ++it) {
@@ -361,7 +371,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
       if (!waitw(bar(B_DFULL + buf), use & 1, false, ab, 7, it)) break;
       tc_fence_after();
       float v[32];
-      tc_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kDCols), v);
+      tc_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kDCols + kNh * hq), v);
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -385,7 +395,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
         m[c] = x;
       }
       if (!waitw(bar(B_SFULL + buf), use & 1, false, ab, 8, it)) break;
-      const float sq = ss[buf * kTR + r];
+      const float sq = ss[(buf * kHalves + hq) * kTR + r];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_SEMPTY + buf));
       if (!push_ready(it, 9)) break;
@@ -393,7 +403,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
         const int rb = it % kNR;
         const uint32_t owner = (uint32_t)(r / kOwn);
         const uint32_t dst = mapa(sb + C::kOffRx + (uint32_t)(rb * C::kRxBytes +
-                                                              ((int)crank * kOwn + (r % kOwn)) * kRec * 4),
+                                                              (((int)crank * kHalves + hq) * kOwn + (r % kOwn)) * kRec * 4),
                                   owner);
         const uint32_t rbar = mapa(bar(B_RX + rb), owner);
         st_async_v4(dst, m[0], m[1], m[2], m[3], rbar);
@@ -418,7 +428,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
       float v = 0.f;
       if (e < kRec) {
 #pragma unroll
-        for (int src = 0; src < kCl; ++src)
+        for (int src = 0; src < kSrc; ++src)
           v += rx[rb * (C::kRxBytes / 4) + (src * kOwn + n) * kRec + e];
       }
       __syncwarp();
@@ -431,8 +441,8 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
       float pg[kHC];
 #pragma unroll
       for (int i = 0; i < kHC; ++i) pg[i] = __shfl_sync(full, gate, hb + i);
-      // the row's 4 gates to CTA e (16 bytes counted on its gate barrier)
-      {
+      // the row's 4 gates to CTA e < kCl (16 bytes counted on its gate barrier)
+      if (e < kCl) {
         const uint32_t gbuf = (uint32_t)(it % kNG);
         const uint32_t dst = mapa(sb + C::kOffGin + gbuf * C::kGinBytes +
                                   (uint32_t)(((int)crank * kOwn + n) * kHC * 4),
@@ -447,15 +457,16 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     }
   } else if (is_comb) {
     // ---- combine warps: y of the CTA's columns from the tile's stages --------
-    // block by block, so each stage is handed back as soon as it is combined:
-    // thread t takes row t / 8, chunk t % 8 of the block's 64 columns
+    // stage by stage, so each stage is handed back as soon as it is combined:
+    // thread t takes half t / 128 (block 2 p + half of stage p), row
+    // (t / 8) % 16, chunk t % 8 of that block's 64 columns
     const int t = comb_index(warp) * 32 + lane;
-    const int rr = t >> 3, c8 = t & 7;
+    const int hh = t >> 7, rr = (t >> 3) & (kTR - 1), c8 = t & 7;
     const float *gin = reinterpret_cast<const float *>(sm + C::kOffGin);
     for (int it = 0; it < T; ++it) {
       const int buf = it % kNG;
       if (!waitw(bar(B_GIN + buf), (uint32_t)((it / kNG) & 1), true, ab, 12, it)) break;
-      const int g0 = it * kHb;                    // the tile's first stage
+      const int g0 = it * kSt;                    // the tile's first stage
       const int64_t grow = (int64_t)(cid + it * ncl) * kTR + rr;
       const float4 pq = *reinterpret_cast<const float4 *>(gin + buf * (kTR * kHC) + rr * kHC);
       const float pv[kHC] = {pq.x, pq.y, pq.z, pq.w};
@@ -466,13 +477,13 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
         if (warp == kComb0) mbar_expect_tx(bar(B_GIN + buf), C::kGinBytes);
       }
 #pragma unroll 1
-      for (int b = 0; b < kHb; ++b) {
+      for (int b = 0; b < kSt; ++b) {
         const int s = (g0 + b) % kStages;
         const uint8_t *st = sm + C::kOffStage + s * kStageBytes;
         uint4 rv[kHC];
 #pragma unroll
         for (int i = 0; i < kHC; ++i)
-          rv[i] = *reinterpret_cast<const uint4 *>(st + sw128_off(4 * rr + i, c8));
+          rv[i] = *reinterpret_cast<const uint4 *>(st + sw128_off(64 * hh + 4 * rr + i, c8));
         // the block's values are in registers: hand the stage back
         uint32_t sink = 0;
 #pragma unroll
@@ -491,8 +502,8 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
           yv[e] = acc;
         }
         if (grow < a.rows)
-          st_stream(reinterpret_cast<uint4 *>(a.y + grow * kH + (int64_t)crank * kHs + b * kBk +
-                                              8 * c8),
+          st_stream(reinterpret_cast<uint4 *>(a.y + grow * kH + (int64_t)crank * kHs +
+                                              (2 * b + hh) * kBk + 8 * c8),
                     pack8_rn(yv));
       }
     }
