@@ -345,9 +345,9 @@ int mhc_fused_post_pre(const uint16_t *R, const uint16_t *y, const float *post,
  *   y[m,h] = bf16( sum_i pre[i] * R[m, i, h] )     (fp32 sum, one rounding)
  *
  * One launch that reads R once and combines every row from shared memory.
- * Chunks of more than 256 rows (logical_rows): 16-CTA clusters over 32-row
+ * Chunks of more than 256 rows (logical_rows): 8-CTA clusters over 16-row
  * tiles (head_tile.cu), the 4 dots on the tensor cores against fn split
- * into bf16 hi + lo, the tile kept in a 12-stage shared-memory ring until
+ * into bf16 hi + lo, the tile kept in an 11-stage shared-memory ring until
  * its gates come back.  Chunks of up to 256 rows: 4-CTA clusters that form
  * the 4 dots in fp32 on the CUDA cores (head_onepass.cu).  The two paths
  * form the dots differently and agree to the gate tolerance; every row
