@@ -69,7 +69,7 @@ def _check(torch, y, pre, mix, R, o, idx=None):
     P.check_bf16(sel(_bits(torch, y)), o["y"], "head y", term_mag=_term_mag(R, o["pre"]))
 
 
-@pytest.mark.parametrize("rows", [1, 7, 128, 129, 1500])
+@pytest.mark.parametrize("rows", [1, 7, 128, 129, 257, 1500])
 def test_hc_head_every_row(torch, mhc, oracle_mod, rows):
     seed = WL[rows].seed if rows in WL else 40 + rows
     R = synth.residual(seed, rows)
@@ -92,6 +92,22 @@ def test_hc_head_full_size_sampled_rows(torch, mhc, oracle_mod, rows):
     idx = np.unique(np.concatenate([[0, 127, 128, rows // 2, rows - 1], rng.integers(0, rows, 20)]))
     o = oracle_mod.hc_head(R[idx], hw.fn, hw.scale, hw.base)
     _check(torch, y, pre, mix, R[idx], o, idx)
+
+
+# non-default eps on both kernels: each is passed through, not a constant
+@pytest.mark.parametrize("rows", [100, 700])
+def test_hc_head_other_eps(torch, mhc, oracle_mod, rows):
+    R = synth.residual(60 + rows, rows)
+    hw = synth.head_weights(60 + rows)
+    pre = torch.empty((rows, HC), dtype=torch.float32, device="cuda")
+    mix = torch.empty((rows, HC), dtype=torch.float32, device="cuda")
+    y = mhc.mhc_hc_head(_dev_bf16(torch, R), _dev_f32(torch, hw.fn), _dev_f32(torch, hw.scale),
+                        _dev_f32(torch, hw.base), norm_eps=0.25, hc_eps=0.125, pre_out=pre,
+                        mix_out=mix)
+    torch.cuda.synchronize()
+    o = P.oracle_rows_parallel(oracle_mod.hc_head, R, rows=rows, fn=hw.fn, scale=hw.scale,
+                               base=hw.base, norm_eps=0.25, hc_eps=0.125)
+    _check(torch, y, pre, mix, R, o)
 
 
 @pytest.mark.parametrize("rows", [256, 2048])    # the <= 256-row kernel and the tile kernel
