@@ -116,8 +116,8 @@ enum Bar : int {
   B_DEMPTY = B_DFULL + 2,         // [2] dot accumulator read out
   B_SFULL = B_DEMPTY + 2,         // [2] a tile's sums of squares written
   B_SEMPTY = B_SFULL + 2,         // [2] a tile's sums of squares read
-  B_RX = B_SEMPTY + 2,            // [kNR] the 16 CTAs' records landed (bytes)
-  B_GIN = B_RX + kNR,             // [kNG] the 16 owners' gates landed (bytes)
+  B_RX = B_SEMPTY + 2,            // [kNR] the 16 records of each owned row landed (bytes)
+  B_GIN = B_RX + kNR,             // [kNG] the 8 owners' gates landed (bytes)
   B_GREAD = B_GIN + kNG,          // [kNG] the combine warps have read the tile's gates
   B_FNREADY = B_GREAD + kNG,      // fn's B tiles written
   B_DRAIN = B_FNREADY + 1,        // final MMA drain
@@ -311,7 +311,7 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     drain1(bar(B_DRAIN), 0);
     __syncwarp();
   } else if (warp >= kSq0 && warp < kSq0 + kSqN) {
-    // ---- sum-of-squares warps: line l = 32 (warp - 8) + lane = 4 r + i ---------
+    // ---- sum-of-squares warps: line l = 32 (warp - 8) + lane = 64 h + 4 r + i --
     const int l = 32 * (warp - kSq0) + lane;
     float *ss = reinterpret_cast<float *>(sm + C::kOffSs);
     int g = 0;
@@ -359,8 +359,8 @@ head_tile_kernel(const __grid_constant__ CUtensorMap tmap, const HeadTileArgs a)
     }
   } else if (warp >= kRead0 && warp < kRead0 + kReadN) {
     // ---- readout warps: the row's 4 dots and sum of squares to its owner -------
-    // lane l of quarter q holds line 32 q + l = 4 r + i; its useful columns
-    // are 8 i .. 8 i + 7
+    // lane l of quarter q holds line 32 q + l = 64 h + 4 r + i (h = q / 2);
+    // its useful columns are 32 h + 8 i .. 32 h + 8 i + 7
     const int quarter = warp & 3, hq = quarter >> 1;   // half of the stage
     const int i_s = lane & 3, r = 8 * (quarter & 1) + (lane >> 2);
     const float *ss = reinterpret_cast<const float *>(sm + C::kOffSs);
@@ -575,7 +575,7 @@ cudaError_t launch_head_tile(const uint16_t *R, const float *fn, const float *sc
   if (e != cudaSuccess) return e;
 
   // R as a 3-D tensor (hidden column, stream, row): a box of 64 columns x
-  // 4 streams x 32 rows lands with the four streams of a row adjacent
+  // 4 streams x 16 rows lands with the four streams of a row adjacent
   CUtensorMap map;
   const cuuint64_t gdim[3] = {(cuuint64_t)kH, (cuuint64_t)kHC, (cuuint64_t)rows};
   const cuuint64_t gstride[2] = {(cuuint64_t)kH * 2, (cuuint64_t)kK * 2};
