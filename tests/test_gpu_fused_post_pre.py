@@ -167,7 +167,7 @@ def test_fused_shards_and_repeat_are_bit_exact(torch, mhc, oracle_mod, rows):
             assert torch.equal(part[k], full[k][r * s:(r + 1) * s]), (k, r)
 
 
-@pytest.mark.parametrize("rows", [7, 48, 49, 1500])
+@pytest.mark.parametrize("rows", [7, 48, 49, 1500, 2100])   # 2100: the 8-CTA build, ragged
 def test_fused_mxfp8_against_the_oracle(torch, mhc, oracle_mod, rows):
     # the fused boundary with the next x_norm as MXFP8 (prefill_sp.py,
     # _mxfp8_quantize on the attention input): R_out, x_norm, post and comb
